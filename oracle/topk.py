@@ -1,0 +1,39 @@
+"""Top-K teacher cache extraction, by a full per-row sort.
+
+TEST INFRASTRUCTURE (see the package docstring).
+
+[ART] offline-cache paragraph, [DAI] "As duas inovações" item 1 and [EPO] "Los
+dos cambios propuestos": the teacher is run once and only its K highest logits
+per position (the most probable tokens) are kept, together with their token ids.
+
+Readings: the cache holds the raw logits (not log-probabilities), widened
+exactly from bf16 to fp32; it is ordered by value, highest first; equal values
+are ordered by ascending token id, and the cut at K keeps the lowest ids;
+-0.0 and +0.0 are equal.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from .kl import bf16_to_f64
+
+
+def topk_cache(bits: np.ndarray, K: int):
+    """Per row of a bf16 [N, V] logits array (raw uint16 bits): ids int32 [N, K], logits fp32 [N, K].
+
+    A stable lexicographic sort on (-value, id) per row, then the first K.
+    """
+    bits = np.asarray(bits)
+    assert bits.dtype == np.uint16 and bits.ndim == 2
+    N, V = bits.shape
+    if not (1 <= K <= V):
+        raise ValueError("K must be in [1, V]")
+    ids = np.empty((N, K), dtype=np.int32)
+    vals = np.empty((N, K), dtype=np.float32)
+    col = np.arange(V)
+    for r in range(N):
+        v = bf16_to_f64(bits[r])
+        order = np.lexsort((col, -v))[:K]          # primary key: -value; secondary: id
+        ids[r] = order
+        vals[r] = v[order].astype(np.float32)
+    return ids, vals
