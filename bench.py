@@ -1,0 +1,321 @@
+#!/usr/bin/env python3
+"""Benchmark: fused chunked KL forward + backward on one GB300 (or N replicas).
+
+One step = kd_fused_kl_fwd + kd_fused_kl_bwd over the whole workload (every
+chunk: teacher prologue, projection + online logsumexp, recompute + dZ, the two
+gradient products).  Default workload: the gpt-oss-shaped long context
+(B=1, T=32768, d=2880, V=201088, K=100, chunk=4096).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Prints ONE JSON line (rank 0).  ``--impl reference`` times the float64 CPU
+oracle on a bounded sample of the same workload on this host's cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "fused KL fwd+bwd tokens/s and TFLOP/s vs BF16 peak; peak device GB (1xGB300)"
+UNIT = "tokens/s"
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return dict(bf16_burst=float(p["bf16_tflops"]), bf16_sustained=float(p["bf16_tflops_sustained"]),
+                    hbm=float(p["hbm_gbs"]), source="measured")
+    except Exception:
+        return dict(bf16_burst=1900.0, bf16_sustained=1700.0, hbm=6800.0, source="fallback")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while open."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.lines.append(ln.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.t.join(timeout=2)
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def cpu_oracle_seconds(Hb, Wb, ids, tlog, mask):
+    """Wall time of the float64 oracle (fused formulation, fwd + bwd with full grad_W) on these rows."""
+    import oracle
+    t0 = time.perf_counter()
+    oracle.fused_chunked_kl(Hb, Wb, ids, tlog, mask, 1.0, chunk=Hb.shape[0], vtile=8192)
+    return time.perf_counter() - t0
+
+
+def run_reference(args, w):
+    import torch
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    from synth import bf16_bits, make_inputs
+    cores = len(os.sched_getaffinity(0))
+    rows = args.ref_rows
+    H, W, ids, tlog, mask = make_inputs(w, "cpu", rows=rows)
+    Hb, Wb, idn, tln = bf16_bits(H), bf16_bits(W), ids.numpy(), tlog.numpy()
+    mn = None if mask is None else mask.numpy()
+    times = []
+    for i in range(args.warmup + args.steps):
+        dt = cpu_oracle_seconds(Hb, Wb, idn, tln, mn)
+        if i >= args.warmup:
+            times.append(dt)
+    t = sum(times) / len(times)
+    v = rows / t
+    line = {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "T": w.T, "d": w.d, "V": w.V, "K": w.K, "chunk": w.chunk},
+        "cpu_baseline": {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"{rows} positions of {w.name} per step (float64 numpy, fused formulation, "
+                                   f"fwd+bwd incl. full grad_W), tokens/s extrapolated per position"},
+        "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default="gptoss")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--ref-rows", type=int, default=32)
+    ap.add_argument("--cpu-rows", type=int, default=64)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    from synth import WORKLOADS
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    from sparse_teacher_kl_gb300.build import build_library
+    build_library()
+    import sparse_teacher_kl_gb300 as kd
+    from synth import make_inputs
+
+    peaks = load_peaks()
+    H, W, ids, tlog, mask = make_inputs(w, dev)
+    N, d, V, K, c = w.N, w.d, w.V, w.K, w.chunk
+    ws = kd.workspace(kd._abi.kd_fused_kl_workspace(N, d, V, K, c), dev)
+    grad_H = torch.empty((N, d), dtype=torch.bfloat16, device=dev)
+    grad_W = torch.zeros((V, d), dtype=torch.float32, device=dev)
+    g = torch.ones(1, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        loss, lse, _ = kd.fused_kl_forward(H, W, ids, tlog, mask, c, 1.0, ws=ws)
+        kd.fused_kl_backward(H, W, ids, tlog, mask, lse, g, c, 1.0, ws=ws, grad_H=grad_H, grad_W=grad_W)
+        return loss
+
+    base_alloc = torch.cuda.memory_allocated(dev)
+    torch.cuda.reset_peak_memory_stats(dev)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    peak_alloc = torch.cuda.max_memory_allocated(dev)
+    st, detail = kd.device_error(ws)
+    if st != 0:
+        raise SystemExit(f"device error {st} ({detail}) during warm-up")
+
+    # ---- timed region: inputs resident in HBM (W = V*d*2 bytes, larger than L2)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clocks, kd.Profile(capacity=64 * (args.steps + 1) * (N // c + 2)) as prof:
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    ms = e0.elapsed_time(e1) / args.steps
+    t_max = torch.tensor([ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t_max, op=dist.ReduceOp.MAX)
+    ms = float(t_max.item())
+
+    # per-kernel breakdown from the library's own launch events
+    summ = prof.summary()
+    launches = sum(n for n, _ in summ.values())
+    kernels = {k: {"launches": n, "total_ms": t, "avg_ms": t / n, "share": t / max(1e-9, ms * args.steps)}
+               for k, (n, t) in sorted(summ.items(), key=lambda kv: -kv[1][1])}
+    dom_name = max(summ.items(), key=lambda kv: kv[1][1])[0]
+    dom = kernels[dom_name]
+    gemm_flops_per_chunk = 2.0 * c * d * V
+    if dom_name == "kd_topk_cache":
+        raise SystemExit("unexpected dominant kernel")
+    achieved = gemm_flops_per_chunk / (dom["avg_ms"] * 1e-3) / 1e12
+    peak = peaks["bf16_sustained"]
+
+    tokens_per_s = world * N / (ms * 1e-3)
+    tflops_exec = w.flops_executed() / (ms * 1e-3) / 1e12
+
+    # ---- end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        Hh = H.cpu().pin_memory()
+        idh = ids.cpu().pin_memory()
+        tlh = tlog.cpu().pin_memory()
+        mh = None if mask is None else mask.cpu().pin_memory()
+        lossh = torch.empty(1, dtype=torch.float32).pin_memory()
+        Hd = torch.empty_like(H)
+        idd = torch.empty_like(ids)
+        tld = torch.empty_like(tlog)
+        md = None if mask is None else torch.empty_like(mask)
+        h2d = Hh.numel() * 2 + idh.numel() * 4 + tlh.numel() * 4 + (0 if mh is None else mh.numel())
+
+        def e2e_step():
+            Hd.copy_(Hh, non_blocking=True)
+            idd.copy_(idh, non_blocking=True)
+            tld.copy_(tlh, non_blocking=True)
+            if md is not None:
+                md.copy_(mh, non_blocking=True)
+            loss, lse, _ = kd.fused_kl_forward(Hd, W, idd, tld, md, c, 1.0, ws=ws)
+            kd.fused_kl_backward(Hd, W, idd, tld, md, lse, g, c, 1.0, ws=ws, grad_H=grad_H, grad_W=grad_W)
+            lossh.copy_(loss, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        f0 = torch.cuda.Event(enable_timing=True)
+        f1 = torch.cuda.Event(enable_timing=True)
+        f0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        f1.record(stream)
+        torch.cuda.synchronize(dev)
+        ems = f0.elapsed_time(f1) / args.steps
+        tm = torch.tensor([ems], dtype=torch.float64, device=dev)
+        if world > 1:
+            dist.all_reduce(tm, op=dist.ReduceOp.MAX)
+        ems = float(tm.item())
+        e2e = {"value": world * N / (ems * 1e-3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": 4, "ms_per_step": ems,
+               "note": "pinned host H, teacher cache and mask copied in, loss copied out; W resident"}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        from synth import bf16_bits
+        r = args.cpu_rows
+        dt = cpu_oracle_seconds(bf16_bits(H[:r]), bf16_bits(W), ids[:r].cpu().numpy(), tlog[:r].cpu().numpy(),
+                                None if mask is None else mask[:r].cpu().numpy())
+        rate = r / dt
+        cpu = {"value": rate, "unit": UNIT, "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
+               "sample": f"{args.cpu_rows} positions of {w.name} (float64 numpy, fused formulation, fwd+bwd incl. "
+                         f"full grad_W) in {dt:.1f} s, extrapolated per position"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": tokens_per_s, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "T": w.T, "d": d, "V": V, "K": K, "chunk": c, "tau": 1.0,
+                       "teacher": w.teacher, "p_valid": w.p_valid,
+                       "l2": f"inputs larger than L2 (W is {V * d * 2 / 1e9:.2f} GB, re-read every chunk)",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "tflops_executed": tflops_exec,
+            "tflops_useful": w.flops_useful() / (ms * 1e-3) / 1e12,
+            "frac_of_bf16_peak": tflops_exec / peak,
+            "peak_device_gb": peak_alloc / 1e9,
+            "workspace_gb": ws.numel() / 1e9,
+            "resident_inputs_outputs_gb": base_alloc / 1e9,
+            "roofline": {"bound": "tensor", "kernel": dom_name, "achieved": achieved, "peak": peak,
+                         "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
+                         "peak_source": f"{peaks['source']} bf16 sustained",
+                         "flops_per_launch": gemm_flops_per_chunk},
+            "kernels": kernels,
+            "gpu_launches": launches,
+            "clocks": clocks.summary(),
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,203 @@
+/*
+ * kdkl.h — C ABI of libkdkl.so: an offline top-K teacher cache and a fused,
+ * chunked KL(p_teacher || q_student) distillation loss for one GB300 (sm_103a).
+ *
+ * The method is the one described in "Efficient Knowledge Distillation for
+ * LLMs: Offline Top-K Logits and a Fused Chunked KL Loss" (Multiverse Computing,
+ * Hugging Face blog, 10 Aug 2026), as reported by:
+ *   [ART] aiexpert.news, "Making knowledge distillation cheap enough to run in
+ *         production" — the offline top-K cache, the three loss formulations
+ *         (dense, forward-chunked, fused chunked) and the top-K limitation;
+ *   [DAI] dailyai.com.br launch report, section "As duas inovações";
+ *   [EPO] epoka.news, sections "Adónde se va la memoria" and "Los dos cambios
+ *         propuestos".
+ *
+ * Conventions shared by every entry point
+ *   - Every pointer argument is DEVICE memory owned by the caller, unless the
+ *     argument says otherwise.  The library allocates no device memory: scratch
+ *     space is the caller's workspace `ws` of at least the size that the matching
+ *     *_workspace() query returns, 256-byte aligned.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Every call
+ *     only enqueues work on it and returns without synchronising.
+ *   - Matrices are row-major.  bf16 is IEEE binary32 with the low 16 bits
+ *     dropped (the raw uint16 pattern).  Token rows are the flattened B*T
+ *     positions.
+ *   - Argument errors are detected on the host, before anything is enqueued,
+ *     and returned as KD_ERR_INVALID_ARG / KD_ERR_WORKSPACE / KD_ERR_UNSUPPORTED;
+ *     no CUDA call is made in that case.  A failed launch returns KD_ERR_CUDA.
+ *     Conditions that only the device can see (a teacher id outside [0, V), a
+ *     bounded wait inside a kernel that ran out) are recorded in an error word
+ *     inside the workspace and read with kd_get_device_error().
+ *   - Calls that share a workspace must be ordered (same stream, or events).
+ */
+#ifndef KDKL_H_
+#define KDKL_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define KD_API __attribute__((visibility("default")))
+#else
+#define KD_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  KD_OK = 0,
+  KD_ERR_INVALID_ARG = 1,   /* a size, pointer, alignment or K out of range     */
+  KD_ERR_UNSUPPORTED = 2,   /* no sm_103a device, or a shape the kernels refuse */
+  KD_ERR_WORKSPACE = 3,     /* ws is NULL, misaligned or smaller than required  */
+  KD_ERR_CUDA = 4,          /* a CUDA runtime/driver call or launch failed      */
+  KD_ERR_TIMEOUT = 5,       /* device: a bounded wait inside a kernel ran out   */
+  KD_ERR_DEVICE = 6         /* device: an input value out of range (teacher id) */
+} kd_status;
+
+#define KD_MAX_K 1024
+
+/* Human-readable name of a kd_status value (static string, never NULL). */
+KD_API const char* kd_status_string(int status);
+
+/* Library version as major*10000 + minor*100 + patch. */
+KD_API int kd_version(void);
+
+/* ------------------------------------------------------------------------ *
+ * Offline top-K teacher cache.
+ * [ART] paragraph on the first fix (offline distillation); [DAI] "As duas
+ * inovações" item 1; [EPO] "Los dos cambios propuestos", first item: the
+ * teacher runs once and only its K highest logits per position, with their
+ * token ids, are kept and reused.
+ * ------------------------------------------------------------------------ */
+
+/* Workspace bytes kd_topk_cache needs (>= 256; it holds the error word). */
+KD_API size_t kd_topk_cache_workspace(int64_t N, int64_t V, int K);
+
+/*
+ * For each of the N rows of a dense bf16 teacher-logits matrix, the K largest
+ * logits and their column (token) ids.
+ *   logits_bf16 : [N, ld] bf16, row r at logits_bf16 + r*ld; columns [0, V) are
+ *                 read.  16-byte aligned; ld >= V and ld*2 a multiple of 16.
+ *   K           : 1 <= K <= min(V, KD_MAX_K).
+ *   ids_out     : [N, K] int32, written.   vals_out: [N, K] fp32, written.
+ * Each output row is ordered by value, highest first; equal values are ordered
+ * by ascending id and the cut at K keeps the lowest ids; -0.0 equals +0.0.
+ * Values are the bf16 inputs widened exactly.  NaN inputs are ordered by their
+ * sign bit like any other bit pattern (positive NaN above +inf).
+ */
+KD_API int kd_topk_cache(const void* logits_bf16, int64_t N, int64_t V, int64_t ld, int K,
+                  int32_t* ids_out, float* vals_out,
+                  void* ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------ *
+ * Fused chunked KL loss.
+ * [ART] paragraph on the second fix; [DAI] "As duas inovações" item 2; [EPO]
+ * "Los dos cambios propuestos", second item.  Per position t (reading: forward
+ * KL, teacher renormalised over its K cached logits, student normalised over
+ * the full vocabulary):
+ *   z_t   = H_t W^T / tau                            (never stored)
+ *   p_t,k = softmax_k(t_logits_t,k / tau)
+ *   KL_t  = sum_k p_t,k (log p_t,k - z_t,id_k + logsumexp_v z_t,v)
+ *   loss  = sum over valid t of KL_t / N_valid       (0 when N_valid == 0)
+ * The positions are processed `chunk` rows at a time; the [chunk, V] logits
+ * live only in tensor memory, tile by tile.
+ * ------------------------------------------------------------------------ */
+
+/* Workspace bytes for kd_fused_kl_fwd and kd_fused_kl_bwd with these sizes
+ * (one query covers both calls).  Grows with chunk*V, not with N*V. */
+KD_API size_t kd_fused_kl_workspace(int64_t N, int64_t d, int64_t V, int K, int64_t chunk);
+
+/*
+ * Forward pass.
+ *   H_bf16   : [N, d] bf16 student hidden states (16-byte aligned rows: d % 8 == 0).
+ *   W_bf16   : [V, d] bf16 LM-head (output projection) weight.
+ *   t_ids    : [N, K] int32 cached teacher token ids, distinct within a row.
+ *   t_logits : [N, K] fp32 cached teacher logits (any order).
+ *   mask     : [N] uint8, 1 = valid position, 0 = padding; NULL = all valid.
+ *   chunk    : positions per chunk, a multiple of 128 (the last chunk may be short).
+ *   tau      : temperature > 0, divides both teacher and student logits.
+ *   loss_out : device fp32 scalar, written.
+ *   lse_out  : [N] fp32, logsumexp_v z_t,v, written; keep it for the backward.
+ *   kl_per_token_out : [N] fp32 KL_t (also for padding rows) or NULL.
+ */
+KD_API int kd_fused_kl_fwd(const void* H_bf16, const void* W_bf16,
+                    const int32_t* t_ids, const float* t_logits, const uint8_t* mask,
+                    int64_t N, int64_t d, int64_t V, int K, int64_t chunk, float tau,
+                    float* loss_out, float* lse_out, float* kl_per_token_out,
+                    void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Backward pass: recomputes each chunk's logits from H and W ([ART], the
+ * backward recomputes every chunk instead of storing it) and forms
+ *   dZ_t = grad_loss * mask_t / (N_valid * tau) * (softmax(z_t) - p_t scattered to its ids)
+ *   grad_H = dZ W            (overwritten; bf16, or fp32 if grad_H_is_fp32)
+ *   grad_W += dZ^T H         (fp32, ACCUMULATED into what the caller passes)
+ * with fp32 tensor-core accumulation; dZ is rounded to bf16 before the two
+ * gradient products.  Inputs as in kd_fused_kl_fwd, plus
+ *   lse       : [N] fp32 from the forward pass with the same inputs.
+ *   grad_loss : device fp32 scalar, the upstream gradient of the loss.
+ *   grad_H    : [N, d] bf16 or fp32.   grad_W : [V, d] fp32.
+ */
+KD_API int kd_fused_kl_bwd(const void* H_bf16, const void* W_bf16,
+                    const int32_t* t_ids, const float* t_logits, const uint8_t* mask,
+                    int64_t N, int64_t d, int64_t V, int K, int64_t chunk, float tau,
+                    const float* lse, const float* grad_loss,
+                    void* grad_H, int grad_H_is_fp32, float* grad_W,
+                    void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Reads (synchronising `stream`) and clears the device error word of a
+ * workspace used by the calls above.  Returns KD_OK, KD_ERR_TIMEOUT or
+ * KD_ERR_DEVICE; *detail_out (may be NULL) receives a call-specific detail
+ * (for KD_ERR_DEVICE: the first offending row).
+ */
+KD_API int kd_get_device_error(void* ws, void* stream, int64_t* detail_out);
+
+/* ------------------------------------------------------------------------ *
+ * Building blocks, exposed for testing and profiling.  No page describes these
+ * separately; they are the pieces the calls above are made of.
+ * ------------------------------------------------------------------------ */
+
+/*
+ * C[M, N] (op)= A · B^T-or-B with bf16 inputs and fp32 tensor-core accumulation,
+ * the projection engine shared by the loss kernels.
+ *   a_mn_major = 0: A is [M, K] row-major (K contiguous); 1: A is [K, M] (M contiguous).
+ *   b_mn_major = 0: B is [N, K] row-major;                 1: B is [K, N].
+ *   C is [M, N] fp32 row-major; accumulate != 0 adds into C.
+ * All leading dimensions are the contiguous extents above; K % 8 == 0 for
+ * K-major operands and M % 8 / N % 8 == 0 for MN-major ones.
+ */
+KD_API int kd_gemm_bf16(const void* A, const void* B, float* C, int64_t M, int64_t N, int64_t K,
+                 int a_mn_major, int b_mn_major, int accumulate,
+                 void* ws, size_t ws_bytes, void* stream);
+
+/* Workspace bytes for kd_gemm_bf16. */
+KD_API size_t kd_gemm_workspace(void);
+
+/*
+ * Self-check of the bounded waits every kernel uses: launches one block that
+ * waits on a shared-memory barrier nothing arrives at, with a limit of
+ * `limit_ns` (1 us .. 1 s) instead of the kernels' 2 s.  The wait gives up, the
+ * kernel records a timeout in the error word of `ws` and exits normally, so
+ * kd_get_device_error(ws) then returns KD_ERR_TIMEOUT and the CUDA context
+ * stays usable.
+ */
+KD_API int kd_check_wait_timeout(void* ws, size_t ws_bytes, int64_t limit_ns, void* stream);
+
+/*
+ * Per-launch timing of this library's kernels, for profiling.  While enabled,
+ * each launch on `stream` is bracketed by two CUDA events (at most `capacity`
+ * launches are recorded).  kd_profile_read synchronises, then fills up to `n`
+ * entries of names[] (static strings), ms[] and returns how many launches were
+ * recorded since kd_profile_begin.  Host-side state; not thread-safe.
+ */
+KD_API int kd_profile_begin(int capacity);
+KD_API int kd_profile_end(void);
+KD_API int kd_profile_read(const char** names, float* ms, int n);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KDKL_H_ */

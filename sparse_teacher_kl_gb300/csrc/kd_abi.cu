@@ -1,0 +1,404 @@
+// The C ABI of libkdkl.so (declared in include/kdkl.h): argument checks,
+// workspace layout, TMA descriptor set-up and the chunk loop that drives the
+// kernels.  Host code only; every arithmetic step runs in the kernels.
+#include <cudaTypedefs.h>
+#include <math.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <mutex>
+#include <vector>
+
+#include "kd_internal.h"
+
+namespace kd {
+
+// ------------------------------------------------------------ profiling ---
+
+struct ProfRec {
+  const char* name;
+  cudaEvent_t start, stop;
+};
+static std::vector<ProfRec> g_prof;
+static int g_prof_used = 0;
+static bool g_prof_on = false;
+
+void prof_before(const char* name, cudaStream_t s) {
+  if (!g_prof_on || g_prof_used >= int(g_prof.size())) return;
+  g_prof[g_prof_used].name = name;
+  cudaEventRecord(g_prof[g_prof_used].start, s);
+}
+
+void prof_after(cudaStream_t s) {
+  if (!g_prof_on || g_prof_used >= int(g_prof.size())) return;
+  cudaEventRecord(g_prof[g_prof_used].stop, s);
+  ++g_prof_used;
+}
+
+// ------------------------------------------------------------ tensor maps ---
+
+static PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+static std::once_flag g_encode_once;
+
+static bool load_encode() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode != nullptr;
+}
+
+bool make_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                       uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer) {
+  if (!load_encode()) return false;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {row_stride_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// ---------------------------------------------------------- device check ---
+
+static int g_dev_ok = -1;  // -1 unknown, 0 no, 1 yes
+
+static kd_status check_device() {
+  if (g_dev_ok < 0) {
+    int dev = 0, major = 0, minor = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return KD_ERR_CUDA;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    g_dev_ok = (major == 10 && minor == 3) ? 1 : 0;
+  }
+  return g_dev_ok ? KD_OK : KD_ERR_UNSUPPORTED;
+}
+
+// -------------------------------------------------------------- layout ---
+
+static inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct KlLayout {
+  size_t ids_sorted, p_sorted, negent, kl, partials, dz, total;
+  int64_t ldz, rows_pad;
+  int n_groups;
+};
+
+static int choose_n_group(int64_t V) {
+  (void)V;
+  return 1;
+}
+
+static KlLayout kl_layout(int64_t N, int64_t d, int64_t V, int K, int64_t chunk) {
+  (void)d;
+  KlLayout L{};
+  const int64_t c = chunk < N ? chunk : N;
+  L.rows_pad = (c + BM - 1) / BM * BM;
+  L.ldz = (V + 7) / 8 * 8;
+  const int n_tiles = int((V + BN - 1) / BN);
+  const int g = choose_n_group(V);
+  L.n_groups = (n_tiles + g - 1) / g;
+  size_t off = sizeof(Ctrl);
+  L.ids_sorted = off; off = align_up(off + size_t(L.rows_pad) * K * 4, 256);
+  L.p_sorted = off;   off = align_up(off + size_t(L.rows_pad) * K * 4, 256);
+  L.negent = off;     off = align_up(off + size_t(L.rows_pad) * 4, 256);
+  L.kl = off;         off = align_up(off + size_t(N) * 4, 256);
+  L.partials = off;   off = align_up(off + size_t(L.n_groups) * L.rows_pad * 16, 256);
+  L.dz = off;         off = align_up(off + size_t(L.rows_pad) * L.ldz * 2, 256);
+  L.total = off;
+  return L;
+}
+
+static bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+static kd_status check_kl_args(const void* H, const void* W, const int32_t* ids, const float* tlog, int64_t N,
+                               int64_t d, int64_t V, int K, int64_t chunk, float tau, const void* ws,
+                               size_t ws_bytes) {
+  if (N < 1 || d < 8 || V < 1 || K < 1 || chunk < BM) return KD_ERR_INVALID_ARG;
+  if (d % 8 != 0 || chunk % BM != 0) return KD_ERR_INVALID_ARG;
+  if (K > KD_MAX_K || int64_t(K) > V) return KD_ERR_INVALID_ARG;
+  if (V > 0x7fffffffLL || N > 0x7fffffffLL || d > 0x7fffffffLL) return KD_ERR_INVALID_ARG;
+  if (!(tau > 0.f) || !isfinite(tau)) return KD_ERR_INVALID_ARG;
+  if (!H || !W || !ids || !tlog) return KD_ERR_INVALID_ARG;
+  if (!aligned(H, 16) || !aligned(W, 16) || !aligned(ids, 4) || !aligned(tlog, 4)) return KD_ERR_INVALID_ARG;
+  if (!ws || !aligned(ws, 256)) return KD_ERR_WORKSPACE;
+  if (ws_bytes < kl_layout(N, d, V, K, chunk).total) return KD_ERR_WORKSPACE;
+  return KD_OK;
+}
+
+static kd_status map_cuda(cudaError_t e) { return e == cudaSuccess ? KD_OK : KD_ERR_CUDA; }
+
+}  // namespace kd
+
+using namespace kd;
+
+extern "C" {
+
+const char* kd_status_string(int status) {
+  switch (status) {
+    case KD_OK: return "KD_OK";
+    case KD_ERR_INVALID_ARG: return "KD_ERR_INVALID_ARG";
+    case KD_ERR_UNSUPPORTED: return "KD_ERR_UNSUPPORTED";
+    case KD_ERR_WORKSPACE: return "KD_ERR_WORKSPACE";
+    case KD_ERR_CUDA: return "KD_ERR_CUDA";
+    case KD_ERR_TIMEOUT: return "KD_ERR_TIMEOUT";
+    case KD_ERR_DEVICE: return "KD_ERR_DEVICE";
+    default: return "KD_ERR_UNKNOWN";
+  }
+}
+
+int kd_version(void) { return 100; }
+
+size_t kd_topk_cache_workspace(int64_t N, int64_t V, int K) {
+  (void)N; (void)V; (void)K;
+  return sizeof(Ctrl);
+}
+
+int kd_topk_cache(const void* logits_bf16, int64_t N, int64_t V, int64_t ld, int K, int32_t* ids_out,
+                  float* vals_out, void* ws, size_t ws_bytes, void* stream) {
+  if (N < 1 || V < 1 || K < 1 || K > KD_MAX_K || int64_t(K) > V || ld < V) return KD_ERR_INVALID_ARG;
+  if (V > 0x7fffffffLL || ld % 8 != 0) return KD_ERR_INVALID_ARG;
+  if (!logits_bf16 || !ids_out || !vals_out) return KD_ERR_INVALID_ARG;
+  if (!aligned(logits_bf16, 16) || !aligned(ids_out, 4) || !aligned(vals_out, 4)) return KD_ERR_INVALID_ARG;
+  if (!ws || !aligned(ws, 256) || ws_bytes < kd_topk_cache_workspace(N, V, K)) return KD_ERR_WORKSPACE;
+  kd_status st = check_device();
+  if (st != KD_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  Ctrl* ctrl = static_cast<Ctrl*>(ws);
+  return map_cuda(launch_topk(static_cast<const uint16_t*>(logits_bf16), N, V, ld, K, ids_out, vals_out,
+                              &ctrl->err, s));
+}
+
+size_t kd_fused_kl_workspace(int64_t N, int64_t d, int64_t V, int K, int64_t chunk) {
+  if (N < 1 || d < 1 || V < 1 || K < 1 || chunk < 1) return 0;
+  return kl_layout(N, d, V, K, chunk).total;
+}
+
+int kd_fused_kl_fwd(const void* H_bf16, const void* W_bf16, const int32_t* t_ids, const float* t_logits,
+                    const uint8_t* mask, int64_t N, int64_t d, int64_t V, int K, int64_t chunk, float tau,
+                    float* loss_out, float* lse_out, float* kl_per_token_out, void* ws, size_t ws_bytes,
+                    void* stream) {
+  kd_status st = check_kl_args(H_bf16, W_bf16, t_ids, t_logits, N, d, V, K, chunk, tau, ws, ws_bytes);
+  if (st != KD_OK) return st;
+  if (!loss_out || !lse_out || !aligned(loss_out, 4) || !aligned(lse_out, 4)) return KD_ERR_INVALID_ARG;
+  if (kl_per_token_out && !aligned(kl_per_token_out, 4)) return KD_ERR_INVALID_ARG;
+  st = check_device();
+  if (st != KD_OK) return st;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const KlLayout L = kl_layout(N, d, V, K, chunk);
+  uint8_t* w8 = static_cast<uint8_t*>(ws);
+  Ctrl* ctrl = reinterpret_cast<Ctrl*>(w8);
+  int32_t* ids_sorted = reinterpret_cast<int32_t*>(w8 + L.ids_sorted);
+  float* p_sorted = reinterpret_cast<float*>(w8 + L.p_sorted);
+  float* negent = reinterpret_cast<float*>(w8 + L.negent);
+  float* kl = kl_per_token_out ? kl_per_token_out : reinterpret_cast<float*>(w8 + L.kl);
+  float4* partials = reinterpret_cast<float4*>(w8 + L.partials);
+  const float inv_tau = 1.0f / tau;
+  const uint16_t* H = static_cast<const uint16_t*>(H_bf16);
+
+  alignas(64) CUtensorMap tw, th;
+  if (!make_tmap_2d_bf16(&tw, W_bf16, uint64_t(d), uint64_t(V), uint64_t(d) * 2, BK, BN)) return KD_ERR_CUDA;
+
+  cudaError_t e = launch_count_valid(mask, N, &ctrl->n_valid, s);
+  if (e != cudaSuccess) return KD_ERR_CUDA;
+  const int grid_max = gemm_max_grid();
+  for (int64_t c0 = 0; c0 < N; c0 += chunk) {
+    const int n = int((N - c0) < chunk ? (N - c0) : chunk);
+    e = launch_teacher_prologue(t_ids + c0 * K, t_logits + c0 * K, n, K, V, inv_tau, ids_sorted, p_sorted, negent,
+                                &ctrl->err, c0, s);
+    if (e != cudaSuccess) return KD_ERR_CUDA;
+    if (!make_tmap_2d_bf16(&th, H + c0 * d, uint64_t(d), uint64_t(n), uint64_t(d) * 2, BK, BM)) return KD_ERR_CUDA;
+    GemmProblem p{};
+    p.M = n; p.N = int(V); p.K = int(d);
+    p.a_mn = 0; p.b_mn = 0; p.epi = EPI_LSE;
+    p.m_tiles = (n + BM - 1) / BM;
+    p.n_tiles = int((V + BN - 1) / BN);
+    p.n_group = choose_n_group(V);
+    p.n_units = p.m_tiles * ((p.n_tiles + p.n_group - 1) / p.n_group);
+    p.ids_sorted = ids_sorted; p.p_sorted = p_sorted; p.Kt = K; p.inv_tau = inv_tau;
+    p.partials = partials; p.rows = n; p.err = &ctrl->err;
+    e = launch_gemm(p, th, tw, grid_max, s);
+    if (e != cudaSuccess) return KD_ERR_CUDA;
+    e = launch_lse_combine(partials, L.n_groups, n, negent, inv_tau, lse_out + c0, kl + c0, s);
+    if (e != cudaSuccess) return KD_ERR_CUDA;
+  }
+  e = launch_loss_reduce(kl, mask, N, &ctrl->n_valid, loss_out, s);
+  return map_cuda(e);
+}
+
+int kd_fused_kl_bwd(const void* H_bf16, const void* W_bf16, const int32_t* t_ids, const float* t_logits,
+                    const uint8_t* mask, int64_t N, int64_t d, int64_t V, int K, int64_t chunk, float tau,
+                    const float* lse, const float* grad_loss, void* grad_H, int grad_H_is_fp32, float* grad_W,
+                    void* ws, size_t ws_bytes, void* stream) {
+  kd_status st = check_kl_args(H_bf16, W_bf16, t_ids, t_logits, N, d, V, K, chunk, tau, ws, ws_bytes);
+  if (st != KD_OK) return st;
+  if (!lse || !grad_loss || !grad_H || !grad_W) return KD_ERR_INVALID_ARG;
+  if (!aligned(lse, 4) || !aligned(grad_loss, 4) || !aligned(grad_H, 16) || !aligned(grad_W, 16))
+    return KD_ERR_INVALID_ARG;
+  st = check_device();
+  if (st != KD_OK) return st;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const KlLayout L = kl_layout(N, d, V, K, chunk);
+  uint8_t* w8 = static_cast<uint8_t*>(ws);
+  Ctrl* ctrl = reinterpret_cast<Ctrl*>(w8);
+  int32_t* ids_sorted = reinterpret_cast<int32_t*>(w8 + L.ids_sorted);
+  float* p_sorted = reinterpret_cast<float*>(w8 + L.p_sorted);
+  float* negent = reinterpret_cast<float*>(w8 + L.negent);
+  uint16_t* dz = reinterpret_cast<uint16_t*>(w8 + L.dz);
+  const float inv_tau = 1.0f / tau;
+  const uint16_t* H = static_cast<const uint16_t*>(H_bf16);
+  const size_t gh_elt = grad_H_is_fp32 ? 4 : 2;
+
+  alignas(64) CUtensorMap tw_k, tw_mn, th_k, th_mn, tdz_k, tdz_mn;
+  if (!make_tmap_2d_bf16(&tw_k, W_bf16, uint64_t(d), uint64_t(V), uint64_t(d) * 2, BK, BN)) return KD_ERR_CUDA;
+  if (!make_tmap_2d_bf16(&tw_mn, W_bf16, uint64_t(d), uint64_t(V), uint64_t(d) * 2, 64, BK)) return KD_ERR_CUDA;
+
+  cudaError_t e = launch_count_valid(mask, N, &ctrl->n_valid, s);
+  if (e != cudaSuccess) return KD_ERR_CUDA;
+  const int grid_max = gemm_max_grid();
+  for (int64_t c0 = 0; c0 < N; c0 += chunk) {
+    const int n = int((N - c0) < chunk ? (N - c0) : chunk);
+    e = launch_teacher_prologue(t_ids + c0 * K, t_logits + c0 * K, n, K, V, inv_tau, ids_sorted, p_sorted, negent,
+                                &ctrl->err, c0, s);
+    if (e != cudaSuccess) return KD_ERR_CUDA;
+    const uint16_t* Hc = H + c0 * d;
+    if (!make_tmap_2d_bf16(&th_k, Hc, uint64_t(d), uint64_t(n), uint64_t(d) * 2, BK, BM)) return KD_ERR_CUDA;
+    if (!make_tmap_2d_bf16(&th_mn, Hc, uint64_t(d), uint64_t(n), uint64_t(d) * 2, 64, BK)) return KD_ERR_CUDA;
+    if (!make_tmap_2d_bf16(&tdz_k, dz, uint64_t(V), uint64_t(n), uint64_t(L.ldz) * 2, BK, BM)) return KD_ERR_CUDA;
+    if (!make_tmap_2d_bf16(&tdz_mn, dz, uint64_t(V), uint64_t(n), uint64_t(L.ldz) * 2, 64, BK)) return KD_ERR_CUDA;
+
+    // B1: recompute the chunk's logits, dZ -> bf16 workspace
+    GemmProblem p{};
+    p.M = n; p.N = int(V); p.K = int(d);
+    p.a_mn = 0; p.b_mn = 0; p.epi = EPI_DZ;
+    p.m_tiles = (n + BM - 1) / BM;
+    p.n_tiles = int((V + BN - 1) / BN);
+    p.n_group = 1;
+    p.n_units = p.m_tiles * p.n_tiles;
+    p.ids_sorted = ids_sorted; p.p_sorted = p_sorted; p.Kt = K; p.inv_tau = inv_tau;
+    p.lse = lse + c0; p.mask = mask ? mask + c0 : nullptr; p.grad_loss = grad_loss; p.n_valid = &ctrl->n_valid;
+    p.dz = dz; p.ldz = L.ldz; p.rows = n; p.err = &ctrl->err;
+    e = launch_gemm(p, th_k, tw_k, grid_max, s);
+    if (e != cudaSuccess) return KD_ERR_CUDA;
+
+    // B2: grad_H rows of the chunk = dZ W  (A = dZ K-major over V, B = W with d contiguous)
+    GemmProblem q{};
+    q.M = n; q.N = int(d); q.K = int(V);
+    q.a_mn = 0; q.b_mn = 1; q.epi = EPI_STORE;
+    q.m_tiles = (n + BM - 1) / BM;
+    q.n_tiles = int((d + BN - 1) / BN);
+    q.n_group = 1;
+    q.n_units = q.m_tiles * q.n_tiles;
+    q.C = static_cast<uint8_t*>(grad_H) + size_t(c0) * d * gh_elt;
+    q.ldc = d; q.c_bf16 = grad_H_is_fp32 ? 0 : 1; q.err = &ctrl->err;
+    e = launch_gemm(q, tdz_k, tw_mn, grid_max, s);
+    if (e != cudaSuccess) return KD_ERR_CUDA;
+
+    // B3: grad_W += dZ^T H_c  (A = dZ with V contiguous, B = H_c with d contiguous)
+    GemmProblem r{};
+    r.M = int(V); r.N = int(d); r.K = n;
+    r.a_mn = 1; r.b_mn = 1; r.epi = EPI_ACCUM;
+    r.m_tiles = int((V + BM - 1) / BM);
+    r.n_tiles = int((d + BN - 1) / BN);
+    r.n_group = 1;
+    r.n_units = r.m_tiles * r.n_tiles;
+    r.C = grad_W; r.ldc = d; r.c_bf16 = 0; r.err = &ctrl->err;
+    e = launch_gemm(r, tdz_mn, th_mn, grid_max, s);
+    if (e != cudaSuccess) return KD_ERR_CUDA;
+  }
+  return KD_OK;
+}
+
+int kd_get_device_error(void* ws, void* stream, int64_t* detail_out) {
+  if (!ws || !aligned(ws, 256)) return KD_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return KD_ERR_CUDA;
+  uint32_t w[2] = {0, 0};
+  if (cudaMemcpy(w, ws, sizeof(w), cudaMemcpyDeviceToHost) != cudaSuccess) return KD_ERR_CUDA;
+  if (cudaMemset(ws, 0, sizeof(w)) != cudaSuccess) return KD_ERR_CUDA;
+  if (detail_out) *detail_out = int64_t(w[1]);
+  if (w[0] == KD_DEVERR_NONE) return KD_OK;
+  if (w[0] == KD_DEVERR_TIMEOUT) return KD_ERR_TIMEOUT;
+  return KD_ERR_DEVICE;
+}
+
+size_t kd_gemm_workspace(void) { return sizeof(Ctrl); }
+
+int kd_check_wait_timeout(void* ws, size_t ws_bytes, int64_t limit_ns, void* stream) {
+  if (!ws || !aligned(ws, 256) || ws_bytes < sizeof(Ctrl)) return KD_ERR_WORKSPACE;
+  if (limit_ns < 1000 || limit_ns > 1000000000LL) return KD_ERR_INVALID_ARG;
+  kd_status st = check_device();
+  if (st != KD_OK) return st;
+  return map_cuda(launch_wait_timeout(&static_cast<Ctrl*>(ws)->err, uint64_t(limit_ns),
+                                      static_cast<cudaStream_t>(stream)));
+}
+
+int kd_gemm_bf16(const void* A, const void* B, float* C, int64_t M, int64_t N, int64_t K, int a_mn, int b_mn,
+                 int accumulate, void* ws, size_t ws_bytes, void* stream) {
+  if (M < 1 || N < 1 || K < 1 || M > 0x7fffffffLL || N > 0x7fffffffLL || K > 0x7fffffffLL)
+    return KD_ERR_INVALID_ARG;
+  if (!A || !B || !C || !aligned(A, 16) || !aligned(B, 16) || !aligned(C, 16)) return KD_ERR_INVALID_ARG;
+  if (N % 4 != 0) return KD_ERR_INVALID_ARG;
+  if ((a_mn ? M : K) % 8 != 0 || (b_mn ? N : K) % 8 != 0) return KD_ERR_INVALID_ARG;
+  if (!ws || !aligned(ws, 256) || ws_bytes < kd_gemm_workspace()) return KD_ERR_WORKSPACE;
+  kd_status st = check_device();
+  if (st != KD_OK) return st;
+  alignas(64) CUtensorMap ta, tb;
+  bool ok = a_mn ? make_tmap_2d_bf16(&ta, A, uint64_t(M), uint64_t(K), uint64_t(M) * 2, 64, BK)
+                 : make_tmap_2d_bf16(&ta, A, uint64_t(K), uint64_t(M), uint64_t(K) * 2, BK, BM);
+  ok = ok && (b_mn ? make_tmap_2d_bf16(&tb, B, uint64_t(N), uint64_t(K), uint64_t(N) * 2, 64, BK)
+                   : make_tmap_2d_bf16(&tb, B, uint64_t(K), uint64_t(N), uint64_t(K) * 2, BK, BN));
+  if (!ok) return KD_ERR_CUDA;
+  GemmProblem p{};
+  p.M = int(M); p.N = int(N); p.K = int(K);
+  p.a_mn = a_mn ? 1 : 0; p.b_mn = b_mn ? 1 : 0;
+  p.epi = accumulate ? EPI_ACCUM : EPI_STORE;
+  p.m_tiles = int((M + BM - 1) / BM);
+  p.n_tiles = int((N + BN - 1) / BN);
+  p.n_group = 1;
+  p.n_units = p.m_tiles * p.n_tiles;
+  p.C = C; p.ldc = N; p.c_bf16 = 0;
+  p.err = &static_cast<Ctrl*>(ws)->err;
+  return map_cuda(launch_gemm(p, ta, tb, gemm_max_grid(), static_cast<cudaStream_t>(stream)));
+}
+
+int kd_profile_begin(int capacity) {
+  if (capacity < 1) return KD_ERR_INVALID_ARG;
+  if (int(g_prof.size()) < capacity) {
+    size_t old = g_prof.size();
+    g_prof.resize(size_t(capacity));
+    for (size_t i = old; i < g_prof.size(); ++i) {
+      if (cudaEventCreate(&g_prof[i].start) != cudaSuccess || cudaEventCreate(&g_prof[i].stop) != cudaSuccess)
+        return KD_ERR_CUDA;
+    }
+  }
+  g_prof_used = 0;
+  g_prof_on = true;
+  return KD_OK;
+}
+
+int kd_profile_end(void) {
+  g_prof_on = false;
+  return KD_OK;
+}
+
+int kd_profile_read(const char** names, float* ms, int n) {
+  for (int i = 0; i < g_prof_used && i < n; ++i) {
+    if (cudaEventSynchronize(g_prof[i].stop) != cudaSuccess) return -KD_ERR_CUDA;
+    float t = 0.f;
+    cudaEventElapsedTime(&t, g_prof[i].start, g_prof[i].stop);
+    if (names) names[i] = g_prof[i].name;
+    if (ms) ms[i] = t;
+  }
+  return g_prof_used;
+}
+
+}  // extern "C"

@@ -1,0 +1,430 @@
+// The projection engine: a persistent, warp-specialised bf16 GEMM on the
+// fifth-generation tensor cores (tcgen05.mma, fp32 accumulators in tensor
+// memory), fed by TMA, with the loss arithmetic fused into the epilogue.
+//
+// One CTA per SM.  Warp 0 issues TMA loads into a 4-stage shared-memory ring,
+// warp 1 owns tensor memory and issues the MMAs (one thread), warps 2..5 drain
+// finished 128 x 256 accumulators from tensor memory while the next tile is
+// being multiplied into the other half of it (512 columns, double-buffered).
+//
+// Epilogues (the loss steps of the fused chunked KL, [ART] paragraph on the
+// second fix; [DAI] "As duas inovações" item 2):
+//   EPI_LSE   z = H_c W^T never leaves the chip: per row, a running max and
+//             sum of 2^((z - max) log2e / tau) across the vocabulary tiles of a
+//             unit, plus sum_k p_k z_id_k for the cached ids that fall in them;
+//             one (max, sum, gather) partial per row and unit.
+//   EPI_DZ    the backward recompute: dZ = scale * (2^(z log2e/tau - lse log2e)
+//             - p on the cached ids), rounded to bf16 into a [rows, ldz] buffer.
+//   EPI_STORE / EPI_ACCUM  plain C = acc / C += acc for the gradient products.
+#include <math.h>
+#include <stdio.h>
+
+#include "kd_device.cuh"
+#include "kd_internal.h"
+
+namespace kd {
+
+struct __align__(8) GemmSmemTail {
+  uint64_t full[STAGES];
+  uint64_t empty[STAGES];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  uint32_t abort_flag;
+};
+
+constexpr size_t GEMM_SMEM_BYTES = 1024 /*alignment slack*/ + size_t(STAGES) * STAGE_BYTES + sizeof(GemmSmemTail);
+
+// Unit u -> tile coordinates.  LSE/DZ walk the vocabulary (n) slowly so that
+// every CTA in flight reads the same few W tiles while the small H chunk stays
+// in L2; the gradient products walk n fastest so that CTAs in flight share A.
+__device__ __forceinline__ void unit_coords(const GemmProblem& p, int u, int& m_blk, int& n_first, int& n_count) {
+  if (p.epi == EPI_LSE || p.epi == EPI_DZ) {
+    const int g = u / p.m_tiles;
+    m_blk = u - g * p.m_tiles;
+    n_first = g * p.n_group;
+    n_count = min(p.n_group, p.n_tiles - n_first);
+  } else {
+    m_blk = u / p.n_tiles;
+    n_first = u - m_blk * p.n_tiles;
+    n_count = 1;
+  }
+}
+
+template <int EPI>
+__global__ void __launch_bounds__(GEMM_THREADS, 1)
+    kd_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                   const GemmProblem p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* stage_base = smem;
+  GemmSmemTail* tail = reinterpret_cast<GemmSmemTail*>(smem + size_t(STAGES) * STAGE_BYTES);
+  volatile uint32_t* abort_flag = &tail->abort_flag;
+
+  const uint32_t warp = threadIdx.x >> 5;
+  const uint32_t lane = lane_id();
+  const int k_blocks = (p.K + BK - 1) / BK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&tail->full[s], 1);
+      mbar_init(&tail->empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tail->tfull[a], 1);
+      mbar_init(&tail->tempty[a], 128);
+    }
+    mbar_init(&tail->drain, 1);
+    tail->abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_map(&tmap_a);
+    tma_prefetch_map(&tmap_b);
+  }
+  if (warp == 1) {
+    tmem_alloc(&tail->tmem_base, TMEM_COLS);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = tail->tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      uint32_t it = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x) {
+        int m_blk, n_first, n_count;
+        unit_coords(p, u, m_blk, n_first, n_count);
+        for (int nb = n_first; nb < n_first + n_count && ok; ++nb) {
+          for (int kb = 0; kb < k_blocks; ++kb, ++it) {
+            const uint32_t s = it % STAGES;
+            const uint32_t ph = (it / STAGES) & 1u;
+            if (!mbar_wait(&tail->empty[s], ph ^ 1u, abort_flag, p.err, 0x100u)) {
+              ok = false;
+              break;
+            }
+            uint8_t* sa = stage_base + size_t(s) * STAGE_BYTES;
+            uint8_t* sb = sa + STAGE_A_BYTES;
+            mbar_arrive_expect_tx(&tail->full[s], STAGE_BYTES);
+            if (p.a_mn == 0) {
+              tma_load_2d(sa, &tmap_a, &tail->full[s], kb * BK, m_blk * BM);
+            } else {
+#pragma unroll
+              for (int j = 0; j < BM / 64; ++j)
+                tma_load_2d(sa + j * 8192, &tmap_a, &tail->full[s], m_blk * BM + j * 64, kb * BK);
+            }
+            if (p.b_mn == 0) {
+              tma_load_2d(sb, &tmap_b, &tail->full[s], kb * BK, nb * BN);
+            } else {
+#pragma unroll
+              for (int j = 0; j < BN / 64; ++j)
+                tma_load_2d(sb + j * 8192, &tmap_b, &tail->full[s], nb * BN + j * 64, kb * BK);
+            }
+          }
+        }
+      }
+      if (!ok) {
+        // Let the copies already issued land before the CTA can exit.
+        const uint32_t first = it > STAGES ? it - STAGES : 0;
+        for (uint32_t j = first; j < it; ++j) {
+          volatile uint32_t never = 0;
+          mbar_wait(&tail->full[j % STAGES], (j / STAGES) & 1u, &never, nullptr, 0);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16_f32(BM, BN, p.a_mn, p.b_mn);
+      const uint32_t a_step = p.a_mn ? 16u * 128u : 32u;
+      const uint32_t b_step = p.b_mn ? 16u * 128u : 32u;
+      const uint32_t a_lbo = p.a_mn ? 8192u : 16u;
+      const uint32_t b_lbo = p.b_mn ? 8192u : 16u;
+      uint32_t it = 0, acc_it = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x) {
+        int m_blk, n_first, n_count;
+        unit_coords(p, u, m_blk, n_first, n_count);
+        for (int nb = n_first; nb < n_first + n_count && ok; ++nb, ++acc_it) {
+          const uint32_t a = acc_it & 1u;
+          const uint32_t aph = (acc_it >> 1) & 1u;
+          if (!mbar_wait(&tail->tempty[a], aph ^ 1u, abort_flag, p.err, 0x200u)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d_tmem = tmem_base + a * BN;
+          for (int kb = 0; kb < k_blocks; ++kb, ++it) {
+            const uint32_t s = it % STAGES;
+            const uint32_t ph = (it / STAGES) & 1u;
+            if (!mbar_wait(&tail->full[s], ph, abort_flag, p.err, 0x300u)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t sa = smem_u32(stage_base + size_t(s) * STAGE_BYTES);
+            const uint32_t sb = sa + STAGE_A_BYTES;
+#pragma unroll
+            for (int k = 0; k < BK / 16; ++k) {
+              const uint64_t ad = sdesc_sw128(sa + k * a_step, a_lbo);
+              const uint64_t bd = sdesc_sw128(sb + k * b_step, b_lbo);
+              umma_bf16(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+            }
+            umma_commit(&tail->empty[s]);
+          }
+          if (ok) umma_commit(&tail->tfull[a]);
+        }
+      }
+      // Drain: every MMA issued above has completed once this arrives.
+      umma_commit(&tail->drain);
+      volatile uint32_t never = 0;
+      mbar_wait(&tail->drain, 0, &never, p.err, 0x400u);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const uint32_t quarter = warp & 3u;  // tensor-memory lane quarter this warp may access
+    const int r_local = int(quarter * 32u + lane);
+    const uint32_t t_lane = tmem_base + ((quarter * 32u) << 16);
+    const float scale2 = 1.4426950408889634f * p.inv_tau;  // log2(e) / tau
+    uint32_t acc_it = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x) {
+      int m_blk, n_first, n_count;
+      unit_coords(p, u, m_blk, n_first, n_count);
+      const int row = m_blk * BM + r_local;
+
+      // Per-row state for the loss epilogues.
+      float run_m = -INFINITY, run_s = 0.f, run_g = 0.f;
+      int cur = 0;
+      int nid = 0x7fffffff;
+      float np_ = 0.f;
+      const int32_t* ids_row = nullptr;
+      const float* p_row = nullptr;
+      float lse2 = 0.f, rowscale = 0.f;
+      if (EPI == EPI_LSE || EPI == EPI_DZ) {
+        const bool row_ok = row < p.rows;
+        cur = p.Kt;
+        if (row_ok) {
+          ids_row = p.ids_sorted + size_t(row) * p.Kt;
+          p_row = p.p_sorted + size_t(row) * p.Kt;
+          const int v_lo = n_first * BN;
+          int lo = 0, hi = p.Kt;  // first entry with id >= v_lo
+          while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (__ldg(ids_row + mid) < v_lo) lo = mid + 1; else hi = mid;
+          }
+          cur = lo;
+          if (cur < p.Kt) {
+            nid = __ldg(ids_row + cur);
+            np_ = __ldg(p_row + cur);
+          }
+        }
+        if (EPI == EPI_DZ && row_ok) {
+          lse2 = p.lse[row] * 1.4426950408889634f;
+          const int nv = *p.n_valid;
+          const bool valid = (p.mask == nullptr) || (p.mask[row] != 0);
+          rowscale = (valid && nv > 0) ? (*p.grad_loss) * p.inv_tau / float(nv) : 0.f;
+        }
+      }
+
+      for (int nb = n_first; nb < n_first + n_count; ++nb, ++acc_it) {
+        const uint32_t a = acc_it & 1u;
+        const uint32_t aph = (acc_it >> 1) & 1u;
+        // the tensor-memory loads below are warp-collective: decide per warp
+        const bool got = mbar_wait(&tail->tfull[a], aph, abort_flag, p.err, 0x500u);
+        if (!__all_sync(0xffffffffu, got)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t t_acc = t_lane + a * BN;
+
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t raw[32];
+          tmem_ld_32x32b_x32(t_acc + c * 32, raw);
+          tmem_ld_wait();
+          float x[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(raw[i]);
+          const int col0 = nb * BN + c * 32;
+
+          if (EPI == EPI_LSE) {
+            if (row < p.rows) {
+              // columns past the vocabulary do not exist
+              if (col0 + 32 > p.N) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                  if (col0 + i >= p.N) x[i] = -INFINITY;
+              }
+              float cm = x[0];
+#pragma unroll
+              for (int i = 1; i < 32; ++i) cm = fmaxf(cm, x[i]);
+              if (cm != -INFINITY) {
+                if (cm > run_m) {
+                  run_s *= ex2_approx((run_m - cm) * scale2);
+                  run_m = cm;
+                }
+                const float off = -run_m * scale2;
+                float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+                for (int i = 0; i < 32; i += 2) {
+                  s0 += ex2_approx(fmaf(x[i], scale2, off));
+                  s1 += ex2_approx(fmaf(x[i + 1], scale2, off));
+                }
+                run_s += s0 + s1;
+              }
+              while (nid < col0 + 32) {
+                run_g = fmaf(np_, select32(x, uint32_t(nid - col0)), run_g);
+                ++cur;
+                if (cur < p.Kt) {
+                  nid = __ldg(ids_row + cur);
+                  np_ = __ldg(p_row + cur);
+                } else {
+                  nid = 0x7fffffff;
+                }
+              }
+            }
+          } else if (EPI == EPI_DZ) {
+            if (row < p.rows) {
+              float q[32];
+#pragma unroll
+              for (int i = 0; i < 32; ++i) q[i] = ex2_approx(fmaf(x[i], scale2, -lse2));
+              while (nid < col0 + 32) {
+                const int off = nid - col0;
+#pragma unroll
+                for (int i = 0; i < 32; ++i) q[i] = (i == off) ? q[i] - np_ : q[i];
+                ++cur;
+                if (cur < p.Kt) {
+                  nid = __ldg(ids_row + cur);
+                  np_ = __ldg(p_row + cur);
+                } else {
+                  nid = 0x7fffffff;
+                }
+              }
+              if (col0 + 32 > p.N) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                  if (col0 + i >= p.N) q[i] = 0.f;
+              }
+              uint16_t* dst = p.dz + size_t(row) * p.ldz + col0;
+#pragma unroll
+              for (int g8 = 0; g8 < 4; ++g8) {
+                if (col0 + g8 * 8 + 8 <= p.ldz) {
+                  uint4 v;
+                  v.x = pack_bf16x2(q[g8 * 8 + 0] * rowscale, q[g8 * 8 + 1] * rowscale);
+                  v.y = pack_bf16x2(q[g8 * 8 + 2] * rowscale, q[g8 * 8 + 3] * rowscale);
+                  v.z = pack_bf16x2(q[g8 * 8 + 4] * rowscale, q[g8 * 8 + 5] * rowscale);
+                  v.w = pack_bf16x2(q[g8 * 8 + 6] * rowscale, q[g8 * 8 + 7] * rowscale);
+                  *reinterpret_cast<uint4*>(dst + g8 * 8) = v;
+                }
+              }
+            }
+          } else {
+            // EPI_STORE / EPI_ACCUM: C[row, col0 + i]
+            if (row < p.M) {
+              if (p.c_bf16) {
+                uint16_t* dst = reinterpret_cast<uint16_t*>(p.C) + size_t(row) * p.ldc + col0;
+#pragma unroll
+                for (int g8 = 0; g8 < 4; ++g8) {
+                  if (col0 + g8 * 8 + 8 <= p.N) {
+                    uint4 v;
+                    v.x = pack_bf16x2(x[g8 * 8 + 0], x[g8 * 8 + 1]);
+                    v.y = pack_bf16x2(x[g8 * 8 + 2], x[g8 * 8 + 3]);
+                    v.z = pack_bf16x2(x[g8 * 8 + 4], x[g8 * 8 + 5]);
+                    v.w = pack_bf16x2(x[g8 * 8 + 6], x[g8 * 8 + 7]);
+                    *reinterpret_cast<uint4*>(dst + g8 * 8) = v;
+                  }
+                }
+              } else {
+                float* dst = reinterpret_cast<float*>(p.C) + size_t(row) * p.ldc + col0;
+#pragma unroll
+                for (int g4 = 0; g4 < 8; ++g4) {
+                  if (col0 + g4 * 4 + 4 <= p.N) {
+                    float4 v = make_float4(x[g4 * 4 + 0], x[g4 * 4 + 1], x[g4 * 4 + 2], x[g4 * 4 + 3]);
+                    if (EPI == EPI_ACCUM) {
+                      const float4 o = *reinterpret_cast<const float4*>(dst + g4 * 4);
+                      v.x += o.x; v.y += o.y; v.z += o.z; v.w += o.w;
+                    }
+                    *reinterpret_cast<float4*>(dst + g4 * 4) = v;
+                  }
+                }
+              }
+            }
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(&tail->tempty[a]);
+      }
+      if (EPI == EPI_LSE && ok && row < p.rows) {
+        const int g = n_first / p.n_group;
+        p.partials[size_t(g) * (p.m_tiles * BM) + row] =
+            make_float4(run_m * scale2, run_s, run_g * p.inv_tau, 0.f);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) {
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+static int g_num_sms = 0;
+
+int gemm_max_grid() {
+  if (g_num_sms == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (g_num_sms <= 0) g_num_sms = 1;
+  }
+  return g_num_sms;
+}
+
+template <int EPI>
+static cudaError_t launch_one(const GemmProblem& p, const CUtensorMap& ta, const CUtensorMap& tb, int grid,
+                              cudaStream_t s) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(kd_gemm_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         int(GEMM_SMEM_BYTES));
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  kd_gemm_kernel<EPI><<<grid, GEMM_THREADS, GEMM_SMEM_BYTES, s>>>(ta, tb, p);
+  return cudaGetLastError();
+}
+
+static const char* gemm_name(int epi, int a_mn, int b_mn) {
+  switch (epi) {
+    case EPI_LSE: return "kd_proj_lse_fwd";
+    case EPI_DZ: return "kd_proj_dz_bwd";
+    case EPI_STORE: return (a_mn == 0 && b_mn == 1) ? "kd_gemm_dz_w" : "kd_gemm_store";
+    default: return (a_mn == 1 && b_mn == 1) ? "kd_gemm_dzT_h" : "kd_gemm_accum";
+  }
+}
+
+cudaError_t launch_gemm(const GemmProblem& p, const CUtensorMap& ta, const CUtensorMap& tb, int grid,
+                        cudaStream_t s) {
+  if (p.n_units <= 0) return cudaSuccess;
+  if (grid > p.n_units) grid = p.n_units;
+  prof_before(gemm_name(p.epi, p.a_mn, p.b_mn), s);
+  cudaError_t e;
+  switch (p.epi) {
+    case EPI_LSE: e = launch_one<EPI_LSE>(p, ta, tb, grid, s); break;
+    case EPI_DZ: e = launch_one<EPI_DZ>(p, ta, tb, grid, s); break;
+    case EPI_STORE: e = launch_one<EPI_STORE>(p, ta, tb, grid, s); break;
+    default: e = launch_one<EPI_ACCUM>(p, ta, tb, grid, s); break;
+  }
+  prof_after(s);
+  return e;
+}
+
+}  // namespace kd

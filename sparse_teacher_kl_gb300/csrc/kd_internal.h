@@ -1,0 +1,107 @@
+// Internal declarations shared by the translation units of libkdkl.so.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/kdkl.h"
+
+namespace kd {
+
+// Device error word codes (first word of every workspace; the second word
+// holds a detail, the third a launch tag).
+constexpr uint32_t KD_DEVERR_NONE = 0;
+constexpr uint32_t KD_DEVERR_TIMEOUT = 1;
+constexpr uint32_t KD_DEVERR_BAD_ID = 2;
+
+// Upper bound on any single wait inside a kernel.  A healthy wait lasts
+// microseconds; this only stops a kernel that would otherwise hang.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+
+// Workspace control block at offset 0 of every workspace.
+struct Ctrl {
+  uint32_t err;        // KD_DEVERR_*
+  uint32_t err_detail;
+  uint32_t pad0[2];
+  int32_t n_valid;     // number of valid positions of the current call
+  uint32_t pad1[59];
+};
+static_assert(sizeof(Ctrl) == 256, "control block is 256 bytes");
+
+// GEMM engine geometry: one CTA computes a 128 x 256 fp32 tile in tensor
+// memory, K staged 64 bf16 (128 B, one swizzle row) at a time.
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;
+constexpr int STAGES = 4;
+constexpr int STAGE_A_BYTES = BM * BK * 2;  // 16 KB
+constexpr int STAGE_B_BYTES = BN * BK * 2;  // 32 KB
+constexpr int STAGE_BYTES = STAGE_A_BYTES + STAGE_B_BYTES;
+constexpr int GEMM_THREADS = 192;           // TMA warp, MMA warp, 4 epilogue warps
+constexpr int TMEM_COLS = 512;              // two 256-column fp32 accumulators
+
+// Epilogue kinds of the GEMM engine.
+enum EpiKind : int {
+  EPI_LSE = 0,    // forward: online logsumexp + teacher-id gather -> partials
+  EPI_DZ = 1,     // backward: dZ = scale * (softmax - p) -> bf16 [rows, ldz]
+  EPI_STORE = 2,  // C = acc -> fp32 or bf16
+  EPI_ACCUM = 3,  // C += acc (fp32)
+};
+
+struct GemmProblem {
+  int M, N, K;           // logical GEMM sizes
+  int a_mn, b_mn;        // operand major-ness (0 = K-major)
+  int epi;               // EpiKind
+  // tile schedule: tiles are (m_blk, n_blk); n_group consecutive n tiles form
+  // one unit processed by one CTA in order (used by EPI_LSE).
+  int m_tiles, n_tiles, n_group, n_units;
+  // EPI_STORE / EPI_ACCUM
+  void* C;
+  int64_t ldc;
+  int c_bf16;
+  // EPI_LSE / EPI_DZ (rows = tokens of the chunk, cols = vocabulary)
+  const int32_t* ids_sorted;  // [rows, K] ascending
+  const float* p_sorted;      // [rows, K] teacher probabilities matching ids_sorted
+  int Kt;                     // teacher K
+  float inv_tau;
+  float4* partials;           // EPI_LSE: [n_units_per_row, rows] (m2, s, G, 0)
+  const float* lse;           // EPI_DZ: [rows] natural-log lse (chunk-relative pointer)
+  const uint8_t* mask;        // EPI_DZ: [rows] or null (chunk-relative pointer)
+  const float* grad_loss;     // EPI_DZ: device scalar
+  const int32_t* n_valid;     // EPI_DZ: device scalar
+  uint16_t* dz;               // EPI_DZ: bf16 [rows, ldz]
+  int64_t ldz;
+  int rows;                   // valid rows of A (tokens in this chunk) for LSE/DZ
+  uint32_t* err;
+};
+
+// Host helpers (kd_tma.cpp part of kd_abi.cu).
+bool make_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                       uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer);
+
+// Launchers (return a cudaError_t).
+cudaError_t launch_gemm(const GemmProblem& p, const CUtensorMap& ta, const CUtensorMap& tb, int grid,
+                        cudaStream_t s);
+int gemm_max_grid();
+
+cudaError_t launch_topk(const uint16_t* X, int64_t N, int64_t V, int64_t ld, int K, int32_t* ids,
+                        float* vals, uint32_t* err, cudaStream_t s);
+
+cudaError_t launch_count_valid(const uint8_t* mask, int64_t N, int32_t* n_valid, cudaStream_t s);
+cudaError_t launch_teacher_prologue(const int32_t* ids, const float* tlog, int rows, int K, int64_t V,
+                                    float inv_tau, int32_t* ids_sorted, float* p_sorted, float* negent,
+                                    uint32_t* err, int64_t row0, cudaStream_t s);
+cudaError_t launch_lse_combine(const float4* partials, int n_units_per_row, int rows, const float* negent,
+                               float inv_tau, float* lse_out, float* kl_out, cudaStream_t s);
+cudaError_t launch_loss_reduce(const float* kl, const uint8_t* mask, int64_t N, const int32_t* n_valid,
+                               float* loss_out, cudaStream_t s);
+
+cudaError_t launch_wait_timeout(uint32_t* err, uint64_t limit_ns, cudaStream_t s);
+
+// Profiling hooks (kd_abi.cu): bracket a launch with events when enabled.
+void prof_before(const char* name, cudaStream_t s);
+void prof_after(cudaStream_t s);
+
+}  // namespace kd

@@ -1,0 +1,226 @@
+// Row-wise steps around the projection engine: the sparse teacher prologue,
+// the merge of per-unit logsumexp partials into per-position KL, the masked
+// token-mean reduction and the valid-position count.  All O(N * K) or
+// O(N * V / 256) work, a small share of a step.
+#include <math.h>
+#include <stdint.h>
+
+#include "kd_device.cuh"
+#include "kd_internal.h"
+
+namespace kd {
+
+// ---------------------------------------------------------- valid count ---
+
+__global__ void kd_count_valid_kernel(const uint8_t* __restrict__ mask, int64_t N, int32_t* __restrict__ n_valid) {
+  __shared__ int32_t warp_sums[32];
+  int32_t c = 0;
+  if (mask == nullptr) {
+    if (threadIdx.x == 0) *n_valid = int32_t(N);
+    return;
+  }
+  for (int64_t i = threadIdx.x; i < N; i += blockDim.x) c += mask[i] != 0;
+  for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+  if ((threadIdx.x & 31) == 0) warp_sums[threadIdx.x >> 5] = c;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    c = (threadIdx.x < (blockDim.x >> 5)) ? warp_sums[threadIdx.x] : 0;
+    for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+    if (threadIdx.x == 0) *n_valid = c;
+  }
+}
+
+cudaError_t launch_count_valid(const uint8_t* mask, int64_t N, int32_t* n_valid, cudaStream_t s) {
+  prof_before("kd_count_valid", s);
+  kd_count_valid_kernel<<<1, 1024, 0, s>>>(mask, N, n_valid);
+  prof_after(s);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------ teacher prologue ---
+// [ART] fused-loss paragraph (the teacher stays sparse) and offline-cache
+// paragraph: per position, p = softmax(t / tau) over the K cached logits (the
+// mass outside them dropped), its negative entropy sum_k p_k log p_k, and the
+// (id, p) pairs ordered by id so that the projection epilogue meets them in
+// vocabulary order.  One warp per position.
+
+constexpr int PRO_WARPS = 4;
+
+__global__ void __launch_bounds__(PRO_WARPS * 32)
+    kd_teacher_prologue_kernel(const int32_t* __restrict__ ids, const float* __restrict__ tlog, int rows, int K,
+                               int KP, int64_t V, float inv_tau, int32_t* __restrict__ ids_sorted,
+                               float* __restrict__ p_sorted, float* __restrict__ negent,
+                               uint32_t* __restrict__ err, int64_t row0) {
+  extern __shared__ unsigned long long pro_smem[];
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  unsigned long long* ent = pro_smem + size_t(warp) * KP;
+  const int row = blockIdx.x * PRO_WARPS + warp;
+  if (row >= rows) return;
+  const int32_t* idr = ids + size_t(row) * K;
+  const float* tr = tlog + size_t(row) * K;
+
+  float m = -INFINITY;
+  for (int k = lane; k < K; k += 32) m = fmaxf(m, tr[k] * inv_tau);
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  float s = 0.f;
+  for (int k = lane; k < K; k += 32) s += expf(tr[k] * inv_tau - m);
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  const float log_s = logf(s);
+  float h = 0.f;
+  bool bad = false;
+  for (int k = lane; k < KP; k += 32) {
+    unsigned long long e = ~0ull;
+    if (k < K) {
+      const float lp = tr[k] * inv_tau - m - log_s;
+      const float pk = expf(lp);
+      if (pk > 0.f) h += pk * lp;
+      const int32_t id = idr[k];
+      bad |= (id < 0) || (int64_t(id) >= V);
+      e = (static_cast<unsigned long long>(uint32_t(id)) << 32) | __float_as_uint(pk);
+    }
+    ent[k] = e;
+  }
+  for (int o = 16; o > 0; o >>= 1) h += __shfl_xor_sync(0xffffffffu, h, o);
+  if (__any_sync(0xffffffffu, bad) && lane == 0) raise_error(err, KD_DEVERR_BAD_ID, uint32_t(row0 + row));
+  __syncwarp();
+  // bitonic sort, ascending by id
+  for (int k = 2; k <= KP; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = lane; i < KP; i += 32) {
+        const int ixj = i ^ j;
+        if (ixj > i) {
+          const unsigned long long a = ent[i], b = ent[ixj];
+          const bool asc = (i & k) == 0;
+          if (asc ? (a > b) : (a < b)) {
+            ent[i] = b;
+            ent[ixj] = a;
+          }
+        }
+      }
+      __syncwarp();
+    }
+  }
+  for (int k = lane; k < K; k += 32) {
+    const unsigned long long e = ent[k];
+    ids_sorted[size_t(row) * K + k] = int32_t(uint32_t(e >> 32));
+    p_sorted[size_t(row) * K + k] = __uint_as_float(uint32_t(e));
+  }
+  if (lane == 0) negent[row] = h;
+}
+
+cudaError_t launch_teacher_prologue(const int32_t* ids, const float* tlog, int rows, int K, int64_t V,
+                                    float inv_tau, int32_t* ids_sorted, float* p_sorted, float* negent,
+                                    uint32_t* err, int64_t row0, cudaStream_t s) {
+  int KP = 32;
+  while (KP < K) KP <<= 1;
+  const size_t smem = size_t(PRO_WARPS) * KP * sizeof(unsigned long long);
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(kd_teacher_prologue_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         int(PRO_WARPS * 1024 * sizeof(unsigned long long)));
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const int grid = (rows + PRO_WARPS - 1) / PRO_WARPS;
+  prof_before("kd_teacher_prologue", s);
+  kd_teacher_prologue_kernel<<<grid, PRO_WARPS * 32, smem, s>>>(ids, tlog, rows, K, KP, V, inv_tau, ids_sorted,
+                                                                p_sorted, negent, err, row0);
+  prof_after(s);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------- lse combine ---
+// Merge the per-unit (max, sum, gather) partials of each position into
+//   lse_t = ln 2 * (M + log2 sum_u s_u 2^(m_u - M)),  KL_t = negent_t - G_t + lse_t
+// ([ART] fused-loss paragraph: the running accumulator of the fused loss).
+
+__global__ void kd_lse_combine_kernel(const float4* __restrict__ partials, int n_units, int rows, int rows_pad,
+                                      const float* __restrict__ negent, float* __restrict__ lse_out,
+                                      float* __restrict__ kl_out) {
+  const int r = blockIdx.x * blockDim.x + threadIdx.x;
+  if (r >= rows) return;
+  float M = -INFINITY;
+  for (int u = 0; u < n_units; ++u) M = fmaxf(M, partials[size_t(u) * rows_pad + r].x);
+  float S = 0.f, G = 0.f;
+  for (int u = 0; u < n_units; ++u) {
+    const float4 q = partials[size_t(u) * rows_pad + r];
+    if (q.x != -INFINITY) S += q.y * exp2f(q.x - M);
+    G += q.z;
+  }
+  const float lse = (M + log2f(S)) * 0.69314718055994531f;
+  lse_out[r] = lse;
+  kl_out[r] = negent[r] - G + lse;
+}
+
+cudaError_t launch_lse_combine(const float4* partials, int n_units_per_row, int rows, const float* negent,
+                               float inv_tau, float* lse_out, float* kl_out, cudaStream_t s) {
+  (void)inv_tau;
+  const int rows_pad = ((rows + BM - 1) / BM) * BM;
+  prof_before("kd_lse_combine", s);
+  kd_lse_combine_kernel<<<(rows + 255) / 256, 256, 0, s>>>(partials, n_units_per_row, rows, rows_pad, negent,
+                                                           lse_out, kl_out);
+  prof_after(s);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------- loss reduce ---
+// loss = sum over valid positions of KL_t / N_valid, 0 if none ([ART] drop-in
+// KL term; the token mean with a padding mask).  One block, fixed summation
+// order in fp64, so the result is deterministic.
+
+__global__ void __launch_bounds__(1024)
+    kd_loss_reduce_kernel(const float* __restrict__ kl, const uint8_t* __restrict__ mask, int64_t N,
+                          const int32_t* __restrict__ n_valid, float* __restrict__ loss_out) {
+  __shared__ double sh[1024];
+  double acc = 0.0;
+  for (int64_t i = threadIdx.x; i < N; i += blockDim.x)
+    if (mask == nullptr || mask[i] != 0) acc += double(kl[i]);
+  sh[threadIdx.x] = acc;
+  __syncthreads();
+  for (int w = blockDim.x >> 1; w > 0; w >>= 1) {
+    if (int(threadIdx.x) < w) sh[threadIdx.x] += sh[threadIdx.x + w];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    const int nv = *n_valid;
+    *loss_out = nv > 0 ? float(sh[0] / double(nv)) : 0.f;
+  }
+}
+
+cudaError_t launch_loss_reduce(const float* kl, const uint8_t* mask, int64_t N, const int32_t* n_valid,
+                               float* loss_out, cudaStream_t s) {
+  prof_before("kd_loss_reduce", s);
+  kd_loss_reduce_kernel<<<1, 1024, 0, s>>>(kl, mask, N, n_valid, loss_out);
+  prof_after(s);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------- bounded-wait check ---
+// Waits on an mbarrier that nothing ever arrives at, with the same bounded
+// wait the projection engine uses, so that a test can see the wait give up and
+// report KD_ERR_TIMEOUT through the workspace error word.
+
+__global__ void kd_wait_timeout_kernel(uint32_t* err, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ uint32_t abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    mbar_wait(&bar, 0, &abort_flag, err, 0x7e57u, limit_ns);
+  }
+  __syncthreads();
+}
+
+cudaError_t launch_wait_timeout(uint32_t* err, uint64_t limit_ns, cudaStream_t s) {
+  prof_before("kd_wait_timeout", s);
+  kd_wait_timeout_kernel<<<1, 32, 0, s>>>(err, limit_ns);
+  prof_after(s);
+  return cudaGetLastError();
+}
+
+}  // namespace kd

@@ -1,0 +1,273 @@
+// Offline top-K teacher cache: the K largest logits of every row of a dense
+// bf16 [N, V] teacher-logits matrix, with their token ids ([ART] paragraph on
+// the first fix; [DAI] "As duas inovações" item 1; [EPO] "Los dos cambios
+// propuestos", first item).
+//
+// HBM-bound: every logit is read exactly once, in 16-byte vectors, by one CTA
+// per row (grid-strided over rows).  Each element becomes a 48-bit composite
+//   (order-preserving 16-bit key of the bf16 value) << 32 | (~column)
+// which is unique per element and orders by value descending, then column
+// ascending; the top-K are the K largest composites.  The row streams through
+// in segments of 4096 elements; a candidate buffer in shared memory receives
+// every element that can still make the top K.  When the buffer passes half
+// full, the K-th largest key T in it is found with two byte histograms and
+// only entries with key >= T are kept; from then on an element needs key > T
+// (any later element with key == T has a larger column and ranks below the K
+// kept ones).  The survivors are sorted once at the end.
+#include <stdint.h>
+
+#include "kd_device.cuh"
+#include "kd_internal.h"
+
+namespace kd {
+
+constexpr int TK_THREADS = 512;
+constexpr int TK_VEC = 8;                      // bf16 per 16-byte load
+constexpr int TK_SEG = TK_THREADS * TK_VEC;    // elements per segment
+constexpr int TK_CAP = 2 * TK_SEG;             // candidate buffer entries
+constexpr int TK_PIPE = 4;                     // segments in flight per thread
+constexpr int TK_HOLD = TK_CAP / TK_THREADS;   // buffer entries per thread
+
+struct TopkSmem {
+  unsigned long long buf[TK_CAP];
+  uint32_t hist[256];
+  uint32_t count;
+  uint32_t sel_bin;
+  uint32_t sel_need;
+  uint32_t sel_above;
+};
+
+// bf16 bits -> unsigned key with the same order as the values (-0 == +0).
+__device__ __forceinline__ uint32_t bf16_key(uint32_t b) {
+  b &= 0xFFFFu;
+  if (b == 0x8000u) b = 0u;
+  return (b & 0x8000u) ? (~b & 0xFFFFu) : (b | 0x8000u);
+}
+
+__device__ __forceinline__ uint32_t comp_key(unsigned long long c) { return uint32_t(c >> 32); }
+
+// Warp 0 finds, scanning bins from the top, the bin where the running count
+// reaches `target`; stores the bin, the count still needed inside it and the
+// count strictly above it.
+__device__ void find_bin_from_top(TopkSmem& sm, uint32_t target) {
+  if (threadIdx.x < 32) {
+    const uint32_t lane = threadIdx.x;
+    uint32_t local[8];
+    uint32_t sum = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      local[j] = sm.hist[255 - (lane * 8 + j)];
+      sum += local[j];
+    }
+    uint32_t incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= uint32_t(o)) incl += t;
+    }
+    const uint32_t excl = incl - sum;
+    if (excl < target && target <= incl) {
+      uint32_t run = excl;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (run < target && target <= run + local[j]) {
+          sm.sel_bin = 255 - (lane * 8 + j);
+          sm.sel_need = target - run;
+          sm.sel_above = run;
+        }
+        run += local[j];
+      }
+    }
+  }
+}
+
+// K-th largest key among buf[0, count) (count >= K); also returns how many
+// entries have key >= that value.
+__device__ uint32_t kth_largest_key(TopkSmem& sm, uint32_t count, uint32_t K, uint32_t& count_ge) {
+  for (int i = threadIdx.x; i < 256; i += TK_THREADS) sm.hist[i] = 0;
+  __syncthreads();
+  for (uint32_t i = threadIdx.x; i < count; i += TK_THREADS) atomicAdd(&sm.hist[comp_key(sm.buf[i]) >> 8], 1u);
+  __syncthreads();
+  find_bin_from_top(sm, K);
+  __syncthreads();
+  const uint32_t b1 = sm.sel_bin, need = sm.sel_need, above1 = sm.sel_above;
+  __syncthreads();
+  for (int i = threadIdx.x; i < 256; i += TK_THREADS) sm.hist[i] = 0;
+  __syncthreads();
+  for (uint32_t i = threadIdx.x; i < count; i += TK_THREADS) {
+    const uint32_t k = comp_key(sm.buf[i]);
+    if ((k >> 8) == b1) atomicAdd(&sm.hist[k & 255u], 1u);
+  }
+  __syncthreads();
+  find_bin_from_top(sm, need);
+  __syncthreads();
+  const uint32_t b2 = sm.sel_bin;
+  count_ge = above1 + sm.sel_above + sm.hist[b2];
+  __syncthreads();
+  return (b1 << 8) | b2;
+}
+
+// Append `c` (if `take`) to sm.buf with one shared atomic per warp.
+__device__ __forceinline__ void warp_append(TopkSmem& sm, bool take, unsigned long long c) {
+  const uint32_t ballot = __ballot_sync(0xffffffffu, take);
+  if (ballot == 0) return;
+  const uint32_t lane = lane_id();
+  uint32_t base = 0;
+  if (lane == 0) base = atomicAdd(&sm.count, uint32_t(__popc(ballot)));
+  base = __shfl_sync(0xffffffffu, base, 0);
+  if (take) sm.buf[base + __popc(ballot & ((1u << lane) - 1u))] = c;
+}
+
+// Keep only the entries with key >= T (in place).
+__device__ void filter_ge(TopkSmem& sm, uint32_t count, uint32_t T) {
+  unsigned long long held[TK_HOLD];
+#pragma unroll
+  for (int j = 0; j < TK_HOLD; ++j) {
+    const uint32_t i = threadIdx.x + j * TK_THREADS;
+    held[j] = (i < count) ? sm.buf[i] : 0ull;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) sm.count = 0;
+  __syncthreads();
+#pragma unroll
+  for (int j = 0; j < TK_HOLD; ++j) {
+    const uint32_t i = threadIdx.x + j * TK_THREADS;
+    warp_append(sm, i < count && comp_key(held[j]) >= T, held[j]);
+  }
+  __syncthreads();
+}
+
+// Sort buf[0, count) descending (bitonic over the next power of two, padded
+// with 0, which is below every real composite).
+__device__ void sort_desc(TopkSmem& sm, uint32_t count) {
+  uint32_t P = 1;
+  while (P < count) P <<= 1;
+  for (uint32_t i = count + threadIdx.x; i < P; i += TK_THREADS) sm.buf[i] = 0ull;
+  __syncthreads();
+  for (uint32_t k = 2; k <= P; k <<= 1) {
+    for (uint32_t j = k >> 1; j > 0; j >>= 1) {
+      for (uint32_t i = threadIdx.x; i < P; i += TK_THREADS) {
+        const uint32_t ixj = i ^ j;
+        if (ixj > i) {
+          const unsigned long long a = sm.buf[i], b = sm.buf[ixj];
+          const bool desc = (i & k) == 0;
+          if (desc ? (a < b) : (a > b)) {
+            sm.buf[i] = b;
+            sm.buf[ixj] = a;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+}
+
+// Bring the buffer back to at most TK_CAP - TK_SEG entries, all of them able
+// to reach the top K; returns the new acceptance threshold (key must exceed it).
+__device__ int compact(TopkSmem& sm, uint32_t K) {
+  const uint32_t count = sm.count;
+  uint32_t count_ge = 0;
+  const uint32_t T = kth_largest_key(sm, count, K, count_ge);
+  if (count_ge <= uint32_t(TK_CAP - TK_SEG)) {
+    if (count_ge < count) filter_ge(sm, count, T);
+    return int(T);
+  }
+  // Too many ties at T: order fully and keep exactly the K best.
+  sort_desc(sm, count);
+  if (threadIdx.x == 0) sm.count = K;
+  __syncthreads();
+  return int(comp_key(sm.buf[K - 1]));
+}
+
+__device__ __forceinline__ uint4 load_seg(const uint16_t* xr, int64_t V, int seg) {
+  const int64_t i0 = int64_t(seg) * TK_SEG + int64_t(threadIdx.x) * TK_VEC;
+  if (i0 + TK_VEC <= V) return __ldcs(reinterpret_cast<const uint4*>(xr + i0));
+  uint32_t w[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+  for (int e = 0; e < TK_VEC; ++e)
+    if (i0 + e < V) w[e >> 1] |= uint32_t(xr[i0 + e]) << (16 * (e & 1));
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+__global__ void __launch_bounds__(TK_THREADS, 2)
+    kd_topk_kernel(const uint16_t* __restrict__ X, int64_t N, int64_t V, int64_t ld, int K,
+                   int32_t* __restrict__ ids_out, float* __restrict__ vals_out) {
+  extern __shared__ __align__(16) uint8_t tk_smem_raw[];
+  TopkSmem& sm = *reinterpret_cast<TopkSmem*>(tk_smem_raw);
+  const int nseg = int((V + TK_SEG - 1) / TK_SEG);
+
+  for (int64_t row = blockIdx.x; row < N; row += gridDim.x) {
+    const uint16_t* xr = X + row * ld;
+    if (threadIdx.x == 0) sm.count = 0;
+    int thresh = -1;  // accept every element until the first compaction
+    uint4 pipe[TK_PIPE];
+#pragma unroll
+    for (int j = 0; j < TK_PIPE; ++j)
+      if (j < nseg) pipe[j] = load_seg(xr, V, j);
+    __syncthreads();
+
+    for (int base = 0; base < nseg; base += TK_PIPE) {
+#pragma unroll
+      for (int j = 0; j < TK_PIPE; ++j) {
+        const int seg = base + j;
+        if (seg < nseg) {
+          const uint4 v = pipe[j];
+          if (seg + TK_PIPE < nseg) pipe[j] = load_seg(xr, V, seg + TK_PIPE);
+          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+          const int64_t i0 = int64_t(seg) * TK_SEG + int64_t(threadIdx.x) * TK_VEC;
+#pragma unroll
+          for (int e = 0; e < TK_VEC; ++e) {
+            const uint32_t key = bf16_key(w[e >> 1] >> (16 * (e & 1)));
+            const bool take = (i0 + e < V) && int(key) > thresh;
+            const unsigned long long c =
+                (static_cast<unsigned long long>(key) << 32) | uint32_t(~uint32_t(i0 + e));
+            warp_append(sm, take, c);
+          }
+          __syncthreads();
+          const uint32_t cnt = sm.count;
+          __syncthreads();  // every thread has read the count before anyone appends again
+          if (cnt > uint32_t(TK_CAP - TK_SEG)) thresh = compact(sm, uint32_t(K));
+        }
+      }
+    }
+
+    // Final: keep the candidates that can be in the top K, order them, emit K.
+    __syncthreads();
+    uint32_t count = sm.count;
+    __syncthreads();
+    if (count > uint32_t(K)) {
+      uint32_t count_ge = 0;
+      const uint32_t T = kth_largest_key(sm, count, uint32_t(K), count_ge);
+      if (count_ge < count) filter_ge(sm, count, T);
+      count = sm.count;
+    }
+    sort_desc(sm, count);
+    for (int j = threadIdx.x; j < K; j += TK_THREADS) {
+      const uint32_t col = ~uint32_t(sm.buf[j]);
+      ids_out[row * K + j] = int32_t(col);
+      vals_out[row * K + j] = __uint_as_float(uint32_t(xr[col]) << 16);
+    }
+    __syncthreads();
+  }
+}
+
+cudaError_t launch_topk(const uint16_t* X, int64_t N, int64_t V, int64_t ld, int K, int32_t* ids, float* vals,
+                        uint32_t* err, cudaStream_t s) {
+  (void)err;
+  static bool attr_set = false;
+  const int smem = int(sizeof(TopkSmem));
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(kd_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  int grid = 2 * gemm_max_grid();
+  if (int64_t(grid) > N) grid = int(N);
+  if (grid <= 0) return cudaSuccess;
+  prof_before("kd_topk_cache", s);
+  kd_topk_kernel<<<grid, TK_THREADS, smem, s>>>(X, N, V, ld, K, ids, vals);
+  prof_after(s);
+  return cudaGetLastError();
+}
+
+}  // namespace kd

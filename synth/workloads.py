@@ -67,6 +67,10 @@ def _distinct_ids(N: int, K: int, V: int, g: torch.Generator, device) -> torch.T
     The ids stay in draw order (not sorted), the way a cache of "the K most
     probable tokens" pairs each id with its logit.
     """
+    if K * K > V:
+        # dense case (K close to V): the first K of a random permutation per row
+        keys = torch.rand((N, V), generator=g, device=device)
+        return torch.argsort(keys, dim=1)[:, :K].to(torch.int32).contiguous()
     ids = torch.randint(0, V, (N, K), generator=g, device=device, dtype=torch.int64)
     if K > 1:
         for _ in range(1000):

@@ -1,0 +1,101 @@
+"""kd_topk_cache against the oracle's full sort: ids and values bit-exact."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from synth import WORKLOADS, bf16_bits, make_dense_teacher_logits
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def kd(cuda_device):
+    from sparse_teacher_kl_gb300.build import build_library
+    build_library()
+    import sparse_teacher_kl_gb300 as kd
+    return kd
+
+
+def _check(kd, X_host, K, dev, rows=None, ld=None):
+    """Run the GPU on X_host (bf16 [N, V], optionally inside a wider [N, ld] buffer); compare rows."""
+    N, V = X_host.shape
+    if ld is None and V % 8 != 0:
+        ld = (V + 7) // 8 * 8
+    if ld is not None and ld != V:
+        buf = torch.zeros((N, ld), dtype=torch.bfloat16)
+        buf[:, :V] = X_host
+        Xd = buf.to(dev)[:, :V]
+    else:
+        Xd = X_host.to(dev)
+    ids = torch.empty((N, K), dtype=torch.int32, device=dev)
+    vals = torch.empty((N, K), dtype=torch.float32, device=dev)
+    ws = kd.workspace(kd._abi.kd_topk_cache_workspace(N, V, K), dev)
+    st = kd._abi.kd_topk_cache(Xd.data_ptr(), N, V, Xd.stride(0), K, ids.data_ptr(), vals.data_ptr(),
+                               ws.data_ptr(), ws.numel(), torch.cuda.current_stream().cuda_stream)
+    assert st == 0
+    torch.cuda.synchronize()
+    rows = np.arange(N) if rows is None else np.asarray(rows)
+    bits = bf16_bits(X_host[torch.as_tensor(rows)])
+    rid, rval = oracle.topk_cache(bits, K)
+    gid = ids.cpu().numpy()[rows]
+    gval = vals.cpu().numpy()[rows]
+    assert np.array_equal(gid, rid), f"ids differ in {np.sum(np.any(gid != rid, axis=1))} rows"
+    assert np.array_equal(gval.view(np.uint32), rval.view(np.uint32)), "values differ"
+
+
+@pytest.mark.parametrize("N,V,K", [(64, 4096, 16), (33, 1000, 100), (8, 40000, 1024), (5, 8, 8), (3, 17, 1)])
+def test_topk_random(kd, cuda_device, N, V, K):
+    X = make_dense_teacher_logits(N, V, seed=N + V + K)
+    _check(kd, X, K, cuda_device)
+
+
+def test_topk_ties_and_signed_zero(kd, cuda_device):
+    g = torch.Generator().manual_seed(1)
+    N, V = 12, 20000
+    X = (torch.round(torch.randn((N, V), generator=g) * 2) / 2)
+    X[0] = 0.0                                   # all equal: lowest ids win
+    X[1, ::2] = -0.0                             # -0 == +0
+    X[2] = torch.linspace(-3, 3, V)              # ascending: every element enters the buffer
+    X[3] = torch.linspace(3, -3, V)              # descending
+    X[4, :] = float("-inf"); X[4, 5000:5003] = 1.0
+    X[5] = torch.round(torch.randn(V, generator=g)) * 0 + 7.0
+    X[5, 19990:] = 8.0                           # best values at the very end
+    X = X.to(torch.bfloat16)
+    for K in (1, 100, 1024):
+        _check(kd, X, K, cuda_device)
+
+
+def test_topk_strided_rows(kd, cuda_device):
+    X = make_dense_teacher_logits(20, 1001, seed=5)
+    _check(kd, X, 50, cuda_device, ld=1008)
+
+
+def test_topk_small_workload(kd, cuda_device):
+    w = WORKLOADS["small"]
+    X = make_dense_teacher_logits(256, w.V, seed=w.seed)
+    _check(kd, X, w.K, cuda_device)
+
+
+def test_topk_mid_workload_sampled(kd, cuda_device):
+    """The 8192 x 151936 dense teacher logits N(0, 2); the oracle checks a sample of rows."""
+    w = WORKLOADS["mid"]
+    X = make_dense_teacher_logits(w.N, w.V, seed=w.seed, device=cuda_device)
+    ids = torch.empty((w.N, w.K), dtype=torch.int32, device=cuda_device)
+    vals = torch.empty((w.N, w.K), dtype=torch.float32, device=cuda_device)
+    ws = kd.workspace(kd._abi.kd_topk_cache_workspace(w.N, w.V, w.K), cuda_device)
+    st = kd._abi.kd_topk_cache(X.data_ptr(), w.N, w.V, w.V, w.K, ids.data_ptr(), vals.data_ptr(),
+                               ws.data_ptr(), ws.numel(), torch.cuda.current_stream().cuda_stream)
+    assert st == 0
+    torch.cuda.synchronize()
+    rows = np.random.default_rng(0).choice(w.N, 48, replace=False)
+    rows = np.concatenate([rows, [0, w.N - 1]])
+    bits = bf16_bits(X[torch.as_tensor(rows, device=cuda_device)])
+    rid, rval = oracle.topk_cache(bits, w.K)
+    assert np.array_equal(ids.cpu().numpy()[rows], rid)
+    assert np.array_equal(vals.cpu().numpy()[rows].view(np.uint32), rval.view(np.uint32))
+    # every row: sorted descending, distinct ids
+    v = vals.cpu()
+    assert bool((v[:, 1:] <= v[:, :-1]).all())
+    s, _ = torch.sort(ids.cpu(), dim=1)
+    assert bool((s[:, 1:] != s[:, :-1]).all())
