@@ -148,11 +148,16 @@ def main():
     ap.add_argument("--cpu-rows", type=int, default=64)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--rows", type=int, default=None, help="override B*T (profiling a reduced case)")
+    ap.add_argument("--vocab", type=int, default=None, help="override V (profiling a reduced case)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
+    import dataclasses
     from synth import WORKLOADS
     w = WORKLOADS[args.workload]
+    if args.rows is not None or args.vocab is not None:
+        w = dataclasses.replace(w, name=f"{w.name}-reduced", B=1, T=args.rows or w.N, V=args.vocab or w.V)
     if args.impl == "reference":
         return run_reference(args, w)
 

@@ -148,6 +148,38 @@ KD_API int kd_fused_kl_bwd(const void* H_bf16, const void* W_bf16,
                     void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * Forward pass without a caller workspace, for callers that cannot allocate
+ * device memory (no counterpart in the paper: it is an integration variant).
+ * Some callers may not call cudaMalloc: plugins whose host framework owns all
+ * device memory through its own pre-sized pool, and latency-critical paths that
+ * cannot take the device-wide synchronisation cudaMalloc/cudaFree may cause;
+ * they cannot provide the workspace kd_fused_kl_fwd needs either.  This call
+ * computes exactly what kd_fused_kl_fwd computes (same arguments minus ws,
+ * ws_bytes), using a scratch array of KD_STATIC_SCRATCH_BYTES compiled into
+ * the library instead of a workspace:
+ *   - every GPU that loads the library holds that array until the process exits;
+ *   - the array's device address is looked up on the first call made with a
+ *     given device current, so make that first call before any stream capture;
+ *   - it returns KD_ERR_WORKSPACE, before any launch, when the problem needs more
+ *     than the array holds, i.e. when kd_fused_kl_workspace(N, d, V, K, chunk)
+ *     exceeds KD_STATIC_SCRATCH_BYTES;
+ *   - it allocates nothing; all calls share the one array, which keeps the last
+ *     call's contents (its control block is cleared at the start of each call),
+ *     so calls whose GPU work overlaps (other streams or host threads) race and
+ *     must be serialised by the caller;
+ *   - device-side conditions (a teacher id out of range) are recorded in the
+ *     shared array and are not reported by this variant.
+ * Argument errors that kd_fused_kl_fwd detects are returned as there; the
+ * scratch set-up and the clearing of its control block may already have been
+ * enqueued when an alignment or shape check fails.
+ */
+#define KD_STATIC_SCRATCH_BYTES (32u * 1024u * 1024u)
+KD_API int kd_fused_kl_fwd_static(const void* H_bf16, const void* W_bf16,
+                    const int32_t* t_ids, const float* t_logits, const uint8_t* mask,
+                    int64_t N, int64_t d, int64_t V, int K, int64_t chunk, float tau,
+                    float* loss_out, float* lse_out, float* kl_per_token_out, void* stream);
+
+/*
  * Reads (synchronising `stream`) and clears the device error word of a
  * workspace used by the calls above.  Returns KD_OK, KD_ERR_TIMEOUT or
  * KD_ERR_DEVICE; *detail_out (may be NULL) receives a call-specific detail

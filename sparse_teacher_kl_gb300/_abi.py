@@ -22,6 +22,7 @@ KD_ERR_CUDA = 4
 KD_ERR_TIMEOUT = 5
 KD_ERR_DEVICE = 6
 KD_MAX_K = 1024
+KD_STATIC_SCRATCH_BYTES = 32 * 1024 * 1024
 
 _c_i64 = ctypes.c_int64
 _c_ptr = ctypes.c_void_p
@@ -39,6 +40,8 @@ _SIGNATURES = {
                                  _c_float, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_size, _c_ptr]),
     "kd_fused_kl_bwd": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_i64, _c_i64, _c_i64, _c_int, _c_i64,
                                  _c_float, _c_ptr, _c_ptr, _c_ptr, _c_int, _c_ptr, _c_ptr, _c_size, _c_ptr]),
+    "kd_fused_kl_fwd_static": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_i64, _c_i64, _c_i64, _c_int,
+                                        _c_i64, _c_float, _c_ptr, _c_ptr, _c_ptr, _c_ptr]),
     "kd_get_device_error": (_c_int, [_c_ptr, _c_ptr, ctypes.POINTER(_c_i64)]),
     "kd_gemm_bf16": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_i64, _c_i64, _c_i64, _c_int, _c_int, _c_int, _c_ptr, _c_size,
                               _c_ptr]),
@@ -104,6 +107,7 @@ kd_topk_cache = _wrap("kd_topk_cache")
 kd_fused_kl_workspace = _wrap("kd_fused_kl_workspace")
 kd_fused_kl_fwd = _wrap("kd_fused_kl_fwd")
 kd_fused_kl_bwd = _wrap("kd_fused_kl_bwd")
+kd_fused_kl_fwd_static = _wrap("kd_fused_kl_fwd_static")
 kd_get_device_error = _wrap("kd_get_device_error")
 kd_gemm_bf16 = _wrap("kd_gemm_bf16")
 kd_gemm_workspace = _wrap("kd_gemm_workspace")
