@@ -97,6 +97,29 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def ncu_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch of ``kernel`` on ``workload`` from profiles/ncu_traffic.json,
+    or None when absent or taken from different kernel sources than the ones built now."""
+    from sparse_teacher_kl_gb300.build import source_digest
+    try:
+        with open(os.path.join(ROOT, "profiles", "ncu_traffic.json")) as f:
+            rec = json.load(f)
+    except Exception:
+        return None
+    if rec.get("source_digest") != source_digest():
+        return None
+    return rec.get("kernels", {}).get(workload, {}).get(kernel)
+
+
+def aggregate_over_ranks(ms_local: float, tokens_per_rank: int, world: int, all_reduce_max=None):
+    """Whole-job step time (max over ranks) and throughput (all ranks' tokens / that time).
+
+    ``all_reduce_max`` maps a float to its maximum over the ranks (identity on one rank).
+    """
+    ms = float(all_reduce_max(ms_local)) if (all_reduce_max is not None and world > 1) else float(ms_local)
+    return ms, world * tokens_per_rank / (ms * 1e-3)
+
+
 def cpu_oracle_seconds(Hb, Wb, ids, tlog, mask):
     """Wall time of the float64 oracle (fused formulation, fwd + bwd with full grad_W) on these rows."""
     import oracle
@@ -215,11 +238,12 @@ def main():
         torch.cuda.synchronize(dev)
     if world > 1:
         dist.barrier()
-    ms = e0.elapsed_time(e1) / args.steps
-    t_max = torch.tensor([ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t_max, op=dist.ReduceOp.MAX)
-    ms = float(t_max.item())
+    def rank_max(x):
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    ms, tokens_per_s = aggregate_over_ranks(e0.elapsed_time(e1) / args.steps, N, world, rank_max)
 
     # per-kernel breakdown from the library's own launch events
     summ = prof.summary()
@@ -234,7 +258,6 @@ def main():
     achieved = gemm_flops_per_chunk / (dom["avg_ms"] * 1e-3) / 1e12
     peak = peaks["bf16_sustained"]
 
-    tokens_per_s = world * N / (ms * 1e-3)
     tflops_exec = w.flops_executed() / (ms * 1e-3) / 1e12
 
     # ---- end to end through the public API with host buffers
@@ -271,12 +294,8 @@ def main():
             e2e_step()
         f1.record(stream)
         torch.cuda.synchronize(dev)
-        ems = f0.elapsed_time(f1) / args.steps
-        tm = torch.tensor([ems], dtype=torch.float64, device=dev)
-        if world > 1:
-            dist.all_reduce(tm, op=dist.ReduceOp.MAX)
-        ems = float(tm.item())
-        e2e = {"value": world * N / (ems * 1e-3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+        ems, e2e_rate = aggregate_over_ranks(f0.elapsed_time(f1) / args.steps, N, world, rank_max)
+        e2e = {"value": e2e_rate, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": 4, "ms_per_step": ems,
                "note": "pinned host H, teacher cache and mask copied in, loss copied out; W resident"}
 
@@ -307,7 +326,7 @@ def main():
             "workspace_gb": ws.numel() / 1e9,
             "resident_inputs_outputs_gb": base_alloc / 1e9,
             "roofline": {"bound": "tensor", "kernel": dom_name, "achieved": achieved, "peak": peak,
-                         "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
+                         "unit": "TFLOP/s", "frac": achieved / peak, "traffic": ncu_traffic(dom_name, w.name),
                          "peak_source": f"{peaks['source']} bf16 sustained",
                          "flops_per_launch": gemm_flops_per_chunk},
             "kernels": kernels,

@@ -46,6 +46,18 @@ def _digest(extra) -> str:
     return h.hexdigest()
 
 
+def source_digest() -> str:
+    """Digest of the CUDA sources and the public header (not of build flags): identifies
+    the kernels that an ncu capture was taken from."""
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(CSRC)) + ["../../include/kdkl.h"]:
+        path = os.path.normpath(os.path.join(CSRC, f))
+        with open(path, "rb") as fh:
+            h.update(os.path.basename(path).encode())
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
 def build_library(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
     extra = ["-Xptxas", "-v"] if ptxas_info else []
     os.makedirs(BUILD, exist_ok=True)

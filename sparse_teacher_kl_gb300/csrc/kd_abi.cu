@@ -52,17 +52,42 @@ static bool load_encode() {
   return g_encode != nullptr;
 }
 
-bool make_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
-                       uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer) {
+static bool make_tmap_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner,
+                         uint64_t outer, uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer) {
   if (!load_encode()) return false;
   const cuuint64_t dims[2] = {inner, outer};
   const cuuint64_t strides[1] = {row_stride_bytes};
   const cuuint32_t box[2] = {box_inner, box_outer};
   const cuuint32_t estr[2] = {1, 1};
-  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+  CUresult r = g_encode(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool make_tmap_dz_blocked(CUtensorMap* map, const void* base, uint64_t rows, uint64_t rows_pad, uint64_t nvb,
+                          uint32_t box_rows) {
+  if (!load_encode()) return false;
+  const cuuint64_t dims[3] = {64, rows, nvb};
+  const cuuint64_t strides[2] = {128, rows_pad * 128};
+  const cuuint32_t box[3] = {64, box_rows, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+bool make_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                       uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer) {
+  return make_tmap_2d(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, inner, outer, row_stride_bytes, box_inner,
+                      box_outer);
+}
+
+bool make_tmap_2d_f32(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                      uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer) {
+  return make_tmap_2d(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, base, inner, outer, row_stride_bytes, box_inner,
+                      box_outer);
 }
 
 // ---------------------------------------------------------- device check ---
@@ -85,8 +110,8 @@ static kd_status check_device() {
 static inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct KlLayout {
-  size_t ids_sorted, p_sorted, negent, kl, partials, dz, total;
-  int64_t ldz, rows_pad;
+  size_t ids_sorted, p_sorted, negent, kl, partials, dz, gh_part, total;
+  int64_t ldz, rows_pad, nvb;
   int n_groups;
 };
 
@@ -96,7 +121,6 @@ static int choose_n_group(int64_t V) {
 }
 
 static KlLayout kl_layout(int64_t N, int64_t d, int64_t V, int K, int64_t chunk) {
-  (void)d;
   KlLayout L{};
   const int64_t c = chunk < N ? chunk : N;
   L.rows_pad = (c + BM - 1) / BM * BM;
@@ -110,9 +134,29 @@ static KlLayout kl_layout(int64_t N, int64_t d, int64_t V, int K, int64_t chunk)
   L.negent = off;     off = align_up(off + size_t(L.rows_pad) * 4, 256);
   L.kl = off;         off = align_up(off + size_t(N) * 4, 256);
   L.partials = off;   off = align_up(off + size_t(L.n_groups) * L.rows_pad * 16, 256);
-  L.dz = off;         off = align_up(off + size_t(L.rows_pad) * L.ldz * 2, 256);
+  L.nvb = (V + 63) / 64;
+  L.dz = off;         off = align_up(off + size_t(L.nvb) * L.rows_pad * 128, 256);
+  L.gh_part = off;    off = align_up(off + size_t(KD_MAX_SPLITS) * L.rows_pad * size_t(d) * 4, 256);
   L.total = off;
   return L;
+}
+
+// Number of K splits for a product of `tiles` output tiles with `k_blocks` steps of
+// BK each: the fewest waves of `grid` persistent CTAs per unit of work, with a small
+// charge per split for the extra partial traffic.
+static int choose_splits(int64_t tiles, int k_blocks, int grid) {
+  int best = 1;
+  double best_cost = 1e300;
+  for (int S = 1; S <= KD_MAX_SPLITS; ++S) {
+    if (S > 1 && k_blocks / S < 32) break;
+    const double waves = double((tiles * S + grid - 1) / grid) / S;
+    const double cost = waves * (1.0 + 0.005 * (S - 1));
+    if (cost < best_cost - 1e-12) {
+      best_cost = cost;
+      best = S;
+    }
+  }
+  return best;
 }
 
 static bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -222,9 +266,10 @@ int kd_fused_kl_fwd(const void* H_bf16, const void* W_bf16, const int32_t* t_ids
     p.n_tiles = int((V + BN - 1) / BN);
     p.n_group = choose_n_group(V);
     p.n_units = p.m_tiles * ((p.n_tiles + p.n_group - 1) / p.n_group);
+    p.k_splits = 1;
     p.ids_sorted = ids_sorted; p.p_sorted = p_sorted; p.Kt = K; p.inv_tau = inv_tau;
     p.partials = partials; p.rows = n; p.err = &ctrl->err;
-    e = launch_gemm(p, th, tw, grid_max, s);
+    e = launch_gemm(p, th, tw, tw, grid_max, s);
     if (e != cudaSuccess) return KD_ERR_CUDA;
     e = launch_lse_combine(partials, L.n_groups, n, negent, inv_tau, lse_out + c0, kl + c0, s);
     if (e != cudaSuccess) return KD_ERR_CUDA;
@@ -257,8 +302,9 @@ int kd_fused_kl_bwd(const void* H_bf16, const void* W_bf16, const int32_t* t_ids
   const uint16_t* H = static_cast<const uint16_t*>(H_bf16);
   const size_t gh_elt = grad_H_is_fp32 ? 4 : 2;
 
-  alignas(64) CUtensorMap tw_k, tw_mn, th_k, th_mn, tdz_k, tdz_mn;
+  alignas(64) CUtensorMap tw_k, tw_mn, th_k, th_mn, tdz_k, tdz_mn, tdz_st, tgw;
   if (!make_tmap_2d_bf16(&tw_k, W_bf16, uint64_t(d), uint64_t(V), uint64_t(d) * 2, BK, BN)) return KD_ERR_CUDA;
+  if (!make_tmap_2d_f32(&tgw, grad_W, uint64_t(d), uint64_t(V), uint64_t(d) * 4, 32, 32)) return KD_ERR_CUDA;
   if (!make_tmap_2d_bf16(&tw_mn, W_bf16, uint64_t(d), uint64_t(V), uint64_t(d) * 2, 64, BK)) return KD_ERR_CUDA;
 
   cudaError_t e = launch_count_valid(mask, N, &ctrl->n_valid, s);
@@ -272,8 +318,10 @@ int kd_fused_kl_bwd(const void* H_bf16, const void* W_bf16, const int32_t* t_ids
     const uint16_t* Hc = H + c0 * d;
     if (!make_tmap_2d_bf16(&th_k, Hc, uint64_t(d), uint64_t(n), uint64_t(d) * 2, BK, BM)) return KD_ERR_CUDA;
     if (!make_tmap_2d_bf16(&th_mn, Hc, uint64_t(d), uint64_t(n), uint64_t(d) * 2, 64, BK)) return KD_ERR_CUDA;
-    if (!make_tmap_2d_bf16(&tdz_k, dz, uint64_t(V), uint64_t(n), uint64_t(L.ldz) * 2, BK, BM)) return KD_ERR_CUDA;
-    if (!make_tmap_2d_bf16(&tdz_mn, dz, uint64_t(V), uint64_t(n), uint64_t(L.ldz) * 2, 64, BK)) return KD_ERR_CUDA;
+    // dZ in blocked layout [vocab/64][row][64]: each box below is one contiguous run
+    if (!make_tmap_dz_blocked(&tdz_k, dz, uint64_t(n), uint64_t(L.rows_pad), uint64_t(L.nvb), BM)) return KD_ERR_CUDA;
+    if (!make_tmap_dz_blocked(&tdz_mn, dz, uint64_t(n), uint64_t(L.rows_pad), uint64_t(L.nvb), BK)) return KD_ERR_CUDA;
+    if (!make_tmap_dz_blocked(&tdz_st, dz, uint64_t(n), uint64_t(L.rows_pad), uint64_t(L.nvb), 32)) return KD_ERR_CUDA;
 
     // B1: recompute the chunk's logits, dZ -> bf16 workspace
     GemmProblem p{};
@@ -283,10 +331,11 @@ int kd_fused_kl_bwd(const void* H_bf16, const void* W_bf16, const int32_t* t_ids
     p.n_tiles = int((V + BN - 1) / BN);
     p.n_group = 1;
     p.n_units = p.m_tiles * p.n_tiles;
+    p.k_splits = 1;
     p.ids_sorted = ids_sorted; p.p_sorted = p_sorted; p.Kt = K; p.inv_tau = inv_tau;
     p.lse = lse + c0; p.mask = mask ? mask + c0 : nullptr; p.grad_loss = grad_loss; p.n_valid = &ctrl->n_valid;
     p.dz = dz; p.ldz = L.ldz; p.rows = n; p.err = &ctrl->err;
-    e = launch_gemm(p, th_k, tw_k, grid_max, s);
+    e = launch_gemm(p, th_k, tw_k, tdz_st, grid_max, s);
     if (e != cudaSuccess) return KD_ERR_CUDA;
 
     // B2: grad_H rows of the chunk = dZ W  (A = dZ K-major over V, B = W with d contiguous)
@@ -296,11 +345,26 @@ int kd_fused_kl_bwd(const void* H_bf16, const void* W_bf16, const int32_t* t_ids
     q.m_tiles = (n + BM - 1) / BM;
     q.n_tiles = int((d + BN - 1) / BN);
     q.n_group = 1;
-    q.n_units = q.m_tiles * q.n_tiles;
-    q.C = static_cast<uint8_t*>(grad_H) + size_t(c0) * d * gh_elt;
-    q.ldc = d; q.c_bf16 = grad_H_is_fp32 ? 0 : 1; q.err = &ctrl->err;
-    e = launch_gemm(q, tdz_k, tw_mn, grid_max, s);
+    q.a_blocked = 1;
+    q.k_splits = choose_splits(int64_t(q.m_tiles) * q.n_tiles, int((V + BK - 1) / BK), grid_max);
+    q.n_units = q.m_tiles * q.n_tiles * q.k_splits;
+    void* gh_out = static_cast<uint8_t*>(grad_H) + size_t(c0) * d * gh_elt;
+    if (q.k_splits == 1) {
+      q.C = gh_out;
+      q.ldc = d; q.c_bf16 = grad_H_is_fp32 ? 0 : 1;
+    } else {
+      q.C = w8 + L.gh_part;  // fp32 partial per split, summed in split order below
+      q.ldc = d; q.c_bf16 = 0;
+      q.split_stride = L.rows_pad * d;
+    }
+    q.err = &ctrl->err;
+    e = launch_gemm(q, tdz_k, tw_mn, tw_mn, grid_max, s);
     if (e != cudaSuccess) return KD_ERR_CUDA;
+    if (q.k_splits > 1) {
+      e = launch_split_reduce(reinterpret_cast<const float*>(w8 + L.gh_part), q.k_splits, L.rows_pad * d,
+                              int64_t(n) * d, gh_out, grad_H_is_fp32 ? 0 : 1, s);
+      if (e != cudaSuccess) return KD_ERR_CUDA;
+    }
 
     // B3: grad_W += dZ^T H_c  (A = dZ with V contiguous, B = H_c with d contiguous)
     GemmProblem r{};
@@ -309,9 +373,11 @@ int kd_fused_kl_bwd(const void* H_bf16, const void* W_bf16, const int32_t* t_ids
     r.m_tiles = int((V + BM - 1) / BM);
     r.n_tiles = int((d + BN - 1) / BN);
     r.n_group = 1;
+    r.a_blocked = 1;
+    r.k_splits = 1;
     r.n_units = r.m_tiles * r.n_tiles;
     r.C = grad_W; r.ldc = d; r.c_bf16 = 0; r.err = &ctrl->err;
-    e = launch_gemm(r, tdz_mn, th_mn, grid_max, s);
+    e = launch_gemm(r, tdz_mn, th_mn, tgw, grid_max, s);
     if (e != cudaSuccess) return KD_ERR_CUDA;
   }
   return KD_OK;
@@ -351,11 +417,12 @@ int kd_gemm_bf16(const void* A, const void* B, float* C, int64_t M, int64_t N, i
   if (!ws || !aligned(ws, 256) || ws_bytes < kd_gemm_workspace()) return KD_ERR_WORKSPACE;
   kd_status st = check_device();
   if (st != KD_OK) return st;
-  alignas(64) CUtensorMap ta, tb;
+  alignas(64) CUtensorMap ta, tb, tc;
   bool ok = a_mn ? make_tmap_2d_bf16(&ta, A, uint64_t(M), uint64_t(K), uint64_t(M) * 2, 64, BK)
                  : make_tmap_2d_bf16(&ta, A, uint64_t(K), uint64_t(M), uint64_t(K) * 2, BK, BM);
   ok = ok && (b_mn ? make_tmap_2d_bf16(&tb, B, uint64_t(N), uint64_t(K), uint64_t(N) * 2, 64, BK)
                    : make_tmap_2d_bf16(&tb, B, uint64_t(K), uint64_t(N), uint64_t(K) * 2, BK, BN));
+  ok = ok && make_tmap_2d_f32(&tc, C, uint64_t(N), uint64_t(M), uint64_t(N) * 4, 32, 32);
   if (!ok) return KD_ERR_CUDA;
   GemmProblem p{};
   p.M = int(M); p.N = int(N); p.K = int(K);
@@ -364,10 +431,11 @@ int kd_gemm_bf16(const void* A, const void* B, float* C, int64_t M, int64_t N, i
   p.m_tiles = int((M + BM - 1) / BM);
   p.n_tiles = int((N + BN - 1) / BN);
   p.n_group = 1;
+  p.k_splits = 1;
   p.n_units = p.m_tiles * p.n_tiles;
   p.C = C; p.ldc = N; p.c_bf16 = 0;
   p.err = &static_cast<Ctrl*>(ws)->err;
-  return map_cuda(launch_gemm(p, ta, tb, gemm_max_grid(), static_cast<cudaStream_t>(stream)));
+  return map_cuda(launch_gemm(p, ta, tb, tc, gemm_max_grid(), static_cast<cudaStream_t>(stream)));
 }
 
 int kd_profile_begin(int capacity) {

@@ -34,37 +34,51 @@ struct __align__(8) GemmSmemTail {
   uint32_t abort_flag;
 };
 
-constexpr size_t GEMM_SMEM_BYTES = 1024 /*alignment slack*/ + size_t(STAGES) * STAGE_BYTES + sizeof(GemmSmemTail);
+constexpr size_t GEMM_SMEM_BYTES =
+    1024 /*alignment slack*/ + size_t(STAGES) * STAGE_BYTES + STAGING_BYTES + sizeof(GemmSmemTail);
+static_assert(GEMM_SMEM_BYTES <= 232448, "shared memory budget of one CTA");
 
 // Unit u -> tile coordinates.  LSE/DZ walk the vocabulary (n) slowly so that
 // every CTA in flight reads the same few W tiles while the small H chunk stays
 // in L2; the gradient products walk n fastest so that CTAs in flight share A.
-__device__ __forceinline__ void unit_coords(const GemmProblem& p, int u, int& m_blk, int& n_first, int& n_count) {
+__device__ __forceinline__ void unit_coords(const GemmProblem& p, int u, int& m_blk, int& n_first, int& n_count,
+                                            int& kb_lo, int& kb_hi, int& split) {
+  const int k_blocks = (p.K + BK - 1) / BK;
   if (p.epi == EPI_LSE || p.epi == EPI_DZ) {
     const int g = u / p.m_tiles;
     m_blk = u - g * p.m_tiles;
     n_first = g * p.n_group;
     n_count = min(p.n_group, p.n_tiles - n_first);
+    kb_lo = 0;
+    kb_hi = k_blocks;
+    split = 0;
   } else {
-    m_blk = u / p.n_tiles;
-    n_first = u - m_blk * p.n_tiles;
+    // split slowest, then m, then n: the CTAs in flight share one K range, so each
+    // A slab is read by all n tiles and each B slab by all m tiles from L2.
+    const int per_split = p.m_tiles * p.n_tiles;
+    split = u / per_split;
+    const int r = u - split * per_split;
+    m_blk = r / p.n_tiles;
+    n_first = r - m_blk * p.n_tiles;
     n_count = 1;
+    kb_lo = int((int64_t(k_blocks) * split) / p.k_splits);
+    kb_hi = int((int64_t(k_blocks) * (split + 1)) / p.k_splits);
   }
 }
 
 template <int EPI>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     kd_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
-                   const GemmProblem p) {
+                   const __grid_constant__ CUtensorMap tmap_c, const GemmProblem p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stage_base = smem;
-  GemmSmemTail* tail = reinterpret_cast<GemmSmemTail*>(smem + size_t(STAGES) * STAGE_BYTES);
+  uint8_t* staging = smem + size_t(STAGES) * STAGE_BYTES;  // 1024-aligned output boxes of the epilogue warps
+  GemmSmemTail* tail = reinterpret_cast<GemmSmemTail*>(staging + STAGING_BYTES);
   volatile uint32_t* abort_flag = &tail->abort_flag;
 
   const uint32_t warp = threadIdx.x >> 5;
   const uint32_t lane = lane_id();
-  const int k_blocks = (p.K + BK - 1) / BK;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -82,6 +96,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_map(&tmap_a);
     tma_prefetch_map(&tmap_b);
+    if (EPI == EPI_ACCUM || EPI == EPI_DZ) tma_prefetch_map(&tmap_c);
   }
   if (warp == 1) {
     tmem_alloc(&tail->tmem_base, TMEM_COLS);
@@ -97,10 +112,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       uint32_t it = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x) {
-        int m_blk, n_first, n_count;
-        unit_coords(p, u, m_blk, n_first, n_count);
+        int m_blk, n_first, n_count, kb_lo, kb_hi, split;
+        unit_coords(p, u, m_blk, n_first, n_count, kb_lo, kb_hi, split);
         for (int nb = n_first; nb < n_first + n_count && ok; ++nb) {
-          for (int kb = 0; kb < k_blocks; ++kb, ++it) {
+          for (int kb = kb_lo; kb < kb_hi; ++kb, ++it) {
             const uint32_t s = it % STAGES;
             const uint32_t ph = (it / STAGES) & 1u;
             if (!mbar_wait(&tail->empty[s], ph ^ 1u, abort_flag, p.err, 0x100u)) {
@@ -110,7 +125,17 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             uint8_t* sa = stage_base + size_t(s) * STAGE_BYTES;
             uint8_t* sb = sa + STAGE_A_BYTES;
             mbar_arrive_expect_tx(&tail->full[s], STAGE_BYTES);
-            if (p.a_mn == 0) {
+            if (p.a_blocked) {
+              // blocked dZ [vocab/64][row][64]: K-major A walks vocabulary blocks; MN-major
+              // A takes the two 64-wide vocabulary blocks of its 128 rows
+              if (p.a_mn == 0) {
+                tma_load_3d(sa, &tmap_a, &tail->full[s], 0, m_blk * BM, kb);
+              } else {
+#pragma unroll
+                for (int j = 0; j < BM / 64; ++j)
+                  tma_load_3d(sa + j * 8192, &tmap_a, &tail->full[s], 0, kb * BK, m_blk * (BM / 64) + j);
+              }
+            } else if (p.a_mn == 0) {
               tma_load_2d(sa, &tmap_a, &tail->full[s], kb * BK, m_blk * BM);
             } else {
 #pragma unroll
@@ -147,8 +172,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       uint32_t it = 0, acc_it = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x) {
-        int m_blk, n_first, n_count;
-        unit_coords(p, u, m_blk, n_first, n_count);
+        int m_blk, n_first, n_count, kb_lo, kb_hi, split;
+        unit_coords(p, u, m_blk, n_first, n_count, kb_lo, kb_hi, split);
         for (int nb = n_first; nb < n_first + n_count && ok; ++nb, ++acc_it) {
           const uint32_t a = acc_it & 1u;
           const uint32_t aph = (acc_it >> 1) & 1u;
@@ -158,7 +183,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           }
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + a * BN;
-          for (int kb = 0; kb < k_blocks; ++kb, ++it) {
+          for (int kb = kb_lo; kb < kb_hi; ++kb, ++it) {
             const uint32_t s = it % STAGES;
             const uint32_t ph = (it / STAGES) & 1u;
             if (!mbar_wait(&tail->full[s], ph, abort_flag, p.err, 0x300u)) {
@@ -172,7 +197,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             for (int k = 0; k < BK / 16; ++k) {
               const uint64_t ad = sdesc_sw128(sa + k * a_step, a_lbo);
               const uint64_t bd = sdesc_sw128(sb + k * b_step, b_lbo);
-              umma_bf16(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+              umma_bf16(d_tmem, ad, bd, idesc, (kb != kb_lo || k != 0) ? 1u : 0u);
             }
             umma_commit(&tail->empty[s]);
           }
@@ -190,11 +215,13 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     const int r_local = int(quarter * 32u + lane);
     const uint32_t t_lane = tmem_base + ((quarter * 32u) << 16);
     const float scale2 = 1.4426950408889634f * p.inv_tau;  // log2(e) / tau
+    uint8_t* my_staging = staging + quarter * 8192u;        // two 4 KB boxes of this warp
+    uint32_t sbuf = 0;
     uint32_t acc_it = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x) {
-      int m_blk, n_first, n_count;
-      unit_coords(p, u, m_blk, n_first, n_count);
+      int m_blk, n_first, n_count, kb_lo, kb_hi, split;
+      unit_coords(p, u, m_blk, n_first, n_count, kb_lo, kb_hi, split);
       const int row = m_blk * BM + r_local;
 
       // Per-row state for the loss epilogues.
@@ -290,8 +317,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
               }
             }
           } else if (EPI == EPI_DZ) {
+            float q[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) q[i] = 0.f;
             if (row < p.rows) {
-              float q[32];
 #pragma unroll
               for (int i = 0; i < 32; ++i) q[i] = ex2_approx(fmaf(x[i], scale2, -lse2));
               while (nid < col0 + 32) {
@@ -311,24 +340,59 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 for (int i = 0; i < 32; ++i)
                   if (col0 + i >= p.N) q[i] = 0.f;
               }
-              uint16_t* dst = p.dz + size_t(row) * p.ldz + col0;
-#pragma unroll
-              for (int g8 = 0; g8 < 4; ++g8) {
-                if (col0 + g8 * 8 + 8 <= p.ldz) {
-                  uint4 v;
-                  v.x = pack_bf16x2(q[g8 * 8 + 0] * rowscale, q[g8 * 8 + 1] * rowscale);
-                  v.y = pack_bf16x2(q[g8 * 8 + 2] * rowscale, q[g8 * 8 + 3] * rowscale);
-                  v.z = pack_bf16x2(q[g8 * 8 + 4] * rowscale, q[g8 * 8 + 5] * rowscale);
-                  v.w = pack_bf16x2(q[g8 * 8 + 6] * rowscale, q[g8 * 8 + 7] * rowscale);
-                  *reinterpret_cast<uint4*>(dst + g8 * 8) = v;
-                }
-              }
             }
+            // Stage bf16 dZ for this warp's 32 rows: two 32-column chunks fill one 32 x 64
+            // box (128-byte rows, 128-byte swizzle), written out by one TMA store that clips
+            // rows past the chunk and columns past the vocabulary.
+            uint8_t* box = my_staging + sbuf * 4096u;
+            if ((c & 1) == 0) {
+              if (lane == 0) bulk_wait_read<1>();
+              __syncwarp();
+            }
+#pragma unroll
+            for (int g8 = 0; g8 < 4; ++g8) {
+              uint4 v;
+              v.x = pack_bf16x2(q[g8 * 8 + 0] * rowscale, q[g8 * 8 + 1] * rowscale);
+              v.y = pack_bf16x2(q[g8 * 8 + 2] * rowscale, q[g8 * 8 + 3] * rowscale);
+              v.z = pack_bf16x2(q[g8 * 8 + 4] * rowscale, q[g8 * 8 + 5] * rowscale);
+              v.w = pack_bf16x2(q[g8 * 8 + 6] * rowscale, q[g8 * 8 + 7] * rowscale);
+              const uint32_t j = uint32_t((c & 1) * 4 + g8);
+              *reinterpret_cast<uint4*>(box + lane * 128u + ((j ^ (lane & 7u)) * 16u)) = v;
+            }
+            if (c & 1) {
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                tma_store_3d(&tmap_c, box, 0, m_blk * BM + int(quarter) * 32, (col0 - 32) / 64);
+                bulk_commit();
+              }
+              sbuf ^= 1u;
+            }
+          } else if (EPI == EPI_ACCUM) {
+            // C[rows of this warp, col0 .. col0+31] += acc: stage the 32 x 32 fp32 box in shared
+            // memory (128-byte swizzle, conflict-free) and add it into C with one TMA reduction;
+            // the read-modify-write happens in L2, off the epilogue's critical path.
+            uint8_t* box = my_staging + sbuf * 4096u;
+            if (lane == 0) bulk_wait_read<1>();  // the group that last used this box has read it
+            __syncwarp();
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const uint32_t off = lane * 128u + ((uint32_t(j) ^ (lane & 7u)) * 16u);
+              *reinterpret_cast<float4*>(box + off) = make_float4(x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_reduce_add_2d(&tmap_c, box, col0, m_blk * BM + int(quarter) * 32);
+              bulk_commit();
+            }
+            sbuf ^= 1u;
           } else {
-            // EPI_STORE / EPI_ACCUM: C[row, col0 + i]
+            // EPI_STORE: C[row, col0 + i]
             if (row < p.M) {
               if (p.c_bf16) {
-                uint16_t* dst = reinterpret_cast<uint16_t*>(p.C) + size_t(row) * p.ldc + col0;
+                uint16_t* dst =
+                    reinterpret_cast<uint16_t*>(p.C) + size_t(split) * p.split_stride + size_t(row) * p.ldc + col0;
 #pragma unroll
                 for (int g8 = 0; g8 < 4; ++g8) {
                   if (col0 + g8 * 8 + 8 <= p.N) {
@@ -341,16 +405,13 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                   }
                 }
               } else {
-                float* dst = reinterpret_cast<float*>(p.C) + size_t(row) * p.ldc + col0;
+                float* dst =
+                    reinterpret_cast<float*>(p.C) + size_t(split) * p.split_stride + size_t(row) * p.ldc + col0;
 #pragma unroll
                 for (int g4 = 0; g4 < 8; ++g4) {
                   if (col0 + g4 * 4 + 4 <= p.N) {
-                    float4 v = make_float4(x[g4 * 4 + 0], x[g4 * 4 + 1], x[g4 * 4 + 2], x[g4 * 4 + 3]);
-                    if (EPI == EPI_ACCUM) {
-                      const float4 o = *reinterpret_cast<const float4*>(dst + g4 * 4);
-                      v.x += o.x; v.y += o.y; v.z += o.z; v.w += o.w;
-                    }
-                    *reinterpret_cast<float4*>(dst + g4 * 4) = v;
+                    *reinterpret_cast<float4*>(dst + g4 * 4) =
+                        make_float4(x[g4 * 4 + 0], x[g4 * 4 + 1], x[g4 * 4 + 2], x[g4 * 4 + 3]);
                   }
                 }
               }
@@ -366,6 +427,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             make_float4(run_m * scale2, run_s, run_g * p.inv_tau, 0.f);
       }
     }
+    if ((EPI == EPI_ACCUM || EPI == EPI_DZ) && lane == 0) bulk_wait_all();  // output boxes done before exit
   }
 
   tc_fence_before();
@@ -389,8 +451,8 @@ int gemm_max_grid() {
 }
 
 template <int EPI>
-static cudaError_t launch_one(const GemmProblem& p, const CUtensorMap& ta, const CUtensorMap& tb, int grid,
-                              cudaStream_t s) {
+static cudaError_t launch_one(const GemmProblem& p, const CUtensorMap& ta, const CUtensorMap& tb,
+                              const CUtensorMap& tc, int grid, cudaStream_t s) {
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kd_gemm_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -398,7 +460,7 @@ static cudaError_t launch_one(const GemmProblem& p, const CUtensorMap& ta, const
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  kd_gemm_kernel<EPI><<<grid, GEMM_THREADS, GEMM_SMEM_BYTES, s>>>(ta, tb, p);
+  kd_gemm_kernel<EPI><<<grid, GEMM_THREADS, GEMM_SMEM_BYTES, s>>>(ta, tb, tc, p);
   return cudaGetLastError();
 }
 
@@ -411,17 +473,17 @@ static const char* gemm_name(int epi, int a_mn, int b_mn) {
   }
 }
 
-cudaError_t launch_gemm(const GemmProblem& p, const CUtensorMap& ta, const CUtensorMap& tb, int grid,
-                        cudaStream_t s) {
+cudaError_t launch_gemm(const GemmProblem& p, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
+                        int grid, cudaStream_t s) {
   if (p.n_units <= 0) return cudaSuccess;
   if (grid > p.n_units) grid = p.n_units;
   prof_before(gemm_name(p.epi, p.a_mn, p.b_mn), s);
   cudaError_t e;
   switch (p.epi) {
-    case EPI_LSE: e = launch_one<EPI_LSE>(p, ta, tb, grid, s); break;
-    case EPI_DZ: e = launch_one<EPI_DZ>(p, ta, tb, grid, s); break;
-    case EPI_STORE: e = launch_one<EPI_STORE>(p, ta, tb, grid, s); break;
-    default: e = launch_one<EPI_ACCUM>(p, ta, tb, grid, s); break;
+    case EPI_LSE: e = launch_one<EPI_LSE>(p, ta, tb, tc, grid, s); break;
+    case EPI_DZ: e = launch_one<EPI_DZ>(p, ta, tb, tc, grid, s); break;
+    case EPI_STORE: e = launch_one<EPI_STORE>(p, ta, tb, tc, grid, s); break;
+    default: e = launch_one<EPI_ACCUM>(p, ta, tb, tc, grid, s); break;
   }
   prof_after(s);
   return e;

@@ -40,6 +40,7 @@ constexpr int STAGE_A_BYTES = BM * BK * 2;  // 16 KB
 constexpr int STAGE_B_BYTES = BN * BK * 2;  // 32 KB
 constexpr int STAGE_BYTES = STAGE_A_BYTES + STAGE_B_BYTES;
 constexpr int GEMM_THREADS = 192;           // TMA warp, MMA warp, 4 epilogue warps
+constexpr int STAGING_BYTES = 4 * 2 * 4096; // per epilogue warp: two 32 x 128 B output boxes
 constexpr int TMEM_COLS = 512;              // two 256-column fp32 accumulators
 
 // Epilogue kinds of the GEMM engine.
@@ -57,6 +58,14 @@ struct GemmProblem {
   // tile schedule: tiles are (m_blk, n_blk); n_group consecutive n tiles form
   // one unit processed by one CTA in order (used by EPI_LSE).
   int m_tiles, n_tiles, n_group, n_units;
+  // split-K (EPI_STORE): the K range is cut into k_splits nearly equal parts; the
+  // partial of split s goes to C + s * split_stride (elements).
+  int k_splits;
+  int64_t split_stride;
+  // blocked dZ: operand A (a_blocked) or the EPI_DZ output is the 3-D blocked layout
+  // dZ[vocab / 64][row][vocab % 64] (see make_tmap_dz_blocked), so that every TMA box
+  // of it is one contiguous run of memory.
+  int a_blocked;
   // EPI_STORE / EPI_ACCUM
   void* C;
   int64_t ldc;
@@ -80,10 +89,19 @@ struct GemmProblem {
 // Host helpers (kd_tma.cpp part of kd_abi.cu).
 bool make_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
                        uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer);
+// dZ chunk in blocked layout: [nvb = ceil(V/64)][rows_pad][64] bf16; dims {64, rows, nvb},
+// box {64, box_rows, 1}, 128-byte swizzle.
+bool make_tmap_dz_blocked(CUtensorMap* map, const void* base, uint64_t rows, uint64_t rows_pad, uint64_t nvb,
+                          uint32_t box_rows);
+bool make_tmap_2d_f32(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                      uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer);
 
 // Launchers (return a cudaError_t).
-cudaError_t launch_gemm(const GemmProblem& p, const CUtensorMap& ta, const CUtensorMap& tb, int grid,
-                        cudaStream_t s);
+// tc: output map for the epilogues that write through TMA (EPI_ACCUM: fp32 C,
+// box 32 x 32; EPI_DZ: bf16 dZ, box 64 x 32; both 128-byte swizzle); ignored
+// by the others.
+cudaError_t launch_gemm(const GemmProblem& p, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
+                        int grid, cudaStream_t s);
 int gemm_max_grid();
 
 cudaError_t launch_topk(const uint16_t* X, int64_t N, int64_t V, int64_t ld, int K, int32_t* ids,
@@ -99,6 +117,10 @@ cudaError_t launch_loss_reduce(const float* kl, const uint8_t* mask, int64_t N, 
                                float* loss_out, cudaStream_t s);
 
 cudaError_t launch_wait_timeout(uint32_t* err, uint64_t limit_ns, cudaStream_t s);
+cudaError_t launch_split_reduce(const float* parts, int splits, int64_t split_stride, int64_t count, void* out,
+                                int out_bf16, cudaStream_t s);
+
+constexpr int KD_MAX_SPLITS = 8;
 
 // Profiling hooks (kd_abi.cu): bracket a launch with events when enabled.
 void prof_before(const char* name, cudaStream_t s);

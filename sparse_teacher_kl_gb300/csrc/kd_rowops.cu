@@ -196,6 +196,43 @@ cudaError_t launch_loss_reduce(const float* kl, const uint8_t* mask, int64_t N, 
   return cudaGetLastError();
 }
 
+// -------------------------------------------------- split-K reduction ---
+// out[i] = sum over s of parts[s * stride + i], in split order (deterministic),
+// to bf16 or fp32.  count and stride are multiples of 4.
+
+__global__ void kd_split_reduce_kernel(const float4* __restrict__ parts, int splits, int64_t stride4,
+                                       int64_t count4, void* __restrict__ out, int out_bf16) {
+  for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < count4; i += int64_t(gridDim.x) * blockDim.x) {
+    float4 a = parts[i];
+    for (int sp = 1; sp < splits; ++sp) {
+      const float4 b = parts[sp * stride4 + i];
+      a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w;
+    }
+    if (out_bf16) {
+      uint2 v;
+      v.x = pack_bf16x2(a.x, a.y);
+      v.y = pack_bf16x2(a.z, a.w);
+      reinterpret_cast<uint2*>(out)[i] = v;
+    } else {
+      reinterpret_cast<float4*>(out)[i] = a;
+    }
+  }
+}
+
+cudaError_t launch_split_reduce(const float* parts, int splits, int64_t split_stride, int64_t count, void* out,
+                                int out_bf16, cudaStream_t s) {
+  const int64_t count4 = count / 4;
+  int grid = int((count4 + 255) / 256);
+  const int cap = 4 * gemm_max_grid();
+  if (grid > cap) grid = cap;
+  if (grid < 1) grid = 1;
+  prof_before("kd_split_reduce", s);
+  kd_split_reduce_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<const float4*>(parts), splits, split_stride / 4,
+                                              count4, out, out_bf16);
+  prof_after(s);
+  return cudaGetLastError();
+}
+
 // ------------------------------------------------- bounded-wait check ---
 // Waits on an mbarrier that nothing ever arrives at, with the same bounded
 // wait the projection engine uses, so that a test can see the wait give up and
