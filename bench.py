@@ -111,6 +111,42 @@ def ncu_traffic(kernel: str, workload: str):
     return rec.get("kernels", {}).get(workload, {}).get(kernel)
 
 
+def dense_torch_reference(H, W, ids, tlog, mask, dev):
+    """Peak device memory and time of one fwd+bwd of the dense formulation in plain PyTorch
+    (full [N, V] student logits and a full-vocabulary teacher grid), for the memory comparison
+    only; reports an estimate instead when it does not fit."""
+    import torch
+    N, V = H.shape[0], W.shape[0]
+    torch.cuda.synchronize(dev)
+    torch.cuda.empty_cache()
+    base = torch.cuda.memory_allocated(dev)
+    torch.cuda.reset_peak_memory_stats(dev)
+    try:
+        Hr = H.detach().requires_grad_(True)
+        Wr = W.detach().requires_grad_(True)
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record()
+        logq = torch.log_softmax((Hr @ Wr.T).float(), dim=1)
+        grid = torch.full((N, V), float("-inf"), device=dev)
+        grid.scatter_(1, ids.long(), tlog)
+        logp = torch.log_softmax(grid, dim=1)
+        p = logp.exp()
+        kl = (p * (torch.where(p > 0, logp, torch.zeros_like(logp)) - logq)).sum(dim=1)
+        m = torch.ones(N, device=dev) if mask is None else mask.float()
+        loss = (kl * m).sum() / m.sum()
+        loss.backward()
+        t1.record()
+        torch.cuda.synchronize(dev)
+        out = {"peak_device_gb": (torch.cuda.max_memory_allocated(dev) - base) / 1e9,
+               "ms_per_step": t0.elapsed_time(t1), "fits": True}
+        del Hr, Wr, logq, grid, logp, p, kl, loss
+    except torch.OutOfMemoryError:
+        out = {"fits": False, "estimate_gb": N * V * 4 * 5 / 1e9}
+    torch.cuda.empty_cache()
+    return out
+
+
 def aggregate_over_ranks(ms_local: float, tokens_per_rank: int, world: int, all_reduce_max=None):
     """Whole-job step time (max over ranks) and throughput (all ranks' tokens / that time).
 
@@ -171,6 +207,7 @@ def main():
     ap.add_argument("--cpu-rows", type=int, default=64)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-modes", action="store_true", help="skip the forward-chunked and dense comparisons")
     ap.add_argument("--rows", type=int, default=None, help="override B*T (profiling a reduced case)")
     ap.add_argument("--vocab", type=int, default=None, help="override V (profiling a reduced case)")
     args = ap.parse_args()
@@ -299,6 +336,38 @@ def main():
                "d2h_bytes_per_step": 4, "ms_per_step": ems,
                "note": "pinned host H, teacher cache and mask copied in, loss copied out; W resident"}
 
+    # ---- the pages' other two formulations on the same inputs, for the memory/time trade-off
+    fc = None
+    if not args.no_modes:
+        zb = kd._abi.kd_chunked_kl_logits_bytes(N, V)
+        z_store = torch.empty((zb,), dtype=torch.uint8, device=dev)
+
+        def fc_step():
+            loss, lse, _, _ = kd.chunked_kl_forward(H, W, ids, tlog, mask, c, 1.0, ws=ws, z_store=z_store)
+            kd.chunked_kl_backward(H, W, ids, tlog, mask, lse, g, z_store, c, 1.0, ws=ws, grad_H=grad_H,
+                                   grad_W=grad_W)
+
+        for _ in range(2):
+            fc_step()
+        torch.cuda.synchronize(dev)
+        h0 = torch.cuda.Event(enable_timing=True)
+        h1 = torch.cuda.Event(enable_timing=True)
+        h0.record(stream)
+        for _ in range(args.steps):
+            fc_step()
+        h1.record(stream)
+        torch.cuda.synchronize(dev)
+        fms = h0.elapsed_time(h1) / args.steps
+        fc = {"ms_per_step": fms, "tokens_per_s": N / (fms * 1e-3),
+              "tflops_executed": w.flops_useful() / (fms * 1e-3) / 1e12,
+              "kept_logits_gb": zb / 1e9, "workspace_gb": ws.numel() / 1e9,
+              "note": "forward keeps bf16 logits [N, V]; backward reads them, no recompute (6*d*V flops/token)"}
+        del z_store
+        torch.cuda.empty_cache()
+    dense = None
+    if not args.no_modes and rank == 0:
+        dense = dense_torch_reference(H, W, ids, tlog, mask, dev)
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         from synth import bf16_bits
@@ -329,6 +398,8 @@ def main():
                          "unit": "TFLOP/s", "frac": achieved / peak, "traffic": ncu_traffic(dom_name, w.name),
                          "peak_source": f"{peaks['source']} bf16 sustained",
                          "flops_per_launch": gemm_flops_per_chunk},
+            "forward_chunked": fc,
+            "dense_torch_reference": dense,
             "kernels": kernels,
             "gpu_launches": launches,
             "clocks": clocks.summary(),

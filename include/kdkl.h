@@ -53,7 +53,8 @@ typedef enum {
   KD_ERR_WORKSPACE = 3,     /* ws is NULL, misaligned or smaller than required  */
   KD_ERR_CUDA = 4,          /* a CUDA runtime/driver call or launch failed      */
   KD_ERR_TIMEOUT = 5,       /* device: a bounded wait inside a kernel ran out   */
-  KD_ERR_DEVICE = 6         /* device: an input value out of range (teacher id) */
+  KD_ERR_DEVICE = 6,        /* device: an input value out of range (teacher id) */
+  KD_ERR_IO = 7             /* cache file: open/read/write failed, truncated or corrupt */
 } kd_status;
 
 #define KD_MAX_K 1024
@@ -82,13 +83,17 @@ KD_API size_t kd_topk_cache_workspace(int64_t N, int64_t V, int K);
  *                 read.  16-byte aligned; ld >= V and ld*2 a multiple of 16.
  *   K           : 1 <= K <= min(V, KD_MAX_K).
  *   ids_out     : [N, K] int32, written.   vals_out: [N, K] fp32, written.
+ *   lse_out     : [N] fp32 or NULL.  If given, also the full-row logsumexp of the
+ *                 logits, so that the probability mass the cache drops,
+ *                 1 - sum_k exp(vals_k - lse), can be reported ([ART] paragraph on
+ *                 the top-K limitation: the cache loses the teacher's tail).
  * Each output row is ordered by value, highest first; equal values are ordered
  * by ascending id and the cut at K keeps the lowest ids; -0.0 equals +0.0.
  * Values are the bf16 inputs widened exactly.  NaN inputs are ordered by their
  * sign bit like any other bit pattern (positive NaN above +inf).
  */
 KD_API int kd_topk_cache(const void* logits_bf16, int64_t N, int64_t V, int64_t ld, int K,
-                  int32_t* ids_out, float* vals_out,
+                  int32_t* ids_out, float* vals_out, float* lse_out,
                   void* ws, size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------------------------------ *
@@ -147,6 +152,36 @@ KD_API int kd_fused_kl_bwd(const void* H_bf16, const void* W_bf16,
                     void* grad_H, int grad_H_is_fp32, float* grad_W,
                     void* ws, size_t ws_bytes, void* stream);
 
+/* ------------------------------------------------------------------------ *
+ * Forward-chunked KL: the same loss, keeping each chunk's student logits.
+ * [ART] fused-loss paragraph, second formulation: the teacher stays sparse and
+ * the loss is taken one chunk at a time, but the full student logits are kept
+ * for the backward pass (so memory grows with sequence x vocabulary), which
+ * saves the backward recompute; the page calls it the fastest of the three.
+ * z_store holds the raw logits H W^T (bf16, before 1/tau) in a blocked layout:
+ * element (t, v) at ((v / 64) * N + t) * 64 + v % 64, i.e.
+ * kd_chunked_kl_logits_bytes(N, V) = ceil(V / 64) * N * 128 bytes, 16-byte
+ * aligned, owned by the caller; the forward writes it, the backward only reads
+ * it.  Everything else (arguments, workspace, outputs, errors) is as for
+ * kd_fused_kl_fwd / kd_fused_kl_bwd; the backward uses the bf16-rounded
+ * logits, so its gradients differ from the fused ones by that rounding.
+ * ------------------------------------------------------------------------ */
+
+KD_API size_t kd_chunked_kl_logits_bytes(int64_t N, int64_t V);
+
+KD_API int kd_chunked_kl_fwd(const void* H_bf16, const void* W_bf16,
+                    const int32_t* t_ids, const float* t_logits, const uint8_t* mask,
+                    int64_t N, int64_t d, int64_t V, int K, int64_t chunk, float tau,
+                    float* loss_out, float* lse_out, float* kl_per_token_out,
+                    void* z_store, size_t z_bytes, void* ws, size_t ws_bytes, void* stream);
+
+KD_API int kd_chunked_kl_bwd(const void* H_bf16, const void* W_bf16,
+                    const int32_t* t_ids, const float* t_logits, const uint8_t* mask,
+                    int64_t N, int64_t d, int64_t V, int K, int64_t chunk, float tau,
+                    const float* lse, const float* grad_loss, const void* z_store, size_t z_bytes,
+                    void* grad_H, int grad_H_is_fp32, float* grad_W,
+                    void* ws, size_t ws_bytes, void* stream);
+
 /*
  * Forward pass without a caller workspace, for callers that cannot allocate
  * device memory (no counterpart in the paper: it is an integration variant).
@@ -186,6 +221,36 @@ KD_API int kd_fused_kl_fwd_static(const void* H_bf16, const void* W_bf16,
  * (for KD_ERR_DEVICE: the first offending row).
  */
 KD_API int kd_get_device_error(void* ws, void* stream, int64_t* detail_out);
+
+/* ------------------------------------------------------------------------ *
+ * On-disk teacher cache ([ART] paragraph on the first fix: run the teacher once,
+ * keep its top-K logits per position on disk, reuse them across experiments).
+ * HOST memory and host files only; no CUDA call.  One file per contiguous range
+ * of positions (a shard): a 64-byte header (magic, version, K, V, N, row0,
+ * logits type, flags, FNV-1a 64 checksum of the payload), then ids int32 [N, K],
+ * logits fp32 or bf16 [N, K] and optionally the teacher's full-row logsumexp
+ * fp32 [N].  bf16 logits round to nearest even (exact for caches extracted from
+ * bf16 teacher logits) and are widened back to fp32 on reading.
+ * ------------------------------------------------------------------------ */
+
+/* Write a shard atomically (temporary file + rename).  lse may be NULL. */
+KD_API int kd_cache_write(const char* path, const int32_t* ids, const float* logits, const float* lse,
+                          int64_t N, int K, int64_t V, int64_t row0, int logits_bf16);
+/* Header fields of a shard (any out pointer may be NULL); checks the file size. */
+KD_API int kd_cache_info(const char* path, int64_t* N, int* K, int64_t* V, int64_t* row0,
+                         int* logits_bf16, int* has_lse);
+/* Recompute the payload checksum: KD_OK, or KD_ERR_IO if the file is corrupt or truncated. */
+KD_API int kd_cache_verify(const char* path);
+/* Read positions [first, first + count) into host buffers ids_out [count, K] and
+ * logits_out [count, K] (fp32); lse_out [count] or NULL. */
+KD_API int kd_cache_read(const char* path, int64_t first, int64_t count, int32_t* ids_out,
+                         float* logits_out, float* lse_out);
+/* Streaming reader: batches of up to rows_per_batch consecutive positions; the next
+ * batch is read on a background thread while the caller uses the current one.
+ * kd_cache_reader_next copies one batch into host buffers (rows_out = 0 at the end). */
+KD_API int kd_cache_reader_open(const char* path, int64_t rows_per_batch, void** handle);
+KD_API int kd_cache_reader_next(void* handle, int32_t* ids_out, float* logits_out, int64_t* rows_out);
+KD_API int kd_cache_reader_close(void* handle);
 
 /* ------------------------------------------------------------------------ *
  * Building blocks, exposed for testing and profiling.  No page describes these

@@ -26,7 +26,7 @@ from .kl import (
     fused_chunked_kl,
     OracleResult,
 )
-from .topk import topk_cache
+from .topk import topk_cache, teacher_logsumexp, dropped_mass
 
 __all__ = [
     "bf16_to_f64",
@@ -36,4 +36,6 @@ __all__ = [
     "fused_chunked_kl",
     "OracleResult",
     "topk_cache",
+    "teacher_logsumexp",
+    "dropped_mass",
 ]

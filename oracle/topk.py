@@ -37,3 +37,24 @@ def topk_cache(bits: np.ndarray, K: int):
         ids[r] = order
         vals[r] = v[order].astype(np.float32)
     return ids, vals
+
+
+def teacher_logsumexp(bits: np.ndarray) -> np.ndarray:
+    """log sum_v exp(t_v) of each row of dense bf16 teacher logits [N, V], in float64.
+
+    [ART] paragraph on the top-K limitation: keeping only the top K logits drops the
+    teacher's tail; with the full-row logsumexp the dropped probability is
+    1 - sum_k exp(t_k - logsumexp).  Rows of all -inf give -inf.
+    """
+    x = bf16_to_f64(np.asarray(bits))
+    m = np.max(x, axis=1)
+    m_safe = np.where(np.isfinite(m), m, 0.0)
+    with np.errstate(divide="ignore"):
+        return m_safe + np.log(np.sum(np.exp(x - m_safe[:, None]), axis=1))
+
+
+def dropped_mass(bits: np.ndarray, K: int) -> np.ndarray:
+    """Teacher probability (softmax over the full row) outside the row's top-K logits."""
+    lse = teacher_logsumexp(bits)
+    _, vals = topk_cache(bits, K)
+    return 1.0 - np.sum(np.exp(vals.astype(np.float64) - lse[:, None]), axis=1)

@@ -20,10 +20,17 @@ from ._abi import KDError, KD_MAX_K
 
 __all__ = [
     "topk_cache",
+    "dropped_mass",
     "fused_kl",
     "fused_kl_forward",
     "fused_kl_backward",
+    "chunked_kl_forward",
+    "chunked_kl_backward",
     "gemm_bf16",
+    "cache_write",
+    "cache_info",
+    "cache_read",
+    "CacheReader",
     "device_error",
     "Profile",
     "KDError",
@@ -55,8 +62,9 @@ def _require_cuda(*ts):
             raise ValueError("all tensors must be contiguous")
 
 
-def topk_cache(logits: torch.Tensor, K: int, ws: Optional[torch.Tensor] = None):
-    """Top-K teacher cache of a dense bf16 [N, V] logits tensor: (ids int32 [N, K], vals fp32 [N, K])."""
+def topk_cache(logits: torch.Tensor, K: int, ws: Optional[torch.Tensor] = None, with_lse: bool = False):
+    """Top-K teacher cache of a dense bf16 [N, V] logits tensor: (ids int32 [N, K], vals fp32 [N, K]),
+    plus the full-row logsumexp [N] when ``with_lse`` (see :func:`dropped_mass`)."""
     _require_cuda(logits)
     if logits.dtype != torch.bfloat16 or logits.dim() != 2:
         raise ValueError("logits must be a 2-D bf16 tensor")
@@ -66,10 +74,19 @@ def topk_cache(logits: torch.Tensor, K: int, ws: Optional[torch.Tensor] = None):
     need = _abi.kd_topk_cache_workspace(N, V, K)
     if ws is None:
         ws = workspace(need, logits.device)
-    st = _abi.kd_topk_cache(_ptr(logits), N, V, logits.stride(0), K, _ptr(ids), _ptr(vals), _ptr(ws),
+    lse = torch.empty((N,), dtype=torch.float32, device=logits.device) if with_lse else None
+    st = _abi.kd_topk_cache(_ptr(logits), N, V, logits.stride(0), K, _ptr(ids), _ptr(vals), _ptr(lse), _ptr(ws),
                             ws.numel(), _stream(logits.device))
     _abi.check(st, "kd_topk_cache")
-    return ids, vals
+    return (ids, vals, lse) if with_lse else (ids, vals)
+
+
+def dropped_mass(vals: torch.Tensor, lse: torch.Tensor, tau: float = 1.0) -> torch.Tensor:
+    """Teacher probability outside the cached top-K per position, 1 - sum_k softmax(t)_k over the full
+    vocabulary (at tau = 1: 1 - sum_k exp(vals_k - lse)).  A diagnostic on the host side of the cache."""
+    if tau != 1.0:
+        raise ValueError("the cached logsumexp is taken at temperature 1")
+    return 1.0 - torch.exp(vals - lse[:, None]).sum(dim=1)
 
 
 def fused_kl_forward(H, W, ids, tlog, mask=None, chunk=4096, tau=1.0, ws=None, kl_out=None):
@@ -105,6 +122,47 @@ def fused_kl_backward(H, W, ids, tlog, mask, lse, grad_loss, chunk=4096, tau=1.0
                               _ptr(lse), _ptr(grad_loss), _ptr(grad_H), 1 if grad_H.dtype == torch.float32 else 0,
                               _ptr(grad_W), _ptr(ws), ws.numel(), _stream(H.device))
     _abi.check(st, "kd_fused_kl_bwd")
+    return grad_H, grad_W
+
+
+def chunked_kl_forward(H, W, ids, tlog, mask=None, chunk=4096, tau=1.0, ws=None, kl_out=None, z_store=None):
+    """kd_chunked_kl_fwd (forward-chunked mode): returns (loss, lse, ws, z_store); z_store keeps the logits."""
+    _require_cuda(H, W, ids, tlog, mask)
+    N, d = H.shape
+    V = W.shape[0]
+    K = ids.shape[1]
+    if ws is None:
+        ws = workspace(_abi.kd_fused_kl_workspace(N, d, V, K, chunk), H.device)
+    zb = _abi.kd_chunked_kl_logits_bytes(N, V)
+    if z_store is None:
+        z_store = torch.empty((zb,), dtype=torch.uint8, device=H.device)
+    loss = torch.empty((1,), dtype=torch.float32, device=H.device)
+    lse = torch.empty((N,), dtype=torch.float32, device=H.device)
+    st = _abi.kd_chunked_kl_fwd(_ptr(H), _ptr(W), _ptr(ids), _ptr(tlog), _ptr(mask), N, d, V, K, chunk, float(tau),
+                                _ptr(loss), _ptr(lse), _ptr(kl_out), _ptr(z_store), z_store.numel(), _ptr(ws),
+                                ws.numel(), _stream(H.device))
+    _abi.check(st, "kd_chunked_kl_fwd")
+    return loss, lse, ws, z_store
+
+
+def chunked_kl_backward(H, W, ids, tlog, mask, lse, grad_loss, z_store, chunk=4096, tau=1.0, ws=None, grad_H=None,
+                        grad_W=None, grad_H_fp32=False):
+    """kd_chunked_kl_bwd: gradients from the logits kept by chunked_kl_forward (no recompute)."""
+    _require_cuda(H, W, ids, tlog, mask, lse, grad_loss, z_store)
+    N, d = H.shape
+    V = W.shape[0]
+    K = ids.shape[1]
+    if ws is None:
+        ws = workspace(_abi.kd_fused_kl_workspace(N, d, V, K, chunk), H.device)
+    if grad_H is None:
+        grad_H = torch.empty((N, d), dtype=torch.float32 if grad_H_fp32 else torch.bfloat16, device=H.device)
+    if grad_W is None:
+        grad_W = torch.zeros((V, d), dtype=torch.float32, device=H.device)
+    st = _abi.kd_chunked_kl_bwd(_ptr(H), _ptr(W), _ptr(ids), _ptr(tlog), _ptr(mask), N, d, V, K, chunk, float(tau),
+                                _ptr(lse), _ptr(grad_loss), _ptr(z_store), z_store.numel(), _ptr(grad_H),
+                                1 if grad_H.dtype == torch.float32 else 0, _ptr(grad_W), _ptr(ws), ws.numel(),
+                                _stream(H.device))
+    _abi.check(st, "kd_chunked_kl_bwd")
     return grad_H, grad_W
 
 
@@ -150,6 +208,92 @@ def device_error(ws: torch.Tensor):
     detail = ctypes.c_int64(0)
     st = _abi.kd_get_device_error(_ptr(ws), _stream(ws.device), ctypes.byref(detail))
     return st, detail.value
+
+
+# ---------------------------------------------------------------- disk cache
+
+def _host_c(t, dtype):
+    t = torch.as_tensor(t)
+    if t.is_cuda:
+        t = t.cpu()
+    return t.to(dtype).contiguous()
+
+
+def cache_write(path: str, ids, vals, V: int, lse=None, row0: int = 0, bf16: bool = False):
+    """Write a top-K cache shard (host copies of ids [N, K] int32, vals [N, K] fp32, lse [N] or None)."""
+    ids = _host_c(ids, torch.int32)
+    vals = _host_c(vals, torch.float32)
+    N, K = ids.shape
+    lse_t = None if lse is None else _host_c(lse, torch.float32)
+    st = _abi.kd_cache_write(str(path).encode(), ids.data_ptr(), vals.data_ptr(), _ptr(lse_t), N, K, int(V),
+                             int(row0), int(bool(bf16)))
+    _abi.check(st, "kd_cache_write")
+
+
+def cache_info(path: str) -> dict:
+    N, K, V, row0, bf, hl = (ctypes.c_int64(), ctypes.c_int(), ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int(),
+                             ctypes.c_int())
+    st = _abi.kd_cache_info(str(path).encode(), ctypes.byref(N), ctypes.byref(K), ctypes.byref(V), ctypes.byref(row0),
+                            ctypes.byref(bf), ctypes.byref(hl))
+    _abi.check(st, "kd_cache_info")
+    return dict(N=N.value, K=K.value, V=V.value, row0=row0.value, bf16=bool(bf.value), has_lse=bool(hl.value))
+
+
+def cache_read(path: str, first: int = 0, count: Optional[int] = None, with_lse: bool = False, pin: bool = False):
+    """Read positions [first, first + count) of a shard into (pinned, if asked) host tensors."""
+    info = cache_info(path)
+    if count is None:
+        count = info["N"] - first
+    K = info["K"]
+    ids = torch.empty((count, K), dtype=torch.int32, pin_memory=pin)
+    vals = torch.empty((count, K), dtype=torch.float32, pin_memory=pin)
+    lse = torch.empty((count,), dtype=torch.float32, pin_memory=pin) if with_lse else None
+    st = _abi.kd_cache_read(str(path).encode(), int(first), int(count), ids.data_ptr(), vals.data_ptr(), _ptr(lse))
+    _abi.check(st, "kd_cache_read")
+    return (ids, vals, lse) if with_lse else (ids, vals)
+
+
+class CacheReader:
+    """Iterate a shard in batches of consecutive positions; the next batch is read from disk on a
+    background thread (native) while the current one is in use.  Yields (ids, vals) host tensors."""
+
+    def __init__(self, path: str, rows_per_batch: int, pin: bool = False):
+        self.info = cache_info(path)
+        self.rows = int(rows_per_batch)
+        self.pin = pin
+        self._h = ctypes.c_void_p()
+        _abi.check(_abi.kd_cache_reader_open(str(path).encode(), self.rows, ctypes.byref(self._h)),
+                   "kd_cache_reader_open")
+
+    def __iter__(self):
+        K = self.info["K"]
+        while True:
+            ids = torch.empty((self.rows, K), dtype=torch.int32, pin_memory=self.pin)
+            vals = torch.empty((self.rows, K), dtype=torch.float32, pin_memory=self.pin)
+            n = ctypes.c_int64(0)
+            _abi.check(_abi.kd_cache_reader_next(self._h, ids.data_ptr(), vals.data_ptr(), ctypes.byref(n)),
+                       "kd_cache_reader_next")
+            if n.value == 0:
+                return
+            yield ids[:n.value], vals[:n.value]
+
+    def close(self):
+        if self._h:
+            _abi.kd_cache_reader_close(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+        return False
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 class Profile:

@@ -21,6 +21,7 @@ KD_ERR_WORKSPACE = 3
 KD_ERR_CUDA = 4
 KD_ERR_TIMEOUT = 5
 KD_ERR_DEVICE = 6
+KD_ERR_IO = 7
 KD_MAX_K = 1024
 KD_STATIC_SCRATCH_BYTES = 32 * 1024 * 1024
 
@@ -34,12 +35,19 @@ _SIGNATURES = {
     "kd_status_string": (ctypes.c_char_p, [_c_int]),
     "kd_version": (_c_int, []),
     "kd_topk_cache_workspace": (_c_size, [_c_i64, _c_i64, _c_int]),
-    "kd_topk_cache": (_c_int, [_c_ptr, _c_i64, _c_i64, _c_i64, _c_int, _c_ptr, _c_ptr, _c_ptr, _c_size, _c_ptr]),
+    "kd_topk_cache": (_c_int, [_c_ptr, _c_i64, _c_i64, _c_i64, _c_int, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_size,
+                               _c_ptr]),
     "kd_fused_kl_workspace": (_c_size, [_c_i64, _c_i64, _c_i64, _c_int, _c_i64]),
     "kd_fused_kl_fwd": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_i64, _c_i64, _c_i64, _c_int, _c_i64,
                                  _c_float, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_size, _c_ptr]),
     "kd_fused_kl_bwd": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_i64, _c_i64, _c_i64, _c_int, _c_i64,
                                  _c_float, _c_ptr, _c_ptr, _c_ptr, _c_int, _c_ptr, _c_ptr, _c_size, _c_ptr]),
+    "kd_chunked_kl_logits_bytes": (_c_size, [_c_i64, _c_i64]),
+    "kd_chunked_kl_fwd": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_i64, _c_i64, _c_i64, _c_int, _c_i64,
+                                   _c_float, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_size, _c_ptr, _c_size, _c_ptr]),
+    "kd_chunked_kl_bwd": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_i64, _c_i64, _c_i64, _c_int, _c_i64,
+                                   _c_float, _c_ptr, _c_ptr, _c_ptr, _c_size, _c_ptr, _c_int, _c_ptr, _c_ptr, _c_size,
+                                   _c_ptr]),
     "kd_fused_kl_fwd_static": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_i64, _c_i64, _c_i64, _c_int,
                                         _c_i64, _c_float, _c_ptr, _c_ptr, _c_ptr, _c_ptr]),
     "kd_get_device_error": (_c_int, [_c_ptr, _c_ptr, ctypes.POINTER(_c_i64)]),
@@ -47,6 +55,15 @@ _SIGNATURES = {
                               _c_ptr]),
     "kd_gemm_workspace": (_c_size, []),
     "kd_check_wait_timeout": (_c_int, [_c_ptr, _c_size, _c_i64, _c_ptr]),
+    "kd_cache_write": (_c_int, [ctypes.c_char_p, _c_ptr, _c_ptr, _c_ptr, _c_i64, _c_int, _c_i64, _c_i64, _c_int]),
+    "kd_cache_info": (_c_int, [ctypes.c_char_p, ctypes.POINTER(_c_i64), ctypes.POINTER(_c_int),
+                               ctypes.POINTER(_c_i64), ctypes.POINTER(_c_i64), ctypes.POINTER(_c_int),
+                               ctypes.POINTER(_c_int)]),
+    "kd_cache_verify": (_c_int, [ctypes.c_char_p]),
+    "kd_cache_read": (_c_int, [ctypes.c_char_p, _c_i64, _c_i64, _c_ptr, _c_ptr, _c_ptr]),
+    "kd_cache_reader_open": (_c_int, [ctypes.c_char_p, _c_i64, ctypes.POINTER(_c_ptr)]),
+    "kd_cache_reader_next": (_c_int, [_c_ptr, _c_ptr, _c_ptr, ctypes.POINTER(_c_i64)]),
+    "kd_cache_reader_close": (_c_int, [_c_ptr]),
     "kd_profile_begin": (_c_int, [_c_int]),
     "kd_profile_end": (_c_int, []),
     "kd_profile_read": (_c_int, [ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(_c_float), _c_int]),
@@ -108,10 +125,20 @@ kd_fused_kl_workspace = _wrap("kd_fused_kl_workspace")
 kd_fused_kl_fwd = _wrap("kd_fused_kl_fwd")
 kd_fused_kl_bwd = _wrap("kd_fused_kl_bwd")
 kd_fused_kl_fwd_static = _wrap("kd_fused_kl_fwd_static")
+kd_chunked_kl_logits_bytes = _wrap("kd_chunked_kl_logits_bytes")
+kd_chunked_kl_fwd = _wrap("kd_chunked_kl_fwd")
+kd_chunked_kl_bwd = _wrap("kd_chunked_kl_bwd")
 kd_get_device_error = _wrap("kd_get_device_error")
 kd_gemm_bf16 = _wrap("kd_gemm_bf16")
 kd_gemm_workspace = _wrap("kd_gemm_workspace")
 kd_check_wait_timeout = _wrap("kd_check_wait_timeout")
+kd_cache_write = _wrap("kd_cache_write")
+kd_cache_info = _wrap("kd_cache_info")
+kd_cache_verify = _wrap("kd_cache_verify")
+kd_cache_read = _wrap("kd_cache_read")
+kd_cache_reader_open = _wrap("kd_cache_reader_open")
+kd_cache_reader_next = _wrap("kd_cache_reader_next")
+kd_cache_reader_close = _wrap("kd_cache_reader_close")
 kd_profile_begin = _wrap("kd_profile_begin")
 kd_profile_end = _wrap("kd_profile_end")
 kd_profile_read = _wrap("kd_profile_read")

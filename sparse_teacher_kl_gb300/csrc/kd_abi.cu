@@ -193,6 +193,7 @@ const char* kd_status_string(int status) {
     case KD_ERR_CUDA: return "KD_ERR_CUDA";
     case KD_ERR_TIMEOUT: return "KD_ERR_TIMEOUT";
     case KD_ERR_DEVICE: return "KD_ERR_DEVICE";
+    case KD_ERR_IO: return "KD_ERR_IO";
     default: return "KD_ERR_UNKNOWN";
   }
 }
@@ -205,17 +206,18 @@ size_t kd_topk_cache_workspace(int64_t N, int64_t V, int K) {
 }
 
 int kd_topk_cache(const void* logits_bf16, int64_t N, int64_t V, int64_t ld, int K, int32_t* ids_out,
-                  float* vals_out, void* ws, size_t ws_bytes, void* stream) {
+                  float* vals_out, float* lse_out, void* ws, size_t ws_bytes, void* stream) {
   if (N < 1 || V < 1 || K < 1 || K > KD_MAX_K || int64_t(K) > V || ld < V) return KD_ERR_INVALID_ARG;
   if (V > 0x7fffffffLL || ld % 8 != 0) return KD_ERR_INVALID_ARG;
   if (!logits_bf16 || !ids_out || !vals_out) return KD_ERR_INVALID_ARG;
   if (!aligned(logits_bf16, 16) || !aligned(ids_out, 4) || !aligned(vals_out, 4)) return KD_ERR_INVALID_ARG;
+  if (lse_out && !aligned(lse_out, 4)) return KD_ERR_INVALID_ARG;
   if (!ws || !aligned(ws, 256) || ws_bytes < kd_topk_cache_workspace(N, V, K)) return KD_ERR_WORKSPACE;
   kd_status st = check_device();
   if (st != KD_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   Ctrl* ctrl = static_cast<Ctrl*>(ws);
-  return map_cuda(launch_topk(static_cast<const uint16_t*>(logits_bf16), N, V, ld, K, ids_out, vals_out,
+  return map_cuda(launch_topk(static_cast<const uint16_t*>(logits_bf16), N, V, ld, K, ids_out, vals_out, lse_out,
                               &ctrl->err, s));
 }
 
@@ -224,10 +226,20 @@ size_t kd_fused_kl_workspace(int64_t N, int64_t d, int64_t V, int K, int64_t chu
   return kl_layout(N, d, V, K, chunk).total;
 }
 
-int kd_fused_kl_fwd(const void* H_bf16, const void* W_bf16, const int32_t* t_ids, const float* t_logits,
+size_t kd_chunked_kl_logits_bytes(int64_t N, int64_t V) {
+  if (N < 1 || V < 1) return 0;
+  return size_t((V + 63) / 64) * size_t(N) * 128;
+}
+
+}  // extern "C"
+
+// Forward pass of both modes: z_store == NULL is the fused chunked loss; otherwise
+// each chunk's raw logits are also written (bf16, blocked) for a backward pass that
+// reads them instead of recomputing them.
+static int fwd_impl(const void* H_bf16, const void* W_bf16, const int32_t* t_ids, const float* t_logits,
                     const uint8_t* mask, int64_t N, int64_t d, int64_t V, int K, int64_t chunk, float tau,
-                    float* loss_out, float* lse_out, float* kl_per_token_out, void* ws, size_t ws_bytes,
-                    void* stream) {
+                    float* loss_out, float* lse_out, float* kl_per_token_out, void* z_store, size_t z_bytes,
+                    void* ws, size_t ws_bytes, void* stream) {
   kd_status st = check_kl_args(H_bf16, W_bf16, t_ids, t_logits, N, d, V, K, chunk, tau, ws, ws_bytes);
   if (st != KD_OK) return st;
   if (!loss_out || !lse_out || !aligned(loss_out, 4) || !aligned(lse_out, 4)) return KD_ERR_INVALID_ARG;
@@ -247,8 +259,13 @@ int kd_fused_kl_fwd(const void* H_bf16, const void* W_bf16, const int32_t* t_ids
   const float inv_tau = 1.0f / tau;
   const uint16_t* H = static_cast<const uint16_t*>(H_bf16);
 
-  alignas(64) CUtensorMap tw, th;
+  alignas(64) CUtensorMap tw, th, tz;
   if (!make_tmap_2d_bf16(&tw, W_bf16, uint64_t(d), uint64_t(V), uint64_t(d) * 2, BK, BN)) return KD_ERR_CUDA;
+  if (z_store) {
+    (void)z_bytes;
+    if (!make_tmap_dz_blocked(&tz, z_store, uint64_t(N), uint64_t(N), uint64_t((V + 63) / 64), 32))
+      return KD_ERR_CUDA;
+  }
 
   cudaError_t e = launch_count_valid(mask, N, &ctrl->n_valid, s);
   if (e != cudaSuccess) return KD_ERR_CUDA;
@@ -261,7 +278,8 @@ int kd_fused_kl_fwd(const void* H_bf16, const void* W_bf16, const int32_t* t_ids
     if (!make_tmap_2d_bf16(&th, H + c0 * d, uint64_t(d), uint64_t(n), uint64_t(d) * 2, BK, BM)) return KD_ERR_CUDA;
     GemmProblem p{};
     p.M = n; p.N = int(V); p.K = int(d);
-    p.a_mn = 0; p.b_mn = 0; p.epi = EPI_LSE;
+    p.a_mn = 0; p.b_mn = 0; p.epi = z_store ? EPI_LSE_Z : EPI_LSE;
+    p.z_row0 = int(c0);
     p.m_tiles = (n + BM - 1) / BM;
     p.n_tiles = int((V + BN - 1) / BN);
     p.n_group = choose_n_group(V);
@@ -269,7 +287,7 @@ int kd_fused_kl_fwd(const void* H_bf16, const void* W_bf16, const int32_t* t_ids
     p.k_splits = 1;
     p.ids_sorted = ids_sorted; p.p_sorted = p_sorted; p.Kt = K; p.inv_tau = inv_tau;
     p.partials = partials; p.rows = n; p.err = &ctrl->err;
-    e = launch_gemm(p, th, tw, tw, grid_max, s);
+    e = launch_gemm(p, th, tw, z_store ? tz : tw, grid_max, s);
     if (e != cudaSuccess) return KD_ERR_CUDA;
     e = launch_lse_combine(partials, L.n_groups, n, negent, inv_tau, lse_out + c0, kl + c0, s);
     if (e != cudaSuccess) return KD_ERR_CUDA;
@@ -278,10 +296,12 @@ int kd_fused_kl_fwd(const void* H_bf16, const void* W_bf16, const int32_t* t_ids
   return map_cuda(e);
 }
 
-int kd_fused_kl_bwd(const void* H_bf16, const void* W_bf16, const int32_t* t_ids, const float* t_logits,
+// Backward pass of both modes: z_store == NULL recomputes each chunk's logits on
+// the tensor cores (fused); otherwise dZ is formed from the stored logits.
+static int bwd_impl(const void* H_bf16, const void* W_bf16, const int32_t* t_ids, const float* t_logits,
                     const uint8_t* mask, int64_t N, int64_t d, int64_t V, int K, int64_t chunk, float tau,
-                    const float* lse, const float* grad_loss, void* grad_H, int grad_H_is_fp32, float* grad_W,
-                    void* ws, size_t ws_bytes, void* stream) {
+                    const float* lse, const float* grad_loss, const void* z_store, void* grad_H, int grad_H_is_fp32,
+                    float* grad_W, void* ws, size_t ws_bytes, void* stream) {
   kd_status st = check_kl_args(H_bf16, W_bf16, t_ids, t_logits, N, d, V, K, chunk, tau, ws, ws_bytes);
   if (st != KD_OK) return st;
   if (!lse || !grad_loss || !grad_H || !grad_W) return KD_ERR_INVALID_ARG;
@@ -323,6 +343,13 @@ int kd_fused_kl_bwd(const void* H_bf16, const void* W_bf16, const int32_t* t_ids
     if (!make_tmap_dz_blocked(&tdz_mn, dz, uint64_t(n), uint64_t(L.rows_pad), uint64_t(L.nvb), BK)) return KD_ERR_CUDA;
     if (!make_tmap_dz_blocked(&tdz_st, dz, uint64_t(n), uint64_t(L.rows_pad), uint64_t(L.nvb), 32)) return KD_ERR_CUDA;
 
+    if (z_store) {
+      // forward-chunked: dZ from the logits the forward pass kept
+      e = launch_dz_from_z(static_cast<const uint16_t*>(z_store), N, c0, n, V, L.nvb, L.rows_pad, lse + c0,
+                           mask ? mask + c0 : nullptr, grad_loss, &ctrl->n_valid, inv_tau, ids_sorted, p_sorted, K,
+                           dz, s);
+      if (e != cudaSuccess) return KD_ERR_CUDA;
+    } else {
     // B1: recompute the chunk's logits, dZ -> bf16 workspace
     GemmProblem p{};
     p.M = n; p.N = int(V); p.K = int(d);
@@ -337,6 +364,7 @@ int kd_fused_kl_bwd(const void* H_bf16, const void* W_bf16, const int32_t* t_ids
     p.dz = dz; p.ldz = L.ldz; p.rows = n; p.err = &ctrl->err;
     e = launch_gemm(p, th_k, tw_k, tdz_st, grid_max, s);
     if (e != cudaSuccess) return KD_ERR_CUDA;
+    }
 
     // B2: grad_H rows of the chunk = dZ W  (A = dZ K-major over V, B = W with d contiguous)
     GemmProblem q{};
@@ -381,6 +409,44 @@ int kd_fused_kl_bwd(const void* H_bf16, const void* W_bf16, const int32_t* t_ids
     if (e != cudaSuccess) return KD_ERR_CUDA;
   }
   return KD_OK;
+}
+
+extern "C" {
+
+int kd_fused_kl_fwd(const void* H_bf16, const void* W_bf16, const int32_t* t_ids, const float* t_logits,
+                    const uint8_t* mask, int64_t N, int64_t d, int64_t V, int K, int64_t chunk, float tau,
+                    float* loss_out, float* lse_out, float* kl_per_token_out, void* ws, size_t ws_bytes,
+                    void* stream) {
+  return fwd_impl(H_bf16, W_bf16, t_ids, t_logits, mask, N, d, V, K, chunk, tau, loss_out, lse_out,
+                  kl_per_token_out, nullptr, 0, ws, ws_bytes, stream);
+}
+
+int kd_fused_kl_bwd(const void* H_bf16, const void* W_bf16, const int32_t* t_ids, const float* t_logits,
+                    const uint8_t* mask, int64_t N, int64_t d, int64_t V, int K, int64_t chunk, float tau,
+                    const float* lse, const float* grad_loss, void* grad_H, int grad_H_is_fp32, float* grad_W,
+                    void* ws, size_t ws_bytes, void* stream) {
+  return bwd_impl(H_bf16, W_bf16, t_ids, t_logits, mask, N, d, V, K, chunk, tau, lse, grad_loss, nullptr, grad_H,
+                  grad_H_is_fp32, grad_W, ws, ws_bytes, stream);
+}
+
+int kd_chunked_kl_fwd(const void* H_bf16, const void* W_bf16, const int32_t* t_ids, const float* t_logits,
+                      const uint8_t* mask, int64_t N, int64_t d, int64_t V, int K, int64_t chunk, float tau,
+                      float* loss_out, float* lse_out, float* kl_per_token_out, void* z_store, size_t z_bytes,
+                      void* ws, size_t ws_bytes, void* stream) {
+  if (!z_store || !aligned(z_store, 16) || N < 1 || V < 1) return KD_ERR_INVALID_ARG;
+  if (z_bytes < kd_chunked_kl_logits_bytes(N, V)) return KD_ERR_INVALID_ARG;
+  return fwd_impl(H_bf16, W_bf16, t_ids, t_logits, mask, N, d, V, K, chunk, tau, loss_out, lse_out,
+                  kl_per_token_out, z_store, z_bytes, ws, ws_bytes, stream);
+}
+
+int kd_chunked_kl_bwd(const void* H_bf16, const void* W_bf16, const int32_t* t_ids, const float* t_logits,
+                      const uint8_t* mask, int64_t N, int64_t d, int64_t V, int K, int64_t chunk, float tau,
+                      const float* lse, const float* grad_loss, const void* z_store, size_t z_bytes, void* grad_H,
+                      int grad_H_is_fp32, float* grad_W, void* ws, size_t ws_bytes, void* stream) {
+  if (!z_store || !aligned(z_store, 16) || N < 1 || V < 1) return KD_ERR_INVALID_ARG;
+  if (z_bytes < kd_chunked_kl_logits_bytes(N, V)) return KD_ERR_INVALID_ARG;
+  return bwd_impl(H_bf16, W_bf16, t_ids, t_logits, mask, N, d, V, K, chunk, tau, lse, grad_loss, z_store, grad_H,
+                  grad_H_is_fp32, grad_W, ws, ws_bytes, stream);
 }
 
 int kd_get_device_error(void* ws, void* stream, int64_t* detail_out) {

@@ -15,6 +15,8 @@
 //             one (max, sum, gather) partial per row and unit.
 //   EPI_DZ    the backward recompute: dZ = scale * (2^(z log2e/tau - lse log2e)
 //             - p on the cached ids), rounded to bf16 into a [rows, ldz] buffer.
+//   EPI_LSE_Z as EPI_LSE, and also writes the raw logits (bf16) out for a
+//             backward pass that does not recompute them (forward-chunked mode).
 //   EPI_STORE / EPI_ACCUM  plain C = acc / C += acc for the gradient products.
 #include <math.h>
 #include <stdio.h>
@@ -44,7 +46,7 @@ static_assert(GEMM_SMEM_BYTES <= 232448, "shared memory budget of one CTA");
 __device__ __forceinline__ void unit_coords(const GemmProblem& p, int u, int& m_blk, int& n_first, int& n_count,
                                             int& kb_lo, int& kb_hi, int& split) {
   const int k_blocks = (p.K + BK - 1) / BK;
-  if (p.epi == EPI_LSE || p.epi == EPI_DZ) {
+  if (p.epi == EPI_LSE || p.epi == EPI_DZ || p.epi == EPI_LSE_Z) {
     const int g = u / p.m_tiles;
     m_blk = u - g * p.m_tiles;
     n_first = g * p.n_group;
@@ -96,7 +98,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_map(&tmap_a);
     tma_prefetch_map(&tmap_b);
-    if (EPI == EPI_ACCUM || EPI == EPI_DZ) tma_prefetch_map(&tmap_c);
+    if (EPI == EPI_DZ || EPI == EPI_LSE_Z) tma_prefetch_map(&tmap_c);
   }
   if (warp == 1) {
     tmem_alloc(&tail->tmem_base, TMEM_COLS);
@@ -232,7 +234,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       const int32_t* ids_row = nullptr;
       const float* p_row = nullptr;
       float lse2 = 0.f, rowscale = 0.f;
-      if (EPI == EPI_LSE || EPI == EPI_DZ) {
+      if (EPI == EPI_LSE || EPI == EPI_DZ || EPI == EPI_LSE_Z) {
         const bool row_ok = row < p.rows;
         cur = p.Kt;
         if (row_ok) {
@@ -280,7 +282,34 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(raw[i]);
           const int col0 = nb * BN + c * 32;
 
-          if (EPI == EPI_LSE) {
+          if (EPI == EPI_LSE_Z) {
+            // forward-chunked: keep this tile's raw logits (bf16) for the backward pass
+            uint8_t* box = my_staging + sbuf * 4096u;
+            if ((c & 1) == 0) {
+              if (lane == 0) bulk_wait_read<1>();
+              __syncwarp();
+            }
+#pragma unroll
+            for (int g8 = 0; g8 < 4; ++g8) {
+              uint4 v;
+              v.x = pack_bf16x2(x[g8 * 8 + 0], x[g8 * 8 + 1]);
+              v.y = pack_bf16x2(x[g8 * 8 + 2], x[g8 * 8 + 3]);
+              v.z = pack_bf16x2(x[g8 * 8 + 4], x[g8 * 8 + 5]);
+              v.w = pack_bf16x2(x[g8 * 8 + 6], x[g8 * 8 + 7]);
+              const uint32_t j = uint32_t((c & 1) * 4 + g8);
+              *reinterpret_cast<uint4*>(box + lane * 128u + ((j ^ (lane & 7u)) * 16u)) = v;
+            }
+            if (c & 1) {
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                tma_store_3d(&tmap_c, box, 0, p.z_row0 + m_blk * BM + int(quarter) * 32, (col0 - 32) / 64);
+                bulk_commit();
+              }
+              sbuf ^= 1u;
+            }
+          }
+          if (EPI == EPI_LSE || EPI == EPI_LSE_Z) {
             if (row < p.rows) {
               // columns past the vocabulary do not exist
               if (col0 + 32 > p.N) {
@@ -369,24 +398,17 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
               sbuf ^= 1u;
             }
           } else if (EPI == EPI_ACCUM) {
-            // C[rows of this warp, col0 .. col0+31] += acc: stage the 32 x 32 fp32 box in shared
-            // memory (128-byte swizzle, conflict-free) and add it into C with one TMA reduction;
-            // the read-modify-write happens in L2, off the epilogue's critical path.
-            uint8_t* box = my_staging + sbuf * 4096u;
-            if (lane == 0) bulk_wait_read<1>();  // the group that last used this box has read it
-            __syncwarp();
+            // C[row, col0 .. col0+31] += acc with fire-and-forget vector reductions: the
+            // read-modify-write happens in L2, nothing waits on it, and the TMA unit stays
+            // free for the operand loads.  Each element gets exactly one addition per launch.
+            if (row < p.M) {
+              float* dst = reinterpret_cast<float*>(p.C) + size_t(row) * p.ldc + col0;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const uint32_t off = lane * 128u + ((uint32_t(j) ^ (lane & 7u)) * 16u);
-              *reinterpret_cast<float4*>(box + off) = make_float4(x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]);
+              for (int g4 = 0; g4 < 8; ++g4) {
+                if (col0 + g4 * 4 + 4 <= p.N)
+                  red_add_v4(dst + g4 * 4, x[g4 * 4 + 0], x[g4 * 4 + 1], x[g4 * 4 + 2], x[g4 * 4 + 3]);
+              }
             }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-              tma_reduce_add_2d(&tmap_c, box, col0, m_blk * BM + int(quarter) * 32);
-              bulk_commit();
-            }
-            sbuf ^= 1u;
           } else {
             // EPI_STORE: C[row, col0 + i]
             if (row < p.M) {
@@ -421,13 +443,13 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         tc_fence_before();
         mbar_arrive(&tail->tempty[a]);
       }
-      if (EPI == EPI_LSE && ok && row < p.rows) {
+      if ((EPI == EPI_LSE || EPI == EPI_LSE_Z) && ok && row < p.rows) {
         const int g = n_first / p.n_group;
         p.partials[size_t(g) * (p.m_tiles * BM) + row] =
             make_float4(run_m * scale2, run_s, run_g * p.inv_tau, 0.f);
       }
     }
-    if ((EPI == EPI_ACCUM || EPI == EPI_DZ) && lane == 0) bulk_wait_all();  // output boxes done before exit
+    if ((EPI == EPI_DZ || EPI == EPI_LSE_Z) && lane == 0) bulk_wait_all();  // output boxes done before exit
   }
 
   tc_fence_before();
@@ -467,6 +489,7 @@ static cudaError_t launch_one(const GemmProblem& p, const CUtensorMap& ta, const
 static const char* gemm_name(int epi, int a_mn, int b_mn) {
   switch (epi) {
     case EPI_LSE: return "kd_proj_lse_fwd";
+    case EPI_LSE_Z: return "kd_proj_lse_z_fwd";
     case EPI_DZ: return "kd_proj_dz_bwd";
     case EPI_STORE: return (a_mn == 0 && b_mn == 1) ? "kd_gemm_dz_w" : "kd_gemm_store";
     default: return (a_mn == 1 && b_mn == 1) ? "kd_gemm_dzT_h" : "kd_gemm_accum";
@@ -481,6 +504,7 @@ cudaError_t launch_gemm(const GemmProblem& p, const CUtensorMap& ta, const CUten
   cudaError_t e;
   switch (p.epi) {
     case EPI_LSE: e = launch_one<EPI_LSE>(p, ta, tb, tc, grid, s); break;
+    case EPI_LSE_Z: e = launch_one<EPI_LSE_Z>(p, ta, tb, tc, grid, s); break;
     case EPI_DZ: e = launch_one<EPI_DZ>(p, ta, tb, tc, grid, s); break;
     case EPI_STORE: e = launch_one<EPI_STORE>(p, ta, tb, tc, grid, s); break;
     default: e = launch_one<EPI_ACCUM>(p, ta, tb, tc, grid, s); break;

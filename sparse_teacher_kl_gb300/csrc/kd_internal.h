@@ -49,6 +49,7 @@ enum EpiKind : int {
   EPI_DZ = 1,     // backward: dZ = scale * (softmax - p) -> bf16 [rows, ldz]
   EPI_STORE = 2,  // C = acc -> fp32 or bf16
   EPI_ACCUM = 3,  // C += acc (fp32)
+  EPI_LSE_Z = 4,  // forward-chunked: EPI_LSE plus the raw logits z -> bf16, blocked [V/64][N][64]
 };
 
 struct GemmProblem {
@@ -66,6 +67,7 @@ struct GemmProblem {
   // dZ[vocab / 64][row][vocab % 64] (see make_tmap_dz_blocked), so that every TMA box
   // of it is one contiguous run of memory.
   int a_blocked;
+  int z_row0;                 // EPI_LSE_Z: row of the stored logits that chunk row 0 maps to
   // EPI_STORE / EPI_ACCUM
   void* C;
   int64_t ldc;
@@ -105,7 +107,7 @@ cudaError_t launch_gemm(const GemmProblem& p, const CUtensorMap& ta, const CUten
 int gemm_max_grid();
 
 cudaError_t launch_topk(const uint16_t* X, int64_t N, int64_t V, int64_t ld, int K, int32_t* ids,
-                        float* vals, uint32_t* err, cudaStream_t s);
+                        float* vals, float* lse, uint32_t* err, cudaStream_t s);
 
 cudaError_t launch_count_valid(const uint8_t* mask, int64_t N, int32_t* n_valid, cudaStream_t s);
 cudaError_t launch_teacher_prologue(const int32_t* ids, const float* tlog, int rows, int K, int64_t V,
@@ -117,6 +119,10 @@ cudaError_t launch_loss_reduce(const float* kl, const uint8_t* mask, int64_t N, 
                                float* loss_out, cudaStream_t s);
 
 cudaError_t launch_wait_timeout(uint32_t* err, uint64_t limit_ns, cudaStream_t s);
+cudaError_t launch_dz_from_z(const uint16_t* z, int64_t N, int64_t c0, int rows, int64_t V, int64_t nvb,
+                             int64_t rows_pad, const float* lse, const uint8_t* mask, const float* grad_loss,
+                             const int32_t* n_valid, float inv_tau, const int32_t* ids_sorted, const float* p_sorted,
+                             int K, uint16_t* dz, cudaStream_t s);
 cudaError_t launch_split_reduce(const float* parts, int splits, int64_t split_stride, int64_t count, void* out,
                                 int out_bf16, cudaStream_t s);
 

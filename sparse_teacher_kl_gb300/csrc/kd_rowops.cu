@@ -196,6 +196,91 @@ cudaError_t launch_loss_reduce(const float* kl, const uint8_t* mask, int64_t N, 
   return cudaGetLastError();
 }
 
+// ------------------------------------------- dZ from stored logits ---
+// Forward-chunked backward ([ART] fused-loss paragraph, second formulation: the
+// chunk's student logits were kept by the forward pass, so the backward reads
+// them instead of recomputing the projection):
+//   dZ_t,v = grad_loss * mask_t / (N_valid * tau) * (2^(z_t,v log2e / tau - lse_t log2e) - p_t,v)
+// Both z and dZ use the blocked layout [V/64][rows][64].  The dense part runs over
+// contiguous 16-byte vectors; the K cached ids of each row are then rewritten
+// with their teacher probability subtracted (one rounding, as in the fused path).
+
+__device__ __forceinline__ float dz_rowscale(const uint8_t* mask, int t, const float* grad_loss,
+                                             const int32_t* n_valid, float inv_tau) {
+  const int nv = *n_valid;
+  const bool valid = (mask == nullptr) || (mask[t] != 0);
+  return (valid && nv > 0) ? (*grad_loss) * inv_tau / float(nv) : 0.f;
+}
+
+__global__ void kd_dz_from_z_kernel(const uint16_t* __restrict__ z, int64_t N, int64_t c0, int rows, int64_t V,
+                                    int64_t nvb, int64_t rows_pad, const float* __restrict__ lse,
+                                    const uint8_t* __restrict__ mask, const float* __restrict__ grad_loss,
+                                    const int32_t* __restrict__ n_valid, float inv_tau, uint16_t* __restrict__ dz) {
+  const float scale2 = 1.4426950408889634f * inv_tau;
+  const int64_t total = nvb * int64_t(rows) * 8;
+  for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < total; i += int64_t(gridDim.x) * blockDim.x) {
+    const int64_t vb = i / (int64_t(rows) * 8);
+    const int64_t rem = i - vb * int64_t(rows) * 8;
+    const int t = int(rem >> 3);
+    const int j8 = int(rem & 7);
+    const int64_t v0 = vb * 64 + j8 * 8;
+    const uint4 zin = *reinterpret_cast<const uint4*>(z + ((vb * N + c0 + t) * 64 + j8 * 8));
+    const float lse2 = lse[t] * 1.4426950408889634f;
+    const float rs = dz_rowscale(mask, t, grad_loss, n_valid, inv_tau);
+    const uint32_t w[4] = {zin.x, zin.y, zin.z, zin.w};
+    float q[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const float zv = __uint_as_float((w[e >> 1] >> (16 * (e & 1))) << 16);
+      q[e] = (v0 + e < V) ? rs * ex2_approx(fmaf(zv, scale2, -lse2)) : 0.f;
+    }
+    uint4 out;
+    out.x = pack_bf16x2(q[0], q[1]);
+    out.y = pack_bf16x2(q[2], q[3]);
+    out.z = pack_bf16x2(q[4], q[5]);
+    out.w = pack_bf16x2(q[6], q[7]);
+    *reinterpret_cast<uint4*>(dz + ((vb * rows_pad + t) * 64 + j8 * 8)) = out;
+  }
+}
+
+__global__ void kd_dz_fixup_kernel(const uint16_t* __restrict__ z, int64_t N, int64_t c0, int rows, int64_t V,
+                                   int64_t rows_pad, const float* __restrict__ lse, const uint8_t* __restrict__ mask,
+                                   const float* __restrict__ grad_loss, const int32_t* __restrict__ n_valid,
+                                   float inv_tau, const int32_t* __restrict__ ids_sorted,
+                                   const float* __restrict__ p_sorted, int K, uint16_t* __restrict__ dz) {
+  const float scale2 = 1.4426950408889634f * inv_tau;
+  const int64_t total = int64_t(rows) * K;
+  for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < total; i += int64_t(gridDim.x) * blockDim.x) {
+    const int t = int(i / K);
+    const int32_t v = ids_sorted[i];
+    if (v < 0 || int64_t(v) >= V) continue;  // reported by the prologue
+    const int64_t vb = v >> 6, j = v & 63;
+    const float zv = __uint_as_float(uint32_t(z[(vb * N + c0 + t) * 64 + j]) << 16);
+    const float q = ex2_approx(fmaf(zv, scale2, -lse[t] * 1.4426950408889634f));
+    const float rs = dz_rowscale(mask, t, grad_loss, n_valid, inv_tau);
+    const uint32_t packed = pack_bf16x2(rs * (q - p_sorted[i]), 0.f);
+    dz[(vb * rows_pad + t) * 64 + j] = uint16_t(packed & 0xFFFFu);
+  }
+}
+
+cudaError_t launch_dz_from_z(const uint16_t* z, int64_t N, int64_t c0, int rows, int64_t V, int64_t nvb,
+                             int64_t rows_pad, const float* lse, const uint8_t* mask, const float* grad_loss,
+                             const int32_t* n_valid, float inv_tau, const int32_t* ids_sorted, const float* p_sorted,
+                             int K, uint16_t* dz, cudaStream_t s) {
+  const int grid = 8 * gemm_max_grid();
+  prof_before("kd_dz_from_z", s);
+  kd_dz_from_z_kernel<<<grid, 256, 0, s>>>(z, N, c0, rows, V, nvb, rows_pad, lse, mask, grad_loss, n_valid, inv_tau,
+                                            dz);
+  prof_after(s);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  prof_before("kd_dz_fixup", s);
+  kd_dz_fixup_kernel<<<(rows * K + 255) / 256, 256, 0, s>>>(z, N, c0, rows, V, rows_pad, lse, mask, grad_loss,
+                                                            n_valid, inv_tau, ids_sorted, p_sorted, K, dz);
+  prof_after(s);
+  return cudaGetLastError();
+}
+
 // -------------------------------------------------- split-K reduction ---
 // out[i] = sum over s of parts[s * stride + i], in split order (deterministic),
 // to bf16 or fp32.  count and stride are multiples of 4.

@@ -14,6 +14,10 @@
 // only entries with key >= T are kept; from then on an element needs key > T
 // (any later element with key == T has a larger column and ranks below the K
 // kept ones).  The survivors are sorted once at the end.
+//
+// Optionally the same pass also takes the full-row logsumexp of the teacher
+// logits, so that the probability mass the cache drops, 1 - sum_k e^(t_k - lse),
+// can be reported per position ([ART] paragraph on the top-K limitation).
 #include <stdint.h>
 
 #include "kd_device.cuh"
@@ -31,6 +35,8 @@ constexpr int TK_HOLD = TK_CAP / TK_THREADS;   // buffer entries per thread
 struct TopkSmem {
   unsigned long long buf[TK_CAP];
   uint32_t hist[256];
+  float red_m[TK_THREADS / 32];
+  float red_s[TK_THREADS / 32];
   uint32_t count;
   uint32_t sel_bin;
   uint32_t sel_need;
@@ -191,7 +197,7 @@ __device__ __forceinline__ uint4 load_seg(const uint16_t* xr, int64_t V, int seg
 
 __global__ void __launch_bounds__(TK_THREADS, 2)
     kd_topk_kernel(const uint16_t* __restrict__ X, int64_t N, int64_t V, int64_t ld, int K,
-                   int32_t* __restrict__ ids_out, float* __restrict__ vals_out) {
+                   int32_t* __restrict__ ids_out, float* __restrict__ vals_out, float* __restrict__ lse_out) {
   extern __shared__ __align__(16) uint8_t tk_smem_raw[];
   TopkSmem& sm = *reinterpret_cast<TopkSmem*>(tk_smem_raw);
   const int nseg = int((V + TK_SEG - 1) / TK_SEG);
@@ -200,6 +206,8 @@ __global__ void __launch_bounds__(TK_THREADS, 2)
     const uint16_t* xr = X + row * ld;
     if (threadIdx.x == 0) sm.count = 0;
     int thresh = -1;  // accept every element until the first compaction
+    // optional full-row logsumexp (base 2, per thread: running max and scaled sum)
+    float lm = -INFINITY, ls = 0.f;
     uint4 pipe[TK_PIPE];
 #pragma unroll
     for (int j = 0; j < TK_PIPE; ++j)
@@ -215,6 +223,24 @@ __global__ void __launch_bounds__(TK_THREADS, 2)
           if (seg + TK_PIPE < nseg) pipe[j] = load_seg(xr, V, seg + TK_PIPE);
           const uint32_t w[4] = {v.x, v.y, v.z, v.w};
           const int64_t i0 = int64_t(seg) * TK_SEG + int64_t(threadIdx.x) * TK_VEC;
+          if (lse_out != nullptr) {
+            float x2[TK_VEC];
+            float vm = -INFINITY;
+#pragma unroll
+            for (int e = 0; e < TK_VEC; ++e) {
+              const float xv = __uint_as_float((w[e >> 1] >> (16 * (e & 1))) << 16) * 1.4426950408889634f;
+              x2[e] = (i0 + e < V) ? xv : -INFINITY;
+              vm = fmaxf(vm, x2[e]);
+            }
+            const float nm = fmaxf(lm, vm);
+            if (nm != -INFINITY) {
+              float acc = ls * ex2_approx(lm - nm);
+#pragma unroll
+              for (int e = 0; e < TK_VEC; ++e) acc += ex2_approx(x2[e] - nm);
+              ls = acc;
+              lm = nm;
+            }
+          }
 #pragma unroll
           for (int e = 0; e < TK_VEC; ++e) {
             const uint32_t key = bf16_key(w[e >> 1] >> (16 * (e & 1)));
@@ -228,6 +254,35 @@ __global__ void __launch_bounds__(TK_THREADS, 2)
           __syncthreads();  // every thread has read the count before anyone appends again
           if (cnt > uint32_t(TK_CAP - TK_SEG)) thresh = compact(sm, uint32_t(K));
         }
+      }
+    }
+
+    if (lse_out != nullptr) {
+      // merge the threads' (max, sum) pairs: warp shuffles, then warp 0 over the warps
+      for (int o = 16; o > 0; o >>= 1) {
+        const float om = __shfl_xor_sync(0xffffffffu, lm, o);
+        const float os = __shfl_xor_sync(0xffffffffu, ls, o);
+        const float nm = fmaxf(lm, om);
+        if (nm != -INFINITY) {
+          ls = ls * ex2_approx(lm - nm) + os * ex2_approx(om - nm);
+          lm = nm;
+        }
+      }
+      if ((threadIdx.x & 31) == 0) {
+        sm.red_m[threadIdx.x >> 5] = lm;
+        sm.red_s[threadIdx.x >> 5] = ls;
+      }
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        float M = -INFINITY, S = 0.f;
+        for (int i = 0; i < TK_THREADS / 32; ++i) {
+          const float nm = fmaxf(M, sm.red_m[i]);
+          if (nm != -INFINITY) {
+            S = S * exp2f(M - nm) + sm.red_s[i] * exp2f(sm.red_m[i] - nm);
+            M = nm;
+          }
+        }
+        lse_out[row] = (M + log2f(S)) * 0.69314718055994531f;
       }
     }
 
@@ -252,7 +307,7 @@ __global__ void __launch_bounds__(TK_THREADS, 2)
 }
 
 cudaError_t launch_topk(const uint16_t* X, int64_t N, int64_t V, int64_t ld, int K, int32_t* ids, float* vals,
-                        uint32_t* err, cudaStream_t s) {
+                        float* lse, uint32_t* err, cudaStream_t s) {
   (void)err;
   static bool attr_set = false;
   const int smem = int(sizeof(TopkSmem));
@@ -265,7 +320,7 @@ cudaError_t launch_topk(const uint16_t* X, int64_t N, int64_t V, int64_t ld, int
   if (int64_t(grid) > N) grid = int(N);
   if (grid <= 0) return cudaSuccess;
   prof_before("kd_topk_cache", s);
-  kd_topk_kernel<<<grid, TK_THREADS, smem, s>>>(X, N, V, ld, K, ids, vals);
+  kd_topk_kernel<<<grid, TK_THREADS, smem, s>>>(X, N, V, ld, K, ids, vals, lse);
   prof_after(s);
   return cudaGetLastError();
 }

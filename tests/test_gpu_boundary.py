@@ -33,9 +33,9 @@ def test_invalid_calls_do_not_touch_outputs(kd, cuda_device):
     vals = torch.full((4, 8), 3.0, device=dev)
     ws = kd.workspace(256, dev)
     s = torch.cuda.current_stream().cuda_stream
-    assert kd._abi.kd_topk_cache(X.data_ptr(), 4, 256, 256, 300, ids.data_ptr(), vals.data_ptr(), ws.data_ptr(),
-                                 256, s) == kd._abi.KD_ERR_INVALID_ARG
-    assert kd._abi.kd_topk_cache(X.data_ptr() + 2, 4, 256, 256, 8, ids.data_ptr(), vals.data_ptr(),
+    assert kd._abi.kd_topk_cache(X.data_ptr(), 4, 256, 256, 300, ids.data_ptr(), vals.data_ptr(), None,
+                                 ws.data_ptr(), 256, s) == kd._abi.KD_ERR_INVALID_ARG
+    assert kd._abi.kd_topk_cache(X.data_ptr() + 2, 4, 256, 256, 8, ids.data_ptr(), vals.data_ptr(), None,
                                  ws.data_ptr(), 256, s) == kd._abi.KD_ERR_INVALID_ARG
     torch.cuda.synchronize()
     assert torch.all(ids == -7) and torch.all(vals == 3.0)

@@ -243,3 +243,43 @@ def test_full_workload_masked_subset(kd, cuda_device, name):
     assert torch.all(gH[others] == 0)
     gW = out2["grad_W"][torch.as_tensor(vrows, device=dev)].double().cpu().numpy()
     assert maxrel(gW, ref.grad_W) <= GRAD_TOL
+
+
+# ----------------------------------------------------------------------------
+# Forward-chunked mode: the forward keeps each chunk's logits (bf16), the backward
+# reads them instead of recomputing.  Checked against the oracle's forward-chunked
+# formulation (which keeps float64 logits) with the same tolerances, and against
+# the fused path's own forward (same arithmetic, so equal up to launch order).
+
+def run_chunked(kd, dev, H, W, ids, tlog, mask, chunk, tau=1.0, grad=1.0):
+    Hd, Wd, idd, tld = (t.to(dev).contiguous() for t in (H, W, ids, tlog))
+    md = None if mask is None else mask.to(dev).contiguous()
+    kl = torch.empty(Hd.shape[0], dtype=torch.float32, device=dev)
+    loss, lse, ws, z = kd.chunked_kl_forward(Hd, Wd, idd, tld, md, chunk, tau, kl_out=kl)
+    g = torch.full((1,), grad, dtype=torch.float32, device=dev)
+    gH, gW = kd.chunked_kl_backward(Hd, Wd, idd, tld, md, lse, g, z, chunk, tau, ws=ws, grad_H_fp32=True)
+    torch.cuda.synchronize()
+    assert kd.device_error(ws)[0] == 0
+    return dict(loss=loss, lse=lse, kl=kl, grad_H=gH, grad_W=gW, z=z)
+
+
+@pytest.mark.parametrize("N,d,V,K,chunk,tau", [
+    (128, 256, 4096, 16, 128, 1.0),
+    (300, 72, 1000, 5, 128, 1.0),
+    (257, 136, 1001, 33, 256, 2.0),
+])
+def test_forward_chunked_matches_oracle(kd, cuda_device, N, d, V, K, chunk, tau):
+    w = Workload("fc", 1, N, d, V, K, chunk, "normal3", 0.9, 777 + N)
+    H, W, ids, tlog, mask = _host(w)
+    out = run_chunked(kd, cuda_device, H, W, ids, tlog, mask, chunk, tau, grad=0.5)
+    ref = oracle.forward_chunked_kl(bf16_bits(H), bf16_bits(W), ids.numpy(), tlog.numpy(), mask.numpy(), tau,
+                                    chunk=chunk, grad_loss=0.5)
+    compare_full(out, ref)
+    fused = run_gpu(kd, cuda_device, H, W, ids, tlog, mask, chunk=chunk, tau=tau, want_bwd=False)
+    assert abs(out["loss"].item() - fused["loss"].item()) <= 1e-6 * abs(fused["loss"].item())
+    # the kept logits are H W^T rounded to bf16, in the blocked layout
+    nvb = (V + 63) // 64
+    zb = out["z"].view(torch.int16).view(nvb, N, 64).permute(1, 0, 2).reshape(N, nvb * 64)[:, :V]
+    zg = zb.contiguous().view(torch.bfloat16).double().cpu().numpy()
+    zr = oracle.bf16_to_f64(bf16_bits(H)) @ oracle.bf16_to_f64(bf16_bits(W)).T
+    assert np.max(np.abs(zg - zr) / (np.abs(zr) + 1e-3)) <= 2.0 ** -7

@@ -31,11 +31,17 @@ def _check(kd, X_host, K, dev, rows=None, ld=None):
     ids = torch.empty((N, K), dtype=torch.int32, device=dev)
     vals = torch.empty((N, K), dtype=torch.float32, device=dev)
     ws = kd.workspace(kd._abi.kd_topk_cache_workspace(N, V, K), dev)
+    lse = torch.empty((N,), dtype=torch.float32, device=dev)
     st = kd._abi.kd_topk_cache(Xd.data_ptr(), N, V, Xd.stride(0), K, ids.data_ptr(), vals.data_ptr(),
-                               ws.data_ptr(), ws.numel(), torch.cuda.current_stream().cuda_stream)
+                               lse.data_ptr(), ws.data_ptr(), ws.numel(), torch.cuda.current_stream().cuda_stream)
     assert st == 0
     torch.cuda.synchronize()
     rows = np.arange(N) if rows is None else np.asarray(rows)
+    ref_lse = oracle.teacher_logsumexp(bf16_bits(X_host[torch.as_tensor(rows)]))
+    got_lse = lse.cpu().numpy()[rows].astype(np.float64)
+    fin = np.isfinite(ref_lse)
+    assert np.array_equal(np.isfinite(got_lse), fin)
+    assert np.max(np.abs(got_lse[fin] - ref_lse[fin]), initial=0.0) <= 1e-5 * max(1.0, np.max(np.abs(ref_lse[fin]), initial=1.0))
     bits = bf16_bits(X_host[torch.as_tensor(rows)])
     rid, rval = oracle.topk_cache(bits, K)
     gid = ids.cpu().numpy()[rows]
@@ -84,7 +90,7 @@ def test_topk_mid_workload_sampled(kd, cuda_device):
     ids = torch.empty((w.N, w.K), dtype=torch.int32, device=cuda_device)
     vals = torch.empty((w.N, w.K), dtype=torch.float32, device=cuda_device)
     ws = kd.workspace(kd._abi.kd_topk_cache_workspace(w.N, w.V, w.K), cuda_device)
-    st = kd._abi.kd_topk_cache(X.data_ptr(), w.N, w.V, w.V, w.K, ids.data_ptr(), vals.data_ptr(),
+    st = kd._abi.kd_topk_cache(X.data_ptr(), w.N, w.V, w.V, w.K, ids.data_ptr(), vals.data_ptr(), None,
                                ws.data_ptr(), ws.numel(), torch.cuda.current_stream().cuda_stream)
     assert st == 0
     torch.cuda.synchronize()
@@ -99,3 +105,16 @@ def test_topk_mid_workload_sampled(kd, cuda_device):
     assert bool((v[:, 1:] <= v[:, :-1]).all())
     s, _ = torch.sort(ids.cpu(), dim=1)
     assert bool((s[:, 1:] != s[:, :-1]).all())
+
+
+def test_topk_dropped_mass(kd, cuda_device):
+    """The mass outside the cache, from the cached values and the row logsumexp, against the oracle;
+    zero (up to rounding) when K = V."""
+    X = make_dense_teacher_logits(16, 2048, seed=3, std=3.0)
+    Xd = X.to(cuda_device)
+    for K in (16, 2048 if 2048 <= kd.KD_MAX_K else 1024):
+        ids, vals, lse = kd.topk_cache(Xd, K, with_lse=True)
+        got = kd.dropped_mass(vals, lse).double().cpu().numpy()
+        ref = oracle.dropped_mass(bf16_bits(X), K)
+        assert np.max(np.abs(got - ref)) <= 1e-5
+    assert np.all(ref >= -1e-12)

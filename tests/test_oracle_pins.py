@@ -238,3 +238,20 @@ def test_bf16_widening_is_exact():
     bits = _bf16_bits_of(x)
     y = oracle.bf16_to_f64(bits)
     assert np.array_equal(y, torch.tensor(x).to(torch.bfloat16).double().numpy())
+
+
+# The teacher's full-row logsumexp (tail-mass diagnostic) is the library logsumexp;
+# the dropped mass is 0 with K = V, in [0, 1) otherwise, and shrinks as K grows.
+def test_teacher_logsumexp_and_dropped_mass():
+    rng = np.random.default_rng(8)
+    x = rng.standard_normal((6, 300)) * 3
+    bits = _bf16_bits_of(x)
+    vals = oracle.bf16_to_f64(bits)
+    assert np.allclose(oracle.teacher_logsumexp(bits), scipy.special.logsumexp(vals, axis=1), rtol=1e-14, atol=0)
+    assert np.max(np.abs(oracle.dropped_mass(bits, 300))) <= 1e-13
+    d10, d50 = oracle.dropped_mass(bits, 10), oracle.dropped_mass(bits, 50)
+    assert np.all((d10 > 0) & (d10 < 1)) and np.all(d50 < d10)
+    # by hand: top-1 of [0, ln 3] keeps 3/4 of the mass
+    b = _bf16_bits_of(np.array([[0.0, np.log(3.0)]]))
+    v = oracle.bf16_to_f64(b)[0]
+    assert abs(oracle.dropped_mass(b, 1)[0] - np.exp(v[0]) / (np.exp(v[0]) + np.exp(v[1]))) <= 1e-15
