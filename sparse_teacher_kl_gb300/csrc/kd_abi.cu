@@ -4,6 +4,7 @@
 #include <cudaTypedefs.h>
 #include <math.h>
 #include <stdio.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include <mutex>
@@ -141,6 +142,21 @@ static KlLayout kl_layout(int64_t N, int64_t d, int64_t V, int K, int64_t chunk)
   return L;
 }
 
+// CTA pairs sharing the B operand (see GemmProblem::cluster) for a launch with
+// m_tiles row tiles.  The loss epilogues need an even m_tiles (no phantom tile
+// writing past the chunk); the gradient products check their rows themselves.
+// KD_GEMM_CLUSTER=1 in the environment turns pairing off (for measurements).
+static int pick_cluster(int epi, int m_tiles) {
+  static int env = -1;
+  if (env < 0) {
+    const char* v = getenv("KD_GEMM_CLUSTER");
+    env = (v && v[0] == '1') ? 1 : 2;
+  }
+  if (env == 1 || m_tiles < 2) return 1;
+  if ((epi == EPI_LSE || epi == EPI_DZ || epi == EPI_LSE_Z) && (m_tiles % 2) != 0) return 1;
+  return 2;
+}
+
 // Number of K splits for a product of `tiles` output tiles with `k_blocks` steps of
 // BK each: the fewest waves of `grid` persistent CTAs per unit of work, with a small
 // charge per split for the extra partial traffic.
@@ -259,8 +275,10 @@ static int fwd_impl(const void* H_bf16, const void* W_bf16, const int32_t* t_ids
   const float inv_tau = 1.0f / tau;
   const uint16_t* H = static_cast<const uint16_t*>(H_bf16);
 
-  alignas(64) CUtensorMap tw, th, tz;
+  alignas(64) CUtensorMap tw, tw_half, th, tz;
   if (!make_tmap_2d_bf16(&tw, W_bf16, uint64_t(d), uint64_t(V), uint64_t(d) * 2, BK, BN)) return KD_ERR_CUDA;
+  if (!make_tmap_2d_bf16(&tw_half, W_bf16, uint64_t(d), uint64_t(V), uint64_t(d) * 2, BK, BN / 2))
+    return KD_ERR_CUDA;
   if (z_store) {
     (void)z_bytes;
     if (!make_tmap_dz_blocked(&tz, z_store, uint64_t(N), uint64_t(N), uint64_t((V + 63) / 64), 32))
@@ -283,11 +301,12 @@ static int fwd_impl(const void* H_bf16, const void* W_bf16, const int32_t* t_ids
     p.m_tiles = (n + BM - 1) / BM;
     p.n_tiles = int((V + BN - 1) / BN);
     p.n_group = choose_n_group(V);
-    p.n_units = p.m_tiles * ((p.n_tiles + p.n_group - 1) / p.n_group);
+    p.cluster = pick_cluster(p.epi, p.m_tiles);
+    p.n_units = ((p.m_tiles + p.cluster - 1) / p.cluster) * ((p.n_tiles + p.n_group - 1) / p.n_group);
     p.k_splits = 1;
     p.ids_sorted = ids_sorted; p.p_sorted = p_sorted; p.Kt = K; p.inv_tau = inv_tau;
     p.partials = partials; p.rows = n; p.err = &ctrl->err;
-    e = launch_gemm(p, th, tw, z_store ? tz : tw, grid_max, s);
+    e = launch_gemm(p, th, p.cluster > 1 ? tw_half : tw, z_store ? tz : tw, grid_max, s);
     if (e != cudaSuccess) return KD_ERR_CUDA;
     e = launch_lse_combine(partials, L.n_groups, n, negent, inv_tau, lse_out + c0, kl + c0, s);
     if (e != cudaSuccess) return KD_ERR_CUDA;
@@ -322,8 +341,10 @@ static int bwd_impl(const void* H_bf16, const void* W_bf16, const int32_t* t_ids
   const uint16_t* H = static_cast<const uint16_t*>(H_bf16);
   const size_t gh_elt = grad_H_is_fp32 ? 4 : 2;
 
-  alignas(64) CUtensorMap tw_k, tw_mn, th_k, th_mn, tdz_k, tdz_mn, tdz_st, tgw;
+  alignas(64) CUtensorMap tw_k, tw_k_half, tw_mn, th_k, th_mn, tdz_k, tdz_mn, tdz_st, tgw;
   if (!make_tmap_2d_bf16(&tw_k, W_bf16, uint64_t(d), uint64_t(V), uint64_t(d) * 2, BK, BN)) return KD_ERR_CUDA;
+  if (!make_tmap_2d_bf16(&tw_k_half, W_bf16, uint64_t(d), uint64_t(V), uint64_t(d) * 2, BK, BN / 2))
+    return KD_ERR_CUDA;
   if (!make_tmap_2d_f32(&tgw, grad_W, uint64_t(d), uint64_t(V), uint64_t(d) * 4, 32, 32)) return KD_ERR_CUDA;
   if (!make_tmap_2d_bf16(&tw_mn, W_bf16, uint64_t(d), uint64_t(V), uint64_t(d) * 2, 64, BK)) return KD_ERR_CUDA;
 
@@ -357,12 +378,13 @@ static int bwd_impl(const void* H_bf16, const void* W_bf16, const int32_t* t_ids
     p.m_tiles = (n + BM - 1) / BM;
     p.n_tiles = int((V + BN - 1) / BN);
     p.n_group = 1;
-    p.n_units = p.m_tiles * p.n_tiles;
+    p.cluster = pick_cluster(p.epi, p.m_tiles);
+    p.n_units = ((p.m_tiles + p.cluster - 1) / p.cluster) * p.n_tiles;
     p.k_splits = 1;
     p.ids_sorted = ids_sorted; p.p_sorted = p_sorted; p.Kt = K; p.inv_tau = inv_tau;
     p.lse = lse + c0; p.mask = mask ? mask + c0 : nullptr; p.grad_loss = grad_loss; p.n_valid = &ctrl->n_valid;
     p.dz = dz; p.ldz = L.ldz; p.rows = n; p.err = &ctrl->err;
-    e = launch_gemm(p, th_k, tw_k, tdz_st, grid_max, s);
+    e = launch_gemm(p, th_k, p.cluster > 1 ? tw_k_half : tw_k, tdz_st, grid_max, s);
     if (e != cudaSuccess) return KD_ERR_CUDA;
     }
 
@@ -375,7 +397,8 @@ static int bwd_impl(const void* H_bf16, const void* W_bf16, const int32_t* t_ids
     q.n_group = 1;
     q.a_blocked = 1;
     q.k_splits = choose_splits(int64_t(q.m_tiles) * q.n_tiles, int((V + BK - 1) / BK), grid_max);
-    q.n_units = q.m_tiles * q.n_tiles * q.k_splits;
+    q.cluster = pick_cluster(q.epi, q.m_tiles);
+    q.n_units = ((q.m_tiles + q.cluster - 1) / q.cluster) * q.n_tiles * q.k_splits;
     void* gh_out = static_cast<uint8_t*>(grad_H) + size_t(c0) * d * gh_elt;
     if (q.k_splits == 1) {
       q.C = gh_out;
@@ -403,7 +426,8 @@ static int bwd_impl(const void* H_bf16, const void* W_bf16, const int32_t* t_ids
     r.n_group = 1;
     r.a_blocked = 1;
     r.k_splits = 1;
-    r.n_units = r.m_tiles * r.n_tiles;
+    r.cluster = pick_cluster(r.epi, r.m_tiles);
+    r.n_units = ((r.m_tiles + r.cluster - 1) / r.cluster) * r.n_tiles;
     r.C = grad_W; r.ldc = d; r.c_bf16 = 0; r.err = &ctrl->err;
     e = launch_gemm(r, tdz_mn, th_mn, tgw, grid_max, s);
     if (e != cudaSuccess) return KD_ERR_CUDA;
@@ -486,8 +510,10 @@ int kd_gemm_bf16(const void* A, const void* B, float* C, int64_t M, int64_t N, i
   alignas(64) CUtensorMap ta, tb, tc;
   bool ok = a_mn ? make_tmap_2d_bf16(&ta, A, uint64_t(M), uint64_t(K), uint64_t(M) * 2, 64, BK)
                  : make_tmap_2d_bf16(&ta, A, uint64_t(K), uint64_t(M), uint64_t(K) * 2, BK, BM);
+  const int m_tiles = int((M + BM - 1) / BM);
+  const int cluster = pick_cluster(accumulate ? EPI_ACCUM : EPI_STORE, m_tiles);
   ok = ok && (b_mn ? make_tmap_2d_bf16(&tb, B, uint64_t(N), uint64_t(K), uint64_t(N) * 2, 64, BK)
-                   : make_tmap_2d_bf16(&tb, B, uint64_t(K), uint64_t(N), uint64_t(K) * 2, BK, BN));
+                   : make_tmap_2d_bf16(&tb, B, uint64_t(K), uint64_t(N), uint64_t(K) * 2, BK, BN / cluster));
   ok = ok && make_tmap_2d_f32(&tc, C, uint64_t(N), uint64_t(M), uint64_t(N) * 4, 32, 32);
   if (!ok) return KD_ERR_CUDA;
   GemmProblem p{};
@@ -498,7 +524,8 @@ int kd_gemm_bf16(const void* A, const void* B, float* C, int64_t M, int64_t N, i
   p.n_tiles = int((N + BN - 1) / BN);
   p.n_group = 1;
   p.k_splits = 1;
-  p.n_units = p.m_tiles * p.n_tiles;
+  p.cluster = cluster;
+  p.n_units = ((p.m_tiles + p.cluster - 1) / p.cluster) * p.n_tiles;
   p.C = C; p.ldc = N; p.c_bf16 = 0;
   p.err = &static_cast<Ctrl*>(ws)->err;
   return map_cuda(launch_gemm(p, ta, tb, tc, gemm_max_grid(), static_cast<cudaStream_t>(stream)));

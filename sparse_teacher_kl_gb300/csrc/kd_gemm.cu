@@ -43,12 +43,13 @@ static_assert(GEMM_SMEM_BYTES <= 232448, "shared memory budget of one CTA");
 // Unit u -> tile coordinates.  LSE/DZ walk the vocabulary (n) slowly so that
 // every CTA in flight reads the same few W tiles while the small H chunk stays
 // in L2; the gradient products walk n fastest so that CTAs in flight share A.
-__device__ __forceinline__ void unit_coords(const GemmProblem& p, int u, int& m_blk, int& n_first, int& n_count,
-                                            int& kb_lo, int& kb_hi, int& split) {
+__device__ __forceinline__ void unit_coords(const GemmProblem& p, int u, uint32_t crank, int& m_blk, int& n_first,
+                                            int& n_count, int& kb_lo, int& kb_hi, int& split) {
   const int k_blocks = (p.K + BK - 1) / BK;
+  const int m_groups = (p.m_tiles + p.cluster - 1) / p.cluster;
   if (p.epi == EPI_LSE || p.epi == EPI_DZ || p.epi == EPI_LSE_Z) {
-    const int g = u / p.m_tiles;
-    m_blk = u - g * p.m_tiles;
+    const int g = u / m_groups;
+    m_blk = (u - g * m_groups) * p.cluster + int(crank);
     n_first = g * p.n_group;
     n_count = min(p.n_group, p.n_tiles - n_first);
     kb_lo = 0;
@@ -57,11 +58,12 @@ __device__ __forceinline__ void unit_coords(const GemmProblem& p, int u, int& m_
   } else {
     // split slowest, then m, then n: the CTAs in flight share one K range, so each
     // A slab is read by all n tiles and each B slab by all m tiles from L2.
-    const int per_split = p.m_tiles * p.n_tiles;
+    const int per_split = m_groups * p.n_tiles;
     split = u / per_split;
     const int r = u - split * per_split;
-    m_blk = r / p.n_tiles;
-    n_first = r - m_blk * p.n_tiles;
+    const int mg = r / p.n_tiles;
+    m_blk = mg * p.cluster + int(crank);
+    n_first = r - mg * p.n_tiles;
     n_count = 1;
     kb_lo = int((int64_t(k_blocks) * split) / p.k_splits);
     kb_hi = int((int64_t(k_blocks) * (split + 1)) / p.k_splits);
@@ -81,11 +83,15 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 
   const uint32_t warp = threadIdx.x >> 5;
   const uint32_t lane = lane_id();
+  const uint32_t crank = p.cluster > 1 ? cluster_ctarank() : 0u;
+  const uint16_t cmask = uint16_t((1u << p.cluster) - 1u);
+  const int u_first = int(blockIdx.x) / p.cluster;
+  const int u_step = int(gridDim.x) / p.cluster;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&tail->full[s], 1);
-      mbar_init(&tail->empty[s], 1);
+      mbar_init(&tail->empty[s], uint32_t(p.cluster));  // every CTA whose data lands in this stage
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tail->tfull[a], 1);
@@ -105,6 +111,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if (p.cluster > 1) cluster_sync();  // the peer's barriers exist before any multicast reaches them
   tc_fence_after();
   const uint32_t tmem_base = tail->tmem_base;
 
@@ -113,9 +120,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     if (lane == 0) {
       uint32_t it = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x) {
+      for (int u = u_first; u < p.n_units && ok; u += u_step) {
         int m_blk, n_first, n_count, kb_lo, kb_hi, split;
-        unit_coords(p, u, m_blk, n_first, n_count, kb_lo, kb_hi, split);
+        unit_coords(p, u, crank, m_blk, n_first, n_count, kb_lo, kb_hi, split);
         for (int nb = n_first; nb < n_first + n_count && ok; ++nb) {
           for (int kb = kb_lo; kb < kb_hi; ++kb, ++it) {
             const uint32_t s = it % STAGES;
@@ -144,7 +151,19 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
               for (int j = 0; j < BM / 64; ++j)
                 tma_load_2d(sa + j * 8192, &tmap_a, &tail->full[s], m_blk * BM + j * 64, kb * BK);
             }
-            if (p.b_mn == 0) {
+            if (p.cluster > 1) {
+              // this CTA's half of B, multicast to both CTAs of the pair
+              if (p.b_mn == 0) {
+                tma_load_2d_mc(sb + crank * (STAGE_B_BYTES / 2), &tmap_b, &tail->full[s], kb * BK,
+                               nb * BN + int(crank) * (BN / 2), cmask);
+              } else {
+#pragma unroll
+                for (int j = 0; j < BN / 128; ++j) {
+                  const int jj = int(crank) * (BN / 128) + j;
+                  tma_load_2d_mc(sb + jj * 8192, &tmap_b, &tail->full[s], nb * BN + jj * 64, kb * BK, cmask);
+                }
+              }
+            } else if (p.b_mn == 0) {
               tma_load_2d(sb, &tmap_b, &tail->full[s], kb * BK, nb * BN);
             } else {
 #pragma unroll
@@ -173,9 +192,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       const uint32_t b_lbo = p.b_mn ? 8192u : 16u;
       uint32_t it = 0, acc_it = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x) {
+      for (int u = u_first; u < p.n_units && ok; u += u_step) {
         int m_blk, n_first, n_count, kb_lo, kb_hi, split;
-        unit_coords(p, u, m_blk, n_first, n_count, kb_lo, kb_hi, split);
+        unit_coords(p, u, crank, m_blk, n_first, n_count, kb_lo, kb_hi, split);
         for (int nb = n_first; nb < n_first + n_count && ok; ++nb, ++acc_it) {
           const uint32_t a = acc_it & 1u;
           const uint32_t aph = (acc_it >> 1) & 1u;
@@ -201,7 +220,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
               const uint64_t bd = sdesc_sw128(sb + k * b_step, b_lbo);
               umma_bf16(d_tmem, ad, bd, idesc, (kb != kb_lo || k != 0) ? 1u : 0u);
             }
-            umma_commit(&tail->empty[s]);
+            if (p.cluster > 1) umma_commit_mc(&tail->empty[s], cmask); else umma_commit(&tail->empty[s]);
           }
           if (ok) umma_commit(&tail->tfull[a]);
         }
@@ -221,9 +240,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     uint32_t sbuf = 0;
     uint32_t acc_it = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < p.n_units && ok; u += gridDim.x) {
+    for (int u = u_first; u < p.n_units && ok; u += u_step) {
       int m_blk, n_first, n_count, kb_lo, kb_hi, split;
-      unit_coords(p, u, m_blk, n_first, n_count, kb_lo, kb_hi, split);
+      unit_coords(p, u, crank, m_blk, n_first, n_count, kb_lo, kb_hi, split);
       const int row = m_blk * BM + r_local;
 
       // Per-row state for the loss epilogues.
@@ -454,6 +473,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 
   tc_fence_before();
   __syncthreads();
+  if (p.cluster > 1) cluster_sync();  // no multicast or remote arrival can still target this CTA
   tc_fence_after();
   if (warp == 1) {
     tmem_dealloc(tmem_base, TMEM_COLS);
@@ -476,13 +496,44 @@ template <int EPI>
 static cudaError_t launch_one(const GemmProblem& p, const CUtensorMap& ta, const CUtensorMap& tb,
                               const CUtensorMap& tc, int grid, cudaStream_t s) {
   static bool attr_set = false;
+  static int max_pairs = 0;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kd_gemm_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          int(GEMM_SMEM_BYTES));
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  kd_gemm_kernel<EPI><<<grid, GEMM_THREADS, GEMM_SMEM_BYTES, s>>>(ta, tb, tc, p);
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.blockDim = dim3(GEMM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = GEMM_SMEM_BYTES;
+  cfg.stream = s;
+  if (p.cluster > 1) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = unsigned(p.cluster);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (max_pairs == 0) {
+      // persistent grid: as many pairs as can be resident at once
+      cfg.gridDim = dim3(unsigned((gemm_max_grid() / p.cluster) * p.cluster), 1, 1);
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, kd_gemm_kernel<EPI>, &cfg) != cudaSuccess || n < 1) n = 1;
+      max_pairs = n;
+    }
+    int pairs = grid / p.cluster;
+    if (pairs > max_pairs) pairs = max_pairs;
+    if (pairs > p.n_units) pairs = p.n_units;
+    if (pairs < 1) pairs = 1;
+    cfg.gridDim = dim3(unsigned(pairs * p.cluster), 1, 1);
+  } else {
+    cfg.gridDim = dim3(unsigned(grid), 1, 1);
+    cfg.attrs = nullptr;
+    cfg.numAttrs = 0;
+  }
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kd_gemm_kernel<EPI>, ta, tb, tc, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -499,7 +550,8 @@ static const char* gemm_name(int epi, int a_mn, int b_mn) {
 cudaError_t launch_gemm(const GemmProblem& p, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
                         int grid, cudaStream_t s) {
   if (p.n_units <= 0) return cudaSuccess;
-  if (grid > p.n_units) grid = p.n_units;
+  if (p.cluster < 1 || p.cluster > 2) return cudaErrorInvalidValue;
+  if (p.cluster == 1 && grid > p.n_units) grid = p.n_units;
   prof_before(gemm_name(p.epi, p.a_mn, p.b_mn), s);
   cudaError_t e;
   switch (p.epi) {
