@@ -111,6 +111,48 @@ def ncu_traffic(kernel: str, workload: str):
     return rec.get("kernels", {}).get(workload, {}).get(kernel)
 
 
+def bench_topk(kd, dev, stream, peaks, steps):
+    """kd_topk_cache on the mid workload's dense teacher logits (8192 x 151936 bf16, N(0, 2), K = 100):
+    HBM-bound, algorithmic bytes N*V*2 read + N*K*8 written per launch."""
+    import torch
+    from synth import WORKLOADS, make_dense_teacher_logits
+    w = WORKLOADS["mid"]
+    N, V, K = w.N, w.V, w.K
+    X = make_dense_teacher_logits(N, V, seed=w.seed, device=dev)
+    ids = torch.empty((N, K), dtype=torch.int32, device=dev)
+    vals = torch.empty((N, K), dtype=torch.float32, device=dev)
+    lse = torch.empty((N,), dtype=torch.float32, device=dev)
+    ws = kd.workspace(kd._abi.kd_topk_cache_workspace(N, V, K), dev)
+    out = {"workload": f"{N}x{V} bf16 N(0,2), K={K}"}
+    for name, lp in (("ids+vals", None), ("ids+vals+lse", lse)):
+        def run():
+            st = kd._abi.kd_topk_cache(X.data_ptr(), N, V, V, K, ids.data_ptr(), vals.data_ptr(),
+                                       None if lp is None else lp.data_ptr(), ws.data_ptr(), ws.numel(),
+                                       stream.cuda_stream)
+            assert st == 0
+        for _ in range(3):
+            run()
+        torch.cuda.synchronize(dev)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(steps):
+            run()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        ms = a.elapsed_time(b) / steps
+        byts = N * V * 2 + N * K * 8 + (N * 4 if lp is not None else 0)
+        gbs = byts / (ms * 1e-3) / 1e9
+        out[name] = {"ms": ms, "achieved_gbs": gbs, "peak_gbs": peaks["hbm"], "frac": gbs / peaks["hbm"],
+                     "bytes_per_launch": byts}
+    out["roofline"] = {"bound": "hbm", "achieved": out["ids+vals"]["achieved_gbs"], "peak": peaks["hbm"],
+                       "unit": "GB/s", "frac": out["ids+vals"]["frac"],
+                       "peak_source": f"{peaks['source']} copy bandwidth"}
+    del X
+    torch.cuda.empty_cache()
+    return out
+
+
 def dense_torch_reference(H, W, ids, tlog, mask, dev):
     """Peak device memory and time of one fwd+bwd of the dense formulation in plain PyTorch
     (full [N, V] student logits and a full-vocabulary teacher grid), for the memory comparison
@@ -208,6 +250,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-modes", action="store_true", help="skip the forward-chunked and dense comparisons")
+    ap.add_argument("--no-topk", action="store_true", help="skip the top-K cache measurement")
     ap.add_argument("--rows", type=int, default=None, help="override B*T (profiling a reduced case)")
     ap.add_argument("--vocab", type=int, default=None, help="override V (profiling a reduced case)")
     args = ap.parse_args()
@@ -368,6 +411,11 @@ def main():
     if not args.no_modes and rank == 0:
         dense = dense_torch_reference(H, W, ids, tlog, mask, dev)
 
+    # ---- offline cache extraction (kd_topk_cache) on the mid workload's dense teacher logits
+    topk = None
+    if not args.no_topk and rank == 0:
+        topk = bench_topk(kd, dev, stream, peaks, args.steps)
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         from synth import bf16_bits
@@ -398,6 +446,7 @@ def main():
                          "unit": "TFLOP/s", "frac": achieved / peak, "traffic": ncu_traffic(dom_name, w.name),
                          "peak_source": f"{peaks['source']} bf16 sustained",
                          "flops_per_launch": gemm_flops_per_chunk},
+            "topk_cache": topk,
             "forward_chunked": fc,
             "dense_torch_reference": dense,
             "kernels": kernels,

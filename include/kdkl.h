@@ -96,6 +96,20 @@ KD_API int kd_topk_cache(const void* logits_bf16, int64_t N, int64_t V, int64_t 
                   int32_t* ids_out, float* vals_out, float* lse_out,
                   void* ws, size_t ws_bytes, void* stream);
 
+/*
+ * The teacher's single pass fused with the cache extraction: for N positions of
+ * teacher hidden states Ht [N, dt] bf16 and the teacher's LM-head Wt [V, dt] bf16,
+ * the logits Ht Wt^T are formed on the tensor cores `chunk` positions at a time
+ * (fp32 accumulation, rounded once to bf16 as a bf16 teacher would emit them) into a
+ * [chunk, V] workspace buffer and reduced to their top K right away, so the dense
+ * [N, V] teacher logits never exist.  Outputs as kd_topk_cache (ids, vals, optional
+ * row logsumexp).  dt % 8 == 0; chunk a multiple of 128.
+ */
+KD_API size_t kd_teacher_topk_workspace(int64_t N, int64_t dt, int64_t V, int K, int64_t chunk);
+KD_API int kd_teacher_topk(const void* Ht_bf16, const void* Wt_bf16, int64_t N, int64_t dt, int64_t V, int K,
+                           int64_t chunk, int32_t* ids_out, float* vals_out, float* lse_out,
+                           void* ws, size_t ws_bytes, void* stream);
+
 /* ------------------------------------------------------------------------ *
  * Fused chunked KL loss.
  * [ART] paragraph on the second fix; [DAI] "As duas inovações" item 2; [EPO]

@@ -26,7 +26,7 @@ from .kl import (
     fused_chunked_kl,
     OracleResult,
 )
-from .topk import topk_cache, teacher_logsumexp, dropped_mass
+from .topk import topk_cache, teacher_logsumexp, dropped_mass, teacher_logits_bf16
 
 __all__ = [
     "bf16_to_f64",
@@ -38,4 +38,5 @@ __all__ = [
     "topk_cache",
     "teacher_logsumexp",
     "dropped_mass",
+    "teacher_logits_bf16",
 ]

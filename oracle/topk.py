@@ -58,3 +58,17 @@ def dropped_mass(bits: np.ndarray, K: int) -> np.ndarray:
     lse = teacher_logsumexp(bits)
     _, vals = topk_cache(bits, K)
     return 1.0 - np.sum(np.exp(vals.astype(np.float64) - lse[:, None]), axis=1)
+
+
+def teacher_logits_bf16(Ht_bits: np.ndarray, Wt_bits: np.ndarray) -> np.ndarray:
+    """Teacher logits Ht Wt^T from bf16 inputs, as the bf16 bit patterns a bf16 teacher emits.
+
+    The product is taken in float64 and rounded to the nearest bf16 (ties to even)
+    through float32; when every product and partial sum is exact (small integer
+    inputs) this is the exact logit.  [ART] paragraph on the first fix: the
+    teacher's single pass produces the logits the cache is taken from.
+    """
+    z = bf16_to_f64(Ht_bits) @ bf16_to_f64(Wt_bits).T
+    f = z.astype(np.float32).view(np.uint32).astype(np.uint64)
+    rounded = (f + 0x7FFF + ((f >> 16) & 1)) >> 16
+    return rounded.astype(np.uint16)

@@ -20,6 +20,7 @@ from ._abi import KDError, KD_MAX_K
 
 __all__ = [
     "topk_cache",
+    "teacher_topk",
     "dropped_mass",
     "fused_kl",
     "fused_kl_forward",
@@ -78,6 +79,24 @@ def topk_cache(logits: torch.Tensor, K: int, ws: Optional[torch.Tensor] = None, 
     st = _abi.kd_topk_cache(_ptr(logits), N, V, logits.stride(0), K, _ptr(ids), _ptr(vals), _ptr(lse), _ptr(ws),
                             ws.numel(), _stream(logits.device))
     _abi.check(st, "kd_topk_cache")
+    return (ids, vals, lse) if with_lse else (ids, vals)
+
+
+def teacher_topk(Ht: torch.Tensor, Wt: torch.Tensor, K: int, chunk: int = 1024, with_lse: bool = False,
+                 ws: Optional[torch.Tensor] = None):
+    """Top-K cache straight from teacher hidden states Ht [N, dt] and LM-head Wt [V, dt] (bf16): the
+    teacher logits exist only one chunk at a time (see kd_teacher_topk)."""
+    _require_cuda(Ht, Wt)
+    N, dt = Ht.shape
+    V = Wt.shape[0]
+    ids = torch.empty((N, K), dtype=torch.int32, device=Ht.device)
+    vals = torch.empty((N, K), dtype=torch.float32, device=Ht.device)
+    lse = torch.empty((N,), dtype=torch.float32, device=Ht.device) if with_lse else None
+    if ws is None:
+        ws = workspace(_abi.kd_teacher_topk_workspace(N, dt, V, K, chunk), Ht.device)
+    st = _abi.kd_teacher_topk(_ptr(Ht), _ptr(Wt), N, dt, V, K, chunk, _ptr(ids), _ptr(vals), _ptr(lse), _ptr(ws),
+                              ws.numel(), _stream(Ht.device))
+    _abi.check(st, "kd_teacher_topk")
     return (ids, vals, lse) if with_lse else (ids, vals)
 
 

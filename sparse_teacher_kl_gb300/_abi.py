@@ -37,6 +37,9 @@ _SIGNATURES = {
     "kd_topk_cache_workspace": (_c_size, [_c_i64, _c_i64, _c_int]),
     "kd_topk_cache": (_c_int, [_c_ptr, _c_i64, _c_i64, _c_i64, _c_int, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_size,
                                _c_ptr]),
+    "kd_teacher_topk_workspace": (_c_size, [_c_i64, _c_i64, _c_i64, _c_int, _c_i64]),
+    "kd_teacher_topk": (_c_int, [_c_ptr, _c_ptr, _c_i64, _c_i64, _c_i64, _c_int, _c_i64, _c_ptr, _c_ptr, _c_ptr, _c_ptr,
+                                 _c_size, _c_ptr]),
     "kd_fused_kl_workspace": (_c_size, [_c_i64, _c_i64, _c_i64, _c_int, _c_i64]),
     "kd_fused_kl_fwd": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_i64, _c_i64, _c_i64, _c_int, _c_i64,
                                  _c_float, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_size, _c_ptr]),
@@ -122,6 +125,8 @@ kd_version = _wrap("kd_version")
 kd_topk_cache_workspace = _wrap("kd_topk_cache_workspace")
 kd_topk_cache = _wrap("kd_topk_cache")
 kd_fused_kl_workspace = _wrap("kd_fused_kl_workspace")
+kd_teacher_topk_workspace = _wrap("kd_teacher_topk_workspace")
+kd_teacher_topk = _wrap("kd_teacher_topk")
 kd_fused_kl_fwd = _wrap("kd_fused_kl_fwd")
 kd_fused_kl_bwd = _wrap("kd_fused_kl_bwd")
 kd_fused_kl_fwd_static = _wrap("kd_fused_kl_fwd_static")

@@ -142,19 +142,22 @@ static KlLayout kl_layout(int64_t N, int64_t d, int64_t V, int K, int64_t chunk)
   return L;
 }
 
-// CTA pairs sharing the B operand (see GemmProblem::cluster) for a launch with
+// CTAs per cluster sharing the B operand (see GemmProblem::cluster) for a launch with
 // m_tiles row tiles.  The loss epilogues need an even m_tiles (no phantom tile
 // writing past the chunk); the gradient products check their rows themselves.
-// KD_GEMM_CLUSTER=1 in the environment turns pairing off (for measurements).
+// KD_GEMM_CLUSTER=1, 2 or 4 in the environment forces one size (for measurements).
 static int pick_cluster(int epi, int m_tiles) {
   static int env = -1;
   if (env < 0) {
     const char* v = getenv("KD_GEMM_CLUSTER");
-    env = (v && v[0] == '1') ? 1 : 2;
+    env = (v && (v[0] == '1' || v[0] == '2' || v[0] == '4')) ? (v[0] - '0') : 0;
   }
-  if (env == 1 || m_tiles < 2) return 1;
-  if ((epi == EPI_LSE || epi == EPI_DZ || epi == EPI_LSE_Z) && (m_tiles % 2) != 0) return 1;
-  return 2;
+  const bool loss_epi = (epi == EPI_LSE || epi == EPI_DZ || epi == EPI_LSE_Z);
+  // measured on the gpt-oss shape: quads help the two gradient products (MN-major
+  // operands, fp32 output), pairs suit the loss epilogues
+  int c = env ? env : (loss_epi ? 2 : 4);
+  while (c > 1 && (m_tiles < c || (loss_epi && (m_tiles % c) != 0))) c >>= 1;
+  return c;
 }
 
 // Number of K splits for a product of `tiles` output tiles with `k_blocks` steps of
@@ -242,6 +245,70 @@ size_t kd_fused_kl_workspace(int64_t N, int64_t d, int64_t V, int K, int64_t chu
   return kl_layout(N, d, V, K, chunk).total;
 }
 
+static size_t teacher_topk_ws(int64_t N, int64_t V, int64_t chunk) {
+  const int64_t c = chunk < N ? chunk : N;
+  const int64_t rows_pad = (c + BM - 1) / BM * BM;
+  const int64_t ldz = (V + 7) / 8 * 8;
+  return sizeof(Ctrl) + align_up(size_t(rows_pad) * size_t(ldz) * 2, 256);
+}
+
+size_t kd_teacher_topk_workspace(int64_t N, int64_t dt, int64_t V, int K, int64_t chunk) {
+  if (N < 1 || dt < 1 || V < 1 || K < 1 || chunk < 1) return 0;
+  return teacher_topk_ws(N, V, chunk);
+}
+
+int kd_teacher_topk(const void* Ht_bf16, const void* Wt_bf16, int64_t N, int64_t dt, int64_t V, int K,
+                    int64_t chunk, int32_t* ids_out, float* vals_out, float* lse_out, void* ws, size_t ws_bytes,
+                    void* stream) {
+  if (N < 1 || dt < 8 || dt % 8 != 0 || V < 1 || K < 1 || K > KD_MAX_K || int64_t(K) > V) return KD_ERR_INVALID_ARG;
+  if (chunk < BM || chunk % BM != 0 || V > 0x7fffffffLL || N > 0x7fffffffLL || dt > 0x7fffffffLL)
+    return KD_ERR_INVALID_ARG;
+  if (!Ht_bf16 || !Wt_bf16 || !ids_out || !vals_out) return KD_ERR_INVALID_ARG;
+  if (!aligned(Ht_bf16, 16) || !aligned(Wt_bf16, 16) || !aligned(ids_out, 4) || !aligned(vals_out, 4))
+    return KD_ERR_INVALID_ARG;
+  if (lse_out && !aligned(lse_out, 4)) return KD_ERR_INVALID_ARG;
+  if (!ws || !aligned(ws, 256)) return KD_ERR_WORKSPACE;
+  if (ws_bytes < teacher_topk_ws(N, V, chunk)) return KD_ERR_WORKSPACE;
+  kd_status st = check_device();
+  if (st != KD_OK) return st;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* w8 = static_cast<uint8_t*>(ws);
+  Ctrl* ctrl = reinterpret_cast<Ctrl*>(w8);
+  uint16_t* zbuf = reinterpret_cast<uint16_t*>(w8 + sizeof(Ctrl));
+  const int64_t ldz = (V + 7) / 8 * 8;
+  const uint16_t* Ht = static_cast<const uint16_t*>(Ht_bf16);
+  const int grid_max = gemm_max_grid();
+  alignas(64) CUtensorMap tw[3], th;
+  for (int i = 0; i < 3; ++i)
+    if (!make_tmap_2d_bf16(&tw[i], Wt_bf16, uint64_t(dt), uint64_t(V), uint64_t(dt) * 2, BK, BN >> i))
+      return KD_ERR_CUDA;
+  for (int64_t c0 = 0; c0 < N; c0 += chunk) {
+    const int n = int((N - c0) < chunk ? (N - c0) : chunk);
+    // the chunk's teacher logits, fp32 on the tensor cores, rounded once to bf16
+    if (!make_tmap_2d_bf16(&th, Ht + c0 * dt, uint64_t(dt), uint64_t(n), uint64_t(dt) * 2, BK, BM))
+      return KD_ERR_CUDA;
+    GemmProblem p{};
+    p.M = n; p.N = int(V); p.K = int(dt);
+    p.a_mn = 0; p.b_mn = 0; p.epi = EPI_STORE;
+    p.m_tiles = (n + BM - 1) / BM;
+    p.n_tiles = int((V + BN - 1) / BN);
+    p.n_group = 1;
+    p.k_splits = 1;
+    p.cluster = pick_cluster(p.epi, p.m_tiles);
+    p.n_units = ((p.m_tiles + p.cluster - 1) / p.cluster) * p.n_tiles;
+    p.C = zbuf; p.ldc = ldz; p.c_bf16 = 1; p.err = &ctrl->err;
+    const int ci = p.cluster == 4 ? 2 : (p.cluster == 2 ? 1 : 0);
+    cudaError_t e = launch_gemm(p, th, tw[ci], tw[0], grid_max, s);
+    if (e != cudaSuccess) return KD_ERR_CUDA;
+    // exact top-K (and row logsumexp) of those bf16 logits
+    e = launch_topk(zbuf, n, V, ldz, K, ids_out + c0 * K, vals_out + c0 * K, lse_out ? lse_out + c0 : nullptr,
+                    &ctrl->err, s);
+    if (e != cudaSuccess) return KD_ERR_CUDA;
+  }
+  return KD_OK;
+}
+
 size_t kd_chunked_kl_logits_bytes(int64_t N, int64_t V) {
   if (N < 1 || V < 1) return 0;
   return size_t((V + 63) / 64) * size_t(N) * 128;
@@ -279,6 +346,9 @@ static int fwd_impl(const void* H_bf16, const void* W_bf16, const int32_t* t_ids
   if (!make_tmap_2d_bf16(&tw, W_bf16, uint64_t(d), uint64_t(V), uint64_t(d) * 2, BK, BN)) return KD_ERR_CUDA;
   if (!make_tmap_2d_bf16(&tw_half, W_bf16, uint64_t(d), uint64_t(V), uint64_t(d) * 2, BK, BN / 2))
     return KD_ERR_CUDA;
+  alignas(64) CUtensorMap tw_quarter;
+  if (!make_tmap_2d_bf16(&tw_quarter, W_bf16, uint64_t(d), uint64_t(V), uint64_t(d) * 2, BK, BN / 4))
+    return KD_ERR_CUDA;
   if (z_store) {
     (void)z_bytes;
     if (!make_tmap_dz_blocked(&tz, z_store, uint64_t(N), uint64_t(N), uint64_t((V + 63) / 64), 32))
@@ -306,7 +376,8 @@ static int fwd_impl(const void* H_bf16, const void* W_bf16, const int32_t* t_ids
     p.k_splits = 1;
     p.ids_sorted = ids_sorted; p.p_sorted = p_sorted; p.Kt = K; p.inv_tau = inv_tau;
     p.partials = partials; p.rows = n; p.err = &ctrl->err;
-    e = launch_gemm(p, th, p.cluster > 1 ? tw_half : tw, z_store ? tz : tw, grid_max, s);
+    e = launch_gemm(p, th, p.cluster == 4 ? tw_quarter : (p.cluster == 2 ? tw_half : tw), z_store ? tz : tw, grid_max,
+                    s);
     if (e != cudaSuccess) return KD_ERR_CUDA;
     e = launch_lse_combine(partials, L.n_groups, n, negent, inv_tau, lse_out + c0, kl + c0, s);
     if (e != cudaSuccess) return KD_ERR_CUDA;
@@ -344,6 +415,9 @@ static int bwd_impl(const void* H_bf16, const void* W_bf16, const int32_t* t_ids
   alignas(64) CUtensorMap tw_k, tw_k_half, tw_mn, th_k, th_mn, tdz_k, tdz_mn, tdz_st, tgw;
   if (!make_tmap_2d_bf16(&tw_k, W_bf16, uint64_t(d), uint64_t(V), uint64_t(d) * 2, BK, BN)) return KD_ERR_CUDA;
   if (!make_tmap_2d_bf16(&tw_k_half, W_bf16, uint64_t(d), uint64_t(V), uint64_t(d) * 2, BK, BN / 2))
+    return KD_ERR_CUDA;
+  alignas(64) CUtensorMap tw_k_quarter;
+  if (!make_tmap_2d_bf16(&tw_k_quarter, W_bf16, uint64_t(d), uint64_t(V), uint64_t(d) * 2, BK, BN / 4))
     return KD_ERR_CUDA;
   if (!make_tmap_2d_f32(&tgw, grad_W, uint64_t(d), uint64_t(V), uint64_t(d) * 4, 32, 32)) return KD_ERR_CUDA;
   if (!make_tmap_2d_bf16(&tw_mn, W_bf16, uint64_t(d), uint64_t(V), uint64_t(d) * 2, 64, BK)) return KD_ERR_CUDA;
@@ -384,7 +458,8 @@ static int bwd_impl(const void* H_bf16, const void* W_bf16, const int32_t* t_ids
     p.ids_sorted = ids_sorted; p.p_sorted = p_sorted; p.Kt = K; p.inv_tau = inv_tau;
     p.lse = lse + c0; p.mask = mask ? mask + c0 : nullptr; p.grad_loss = grad_loss; p.n_valid = &ctrl->n_valid;
     p.dz = dz; p.ldz = L.ldz; p.rows = n; p.err = &ctrl->err;
-    e = launch_gemm(p, th_k, p.cluster > 1 ? tw_k_half : tw_k, tdz_st, grid_max, s);
+    e = launch_gemm(p, th_k, p.cluster == 4 ? tw_k_quarter : (p.cluster == 2 ? tw_k_half : tw_k), tdz_st, grid_max,
+                    s);
     if (e != cudaSuccess) return KD_ERR_CUDA;
     }
 

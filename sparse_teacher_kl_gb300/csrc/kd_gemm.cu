@@ -153,13 +153,15 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             }
             if (p.cluster > 1) {
               // this CTA's half of B, multicast to both CTAs of the pair
+              // this CTA's 1/cluster share of B, multicast to every CTA of the cluster
               if (p.b_mn == 0) {
-                tma_load_2d_mc(sb + crank * (STAGE_B_BYTES / 2), &tmap_b, &tail->full[s], kb * BK,
-                               nb * BN + int(crank) * (BN / 2), cmask);
+                const int rows = BN / p.cluster;
+                tma_load_2d_mc(sb + crank * (STAGE_B_BYTES / p.cluster), &tmap_b, &tail->full[s], kb * BK,
+                               nb * BN + int(crank) * rows, cmask);
               } else {
-#pragma unroll
-                for (int j = 0; j < BN / 128; ++j) {
-                  const int jj = int(crank) * (BN / 128) + j;
+                const int per = (BN / 64) / p.cluster;  // 64-column boxes per CTA
+                for (int j = 0; j < per; ++j) {
+                  const int jj = int(crank) * per + j;
                   tma_load_2d_mc(sb + jj * 8192, &tmap_b, &tail->full[s], nb * BN + jj * 64, kb * BK, cmask);
                 }
               }
@@ -436,7 +438,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     reinterpret_cast<uint16_t*>(p.C) + size_t(split) * p.split_stride + size_t(row) * p.ldc + col0;
 #pragma unroll
                 for (int g8 = 0; g8 < 4; ++g8) {
-                  if (col0 + g8 * 8 + 8 <= p.N) {
+                  // whole 8-column groups that start inside the matrix; the row stride ldc is
+                  // a multiple of 8, so a group ending past column N stays inside its row
+                  if (col0 + g8 * 8 < p.N && col0 + g8 * 8 + 8 <= p.ldc) {
                     uint4 v;
                     v.x = pack_bf16x2(x[g8 * 8 + 0], x[g8 * 8 + 1]);
                     v.y = pack_bf16x2(x[g8 * 8 + 2], x[g8 * 8 + 3]);
@@ -450,7 +454,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     reinterpret_cast<float*>(p.C) + size_t(split) * p.split_stride + size_t(row) * p.ldc + col0;
 #pragma unroll
                 for (int g4 = 0; g4 < 8; ++g4) {
-                  if (col0 + g4 * 4 + 4 <= p.N) {
+                  if (col0 + g4 * 4 < p.N && col0 + g4 * 4 + 4 <= p.ldc) {
                     *reinterpret_cast<float4*>(dst + g4 * 4) =
                         make_float4(x[g4 * 4 + 0], x[g4 * 4 + 1], x[g4 * 4 + 2], x[g4 * 4 + 3]);
                   }
@@ -550,7 +554,7 @@ static const char* gemm_name(int epi, int a_mn, int b_mn) {
 cudaError_t launch_gemm(const GemmProblem& p, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
                         int grid, cudaStream_t s) {
   if (p.n_units <= 0) return cudaSuccess;
-  if (p.cluster < 1 || p.cluster > 2) return cudaErrorInvalidValue;
+  if (p.cluster != 1 && p.cluster != 2 && p.cluster != 4) return cudaErrorInvalidValue;
   if (p.cluster == 1 && grid > p.n_units) grid = p.n_units;
   prof_before(gemm_name(p.epi, p.a_mn, p.b_mn), s);
   cudaError_t e;

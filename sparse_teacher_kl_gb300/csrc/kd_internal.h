@@ -68,9 +68,10 @@ struct GemmProblem {
   // of it is one contiguous run of memory.
   int a_blocked;
   int z_row0;                 // EPI_LSE_Z: row of the stored logits that chunk row 0 maps to
-  // cluster = 2: CTA pairs take m tiles (2j, 2j+1) of the same n tile and share the B
-  // operand: each loads one half of it (K-major B map box 64 x 128) multicast to both.
-  // n_units then counts pairs.  cluster = 1: every CTA loads its own operands.
+  // cluster = 2 or 4: the CTAs of a cluster take consecutive m tiles of the same n tile
+  // and share the B operand: each loads 1/cluster of it (K-major B map box 64 x 256/cluster)
+  // multicast to all of them.  n_units then counts clusters' units.  cluster = 1: every
+  // CTA loads its own operands.
   int cluster;
   // EPI_STORE / EPI_ACCUM
   void* C;

@@ -118,3 +118,42 @@ def test_topk_dropped_mass(kd, cuda_device):
         ref = oracle.dropped_mass(bf16_bits(X), K)
         assert np.max(np.abs(got - ref)) <= 1e-5
     assert np.all(ref >= -1e-12)
+
+
+def test_teacher_topk_exact_integer_logits(kd, cuda_device):
+    """Small-integer teacher hidden states and weights make every logit an exact bf16 integer, so the
+    fused projection + top-K must match the oracle's cache of the exact logits bit for bit (with
+    many ties, broken by the lower id)."""
+    g = torch.Generator().manual_seed(21)
+    N, dt, V, K = 300, 64, 5000, 37
+    Ht = torch.randint(-2, 3, (N, dt), generator=g).to(torch.bfloat16)
+    Wt = torch.randint(-2, 3, (V, dt), generator=g).to(torch.bfloat16)
+    ids, vals, lse = kd.teacher_topk(Ht.to(cuda_device), Wt.to(cuda_device), K, chunk=128, with_lse=True)
+    torch.cuda.synchronize()
+    zbits = oracle.teacher_logits_bf16(bf16_bits(Ht), bf16_bits(Wt))
+    rid, rval = oracle.topk_cache(zbits, K)
+    assert np.array_equal(ids.cpu().numpy(), rid)
+    assert np.array_equal(vals.cpu().numpy().view(np.uint32), rval.view(np.uint32))
+    ref_lse = oracle.teacher_logsumexp(zbits)
+    assert np.max(np.abs(lse.cpu().numpy() - ref_lse)) <= 1e-5 * np.max(np.abs(ref_lse))
+
+
+def test_teacher_topk_random_is_a_valid_topk(kd, cuda_device):
+    """Random teacher inputs: the kept values are the logits rounded to bf16 (within one bf16 step of the
+    float64 product) and no logit left out exceeds the smallest kept one by more than that rounding."""
+    g = torch.Generator().manual_seed(22)
+    N, dt, V, K = 260, 200, 3001, 50
+    Ht = torch.randn((N, dt), generator=g).to(torch.bfloat16)
+    Wt = (torch.randn((V, dt), generator=g) / 14).to(torch.bfloat16)
+    ids, vals = kd.teacher_topk(Ht.to(cuda_device), Wt.to(cuda_device), K, chunk=128)
+    torch.cuda.synchronize()
+    z = oracle.bf16_to_f64(bf16_bits(Ht)) @ oracle.bf16_to_f64(bf16_bits(Wt)).T
+    ids, vals = ids.cpu().numpy(), vals.cpu().numpy().astype(np.float64)
+    for r in range(N):
+        sel = ids[r]
+        assert len(set(sel.tolist())) == K and np.all(np.diff(vals[r]) <= 0)
+        ulp = 2.0 ** (np.floor(np.log2(np.maximum(np.abs(z[r, sel]), 1e-30))) - 7)
+        assert np.all(np.abs(vals[r] - z[r, sel]) <= ulp)
+        rest = np.ones(V, bool)
+        rest[sel] = False
+        assert z[r, rest].max() <= vals[r].min() + 2 * ulp.max()

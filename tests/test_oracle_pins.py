@@ -255,3 +255,15 @@ def test_teacher_logsumexp_and_dropped_mass():
     b = _bf16_bits_of(np.array([[0.0, np.log(3.0)]]))
     v = oracle.bf16_to_f64(b)[0]
     assert abs(oracle.dropped_mass(b, 1)[0] - np.exp(v[0]) / (np.exp(v[0]) + np.exp(v[1]))) <= 1e-15
+
+
+# The teacher-logit rounding of the fused cache builder is torch's own fp32 -> bf16
+# conversion (round to nearest even) applied to the product.
+def test_teacher_logits_bf16_rounding():
+    rng = np.random.default_rng(12)
+    Ht = _bf16_bits_of(rng.standard_normal((9, 24)))
+    Wt = _bf16_bits_of(rng.standard_normal((40, 24)))
+    got = oracle.teacher_logits_bf16(Ht, Wt)
+    z = oracle.bf16_to_f64(Ht) @ oracle.bf16_to_f64(Wt).T
+    ref = torch.tensor(z, dtype=torch.float32).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(got, ref)
