@@ -251,6 +251,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-modes", action="store_true", help="skip the forward-chunked and dense comparisons")
     ap.add_argument("--no-topk", action="store_true", help="skip the top-K cache measurement")
+    ap.add_argument("--topk-only", action="store_true", help="only the top-K cache measurement (profiling)")
     ap.add_argument("--rows", type=int, default=None, help="override B*T (profiling a reduced case)")
     ap.add_argument("--vocab", type=int, default=None, help="override V (profiling a reduced case)")
     args = ap.parse_args()
@@ -281,6 +282,9 @@ def main():
     from synth import make_inputs
 
     peaks = load_peaks()
+    if args.topk_only:
+        print(json.dumps({"topk_cache": bench_topk(kd, dev, torch.cuda.current_stream(dev), peaks, args.steps)}))
+        return 0
     H, W, ids, tlog, mask = make_inputs(w, dev)
     N, d, V, K, c = w.N, w.d, w.V, w.K, w.chunk
     ws = kd.workspace(kd._abi.kd_fused_kl_workspace(N, d, V, K, c), dev)

@@ -160,6 +160,27 @@ static int pick_cluster(int epi, int m_tiles) {
   return c;
 }
 
+// CTA-pair tensor-core mode (GemmProblem::cta_pair), used for every launch with at
+// least two row tiles (measured on the gpt-oss shape: 342k vs 295k tokens/s for the
+// single-CTA tiles with shared B).  KD_GEMM_PAIR=0 turns it off (for measurements).
+static bool pair_mode() {
+  static int env = -1;
+  if (env < 0) {
+    const char* v = getenv("KD_GEMM_PAIR");
+    env = (v && v[0] == '0') ? 0 : 1;
+  }
+  return env == 1;
+}
+
+static void set_cluster(GemmProblem& p) {
+  p.cluster = pick_cluster(p.epi, p.m_tiles);
+  p.cta_pair = 0;
+  if (p.cluster >= 2 && pair_mode()) {
+    p.cluster = 2;
+    p.cta_pair = 1;
+  }
+}
+
 // Number of K splits for a product of `tiles` output tiles with `k_blocks` steps of
 // BK each: the fewest waves of `grid` persistent CTAs per unit of work, with a small
 // charge per split for the extra partial traffic.
@@ -295,7 +316,7 @@ int kd_teacher_topk(const void* Ht_bf16, const void* Wt_bf16, int64_t N, int64_t
     p.n_tiles = int((V + BN - 1) / BN);
     p.n_group = 1;
     p.k_splits = 1;
-    p.cluster = pick_cluster(p.epi, p.m_tiles);
+    set_cluster(p);
     p.n_units = ((p.m_tiles + p.cluster - 1) / p.cluster) * p.n_tiles;
     p.C = zbuf; p.ldc = ldz; p.c_bf16 = 1; p.err = &ctrl->err;
     const int ci = p.cluster == 4 ? 2 : (p.cluster == 2 ? 1 : 0);
@@ -371,7 +392,7 @@ static int fwd_impl(const void* H_bf16, const void* W_bf16, const int32_t* t_ids
     p.m_tiles = (n + BM - 1) / BM;
     p.n_tiles = int((V + BN - 1) / BN);
     p.n_group = choose_n_group(V);
-    p.cluster = pick_cluster(p.epi, p.m_tiles);
+    set_cluster(p);
     p.n_units = ((p.m_tiles + p.cluster - 1) / p.cluster) * ((p.n_tiles + p.n_group - 1) / p.n_group);
     p.k_splits = 1;
     p.ids_sorted = ids_sorted; p.p_sorted = p_sorted; p.Kt = K; p.inv_tau = inv_tau;
@@ -452,7 +473,7 @@ static int bwd_impl(const void* H_bf16, const void* W_bf16, const int32_t* t_ids
     p.m_tiles = (n + BM - 1) / BM;
     p.n_tiles = int((V + BN - 1) / BN);
     p.n_group = 1;
-    p.cluster = pick_cluster(p.epi, p.m_tiles);
+    set_cluster(p);
     p.n_units = ((p.m_tiles + p.cluster - 1) / p.cluster) * p.n_tiles;
     p.k_splits = 1;
     p.ids_sorted = ids_sorted; p.p_sorted = p_sorted; p.Kt = K; p.inv_tau = inv_tau;
@@ -472,7 +493,7 @@ static int bwd_impl(const void* H_bf16, const void* W_bf16, const int32_t* t_ids
     q.n_group = 1;
     q.a_blocked = 1;
     q.k_splits = choose_splits(int64_t(q.m_tiles) * q.n_tiles, int((V + BK - 1) / BK), grid_max);
-    q.cluster = pick_cluster(q.epi, q.m_tiles);
+    set_cluster(q);
     q.n_units = ((q.m_tiles + q.cluster - 1) / q.cluster) * q.n_tiles * q.k_splits;
     void* gh_out = static_cast<uint8_t*>(grad_H) + size_t(c0) * d * gh_elt;
     if (q.k_splits == 1) {
@@ -501,7 +522,7 @@ static int bwd_impl(const void* H_bf16, const void* W_bf16, const int32_t* t_ids
     r.n_group = 1;
     r.a_blocked = 1;
     r.k_splits = 1;
-    r.cluster = pick_cluster(r.epi, r.m_tiles);
+    set_cluster(r);
     r.n_units = ((r.m_tiles + r.cluster - 1) / r.cluster) * r.n_tiles;
     r.C = grad_W; r.ldc = d; r.c_bf16 = 0; r.err = &ctrl->err;
     e = launch_gemm(r, tdz_mn, th_mn, tgw, grid_max, s);
@@ -585,21 +606,20 @@ int kd_gemm_bf16(const void* A, const void* B, float* C, int64_t M, int64_t N, i
   alignas(64) CUtensorMap ta, tb, tc;
   bool ok = a_mn ? make_tmap_2d_bf16(&ta, A, uint64_t(M), uint64_t(K), uint64_t(M) * 2, 64, BK)
                  : make_tmap_2d_bf16(&ta, A, uint64_t(K), uint64_t(M), uint64_t(K) * 2, BK, BM);
-  const int m_tiles = int((M + BM - 1) / BM);
-  const int cluster = pick_cluster(accumulate ? EPI_ACCUM : EPI_STORE, m_tiles);
+  GemmProblem p{};
+  p.epi = accumulate ? EPI_ACCUM : EPI_STORE;
+  p.m_tiles = int((M + BM - 1) / BM);
+  set_cluster(p);
+  const int cluster = p.cluster;
   ok = ok && (b_mn ? make_tmap_2d_bf16(&tb, B, uint64_t(N), uint64_t(K), uint64_t(N) * 2, 64, BK)
                    : make_tmap_2d_bf16(&tb, B, uint64_t(K), uint64_t(N), uint64_t(K) * 2, BK, BN / cluster));
   ok = ok && make_tmap_2d_f32(&tc, C, uint64_t(N), uint64_t(M), uint64_t(N) * 4, 32, 32);
   if (!ok) return KD_ERR_CUDA;
-  GemmProblem p{};
   p.M = int(M); p.N = int(N); p.K = int(K);
   p.a_mn = a_mn ? 1 : 0; p.b_mn = b_mn ? 1 : 0;
-  p.epi = accumulate ? EPI_ACCUM : EPI_STORE;
-  p.m_tiles = int((M + BM - 1) / BM);
   p.n_tiles = int((N + BN - 1) / BN);
   p.n_group = 1;
   p.k_splits = 1;
-  p.cluster = cluster;
   p.n_units = ((p.m_tiles + p.cluster - 1) / p.cluster) * p.n_tiles;
   p.C = C; p.ldc = N; p.c_bf16 = 0;
   p.err = &static_cast<Ctrl*>(ws)->err;

@@ -26,9 +26,11 @@
 
 namespace kd {
 
+constexpr int MAX_STAGES = 6;
+
 struct __align__(8) GemmSmemTail {
-  uint64_t full[STAGES];
-  uint64_t empty[STAGES];
+  uint64_t full[MAX_STAGES];
+  uint64_t empty[MAX_STAGES];
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t drain;
@@ -36,9 +38,21 @@ struct __align__(8) GemmSmemTail {
   uint32_t abort_flag;
 };
 
-constexpr size_t GEMM_SMEM_BYTES =
-    1024 /*alignment slack*/ + size_t(STAGES) * STAGE_BYTES + STAGING_BYTES + sizeof(GemmSmemTail);
-static_assert(GEMM_SMEM_BYTES <= 232448, "shared memory budget of one CTA");
+// Shared-memory ring per CTA.  One CTA per tile (CG = 1): a stage holds A 128 x 64 and
+// B 256 x 64 (48 KB), 4 stages.  CTA pair per tile (CG = 2, tcgen05 cta_group::2): each
+// CTA holds its 128 rows of A and its 128 columns of B (32 KB), so 6 stages fit and each
+// SM moves a third less operand data per flop.
+template <int CG>
+struct Geo {
+  static constexpr int kStages = CG == 2 ? 6 : STAGES;
+  static constexpr int kA = STAGE_A_BYTES;
+  static constexpr int kB = CG == 2 ? STAGE_B_BYTES / 2 : STAGE_B_BYTES;
+  static constexpr int kStage = kA + kB;
+  static constexpr size_t kSmem =
+      1024 /*alignment slack*/ + size_t(kStages) * kStage + STAGING_BYTES + sizeof(GemmSmemTail);
+  static_assert(kStages <= MAX_STAGES, "barrier arrays");
+  static_assert(kSmem <= 232448, "shared memory budget of one CTA");
+};
 
 // Unit u -> tile coordinates.  LSE/DZ walk the vocabulary (n) slowly so that
 // every CTA in flight reads the same few W tiles while the small H chunk stays
@@ -70,14 +84,15 @@ __device__ __forceinline__ void unit_coords(const GemmProblem& p, int u, uint32_
   }
 }
 
-template <int EPI>
+template <int EPI, int CG>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     kd_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                    const __grid_constant__ CUtensorMap tmap_c, const GemmProblem p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  using G = Geo<CG>;
   uint8_t* stage_base = smem;
-  uint8_t* staging = smem + size_t(STAGES) * STAGE_BYTES;  // 1024-aligned output boxes of the epilogue warps
+  uint8_t* staging = smem + size_t(G::kStages) * G::kStage;  // 1024-aligned output boxes of the epilogue warps
   GemmSmemTail* tail = reinterpret_cast<GemmSmemTail*>(staging + STAGING_BYTES);
   volatile uint32_t* abort_flag = &tail->abort_flag;
 
@@ -89,13 +104,16 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   const int u_step = int(gridDim.x) / p.cluster;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
+    for (int s = 0; s < G::kStages; ++s) {
       mbar_init(&tail->full[s], 1);
-      mbar_init(&tail->empty[s], uint32_t(p.cluster));  // every CTA whose data lands in this stage
+      // released by every CTA whose data lands in this stage (B multicast), or once by
+      // the pair's single MMA thread
+      mbar_init(&tail->empty[s], CG == 2 ? 1u : uint32_t(p.cluster));
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tail->tfull[a], 1);
-      mbar_init(&tail->tempty[a], 128);
+      // the pair's MMA thread waits for both CTAs' epilogues
+      mbar_init(&tail->tempty[a], (CG == 2 && crank == 0) ? 256u : 128u);
     }
     mbar_init(&tail->drain, 1);
     tail->abort_flag = 0;
@@ -107,7 +125,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     if (EPI == EPI_DZ || EPI == EPI_LSE_Z) tma_prefetch_map(&tmap_c);
   }
   if (warp == 1) {
-    tmem_alloc(&tail->tmem_base, TMEM_COLS);
+    if (CG == 2) tmem_alloc_pair(&tail->tmem_base, TMEM_COLS); else tmem_alloc(&tail->tmem_base, TMEM_COLS);
   }
   tc_fence_before();
   __syncthreads();
@@ -125,15 +143,45 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         unit_coords(p, u, crank, m_blk, n_first, n_count, kb_lo, kb_hi, split);
         for (int nb = n_first; nb < n_first + n_count && ok; ++nb) {
           for (int kb = kb_lo; kb < kb_hi; ++kb, ++it) {
-            const uint32_t s = it % STAGES;
-            const uint32_t ph = (it / STAGES) & 1u;
+            const uint32_t s = it % G::kStages;
+            const uint32_t ph = (it / G::kStages) & 1u;
             if (!mbar_wait(&tail->empty[s], ph ^ 1u, abort_flag, p.err, 0x100u)) {
               ok = false;
               break;
             }
-            uint8_t* sa = stage_base + size_t(s) * STAGE_BYTES;
-            uint8_t* sb = sa + STAGE_A_BYTES;
-            mbar_arrive_expect_tx(&tail->full[s], STAGE_BYTES);
+            uint8_t* sa = stage_base + size_t(s) * G::kStage;
+            uint8_t* sb = sa + G::kA;
+            if (CG == 2) {
+              // both CTAs' halves complete on the first CTA's barrier, where the MMA waits
+              const uint32_t bar0 = mapa_u32(&tail->full[s], 0);
+              if (crank == 0) mbar_arrive_expect_tx(&tail->full[s], 2 * G::kStage);
+              if (p.a_blocked) {
+                if (p.a_mn == 0) {
+                  tma_load_3d_pair(sa, &tmap_a, bar0, 0, m_blk * BM, kb);
+                } else {
+#pragma unroll
+                  for (int j = 0; j < BM / 64; ++j)
+                    tma_load_3d_pair(sa + j * 8192, &tmap_a, bar0, 0, kb * BK, m_blk * (BM / 64) + j);
+                }
+              } else if (p.a_mn == 0) {
+                tma_load_2d_pair(sa, &tmap_a, bar0, kb * BK, m_blk * BM);
+              } else {
+#pragma unroll
+                for (int j = 0; j < BM / 64; ++j)
+                  tma_load_2d_pair(sa + j * 8192, &tmap_a, bar0, m_blk * BM + j * 64, kb * BK);
+              }
+              // this CTA's 128 columns of the pair's 256-column B tile
+              if (p.b_mn == 0) {
+                tma_load_2d_pair(sb, &tmap_b, bar0, kb * BK, nb * BN + int(crank) * (BN / 2));
+              } else {
+#pragma unroll
+                for (int j = 0; j < BN / 128; ++j)
+                  tma_load_2d_pair(sb + j * 8192, &tmap_b, bar0, nb * BN + (int(crank) * (BN / 128) + j) * 64,
+                                   kb * BK);
+              }
+              continue;
+            }
+            mbar_arrive_expect_tx(&tail->full[s], G::kStage);
             if (p.a_blocked) {
               // blocked dZ [vocab/64][row][64]: K-major A walks vocabulary blocks; MN-major
               // A takes the two 64-wide vocabulary blocks of its 128 rows
@@ -156,7 +204,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
               // this CTA's 1/cluster share of B, multicast to every CTA of the cluster
               if (p.b_mn == 0) {
                 const int rows = BN / p.cluster;
-                tma_load_2d_mc(sb + crank * (STAGE_B_BYTES / p.cluster), &tmap_b, &tail->full[s], kb * BK,
+                tma_load_2d_mc(sb + crank * (G::kB / p.cluster), &tmap_b, &tail->full[s], kb * BK,
                                nb * BN + int(crank) * rows, cmask);
               } else {
                 const int per = (BN / 64) / p.cluster;  // 64-column boxes per CTA
@@ -175,19 +223,20 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           }
         }
       }
-      if (!ok) {
-        // Let the copies already issued land before the CTA can exit.
-        const uint32_t first = it > STAGES ? it - STAGES : 0;
+      if (!ok && (CG == 1 || crank == 0)) {
+        // Let the copies already issued land before the CTA can exit (for a pair, all of
+        // them complete on the first CTA's barriers).
+        const uint32_t first = it > uint32_t(G::kStages) ? it - G::kStages : 0;
         for (uint32_t j = first; j < it; ++j) {
           volatile uint32_t never = 0;
-          mbar_wait(&tail->full[j % STAGES], (j / STAGES) & 1u, &never, nullptr, 0);
+          mbar_wait(&tail->full[j % G::kStages], (j / G::kStages) & 1u, &never, nullptr, 0);
         }
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      const uint32_t idesc = idesc_bf16_f32(BM, BN, p.a_mn, p.b_mn);
+    if (lane == 0 && (CG == 1 || crank == 0)) {  // a pair's MMAs are issued by its first CTA
+      const uint32_t idesc = idesc_bf16_f32(BM * CG, BN, p.a_mn, p.b_mn);
       const uint32_t a_step = p.a_mn ? 16u * 128u : 32u;
       const uint32_t b_step = p.b_mn ? 16u * 128u : 32u;
       const uint32_t a_lbo = p.a_mn ? 8192u : 16u;
@@ -207,28 +256,33 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + a * BN;
           for (int kb = kb_lo; kb < kb_hi; ++kb, ++it) {
-            const uint32_t s = it % STAGES;
-            const uint32_t ph = (it / STAGES) & 1u;
+            const uint32_t s = it % G::kStages;
+            const uint32_t ph = (it / G::kStages) & 1u;
             if (!mbar_wait(&tail->full[s], ph, abort_flag, p.err, 0x300u)) {
               ok = false;
               break;
             }
             tc_fence_after();
-            const uint32_t sa = smem_u32(stage_base + size_t(s) * STAGE_BYTES);
-            const uint32_t sb = sa + STAGE_A_BYTES;
+            const uint32_t sa = smem_u32(stage_base + size_t(s) * G::kStage);
+            const uint32_t sb = sa + G::kA;
 #pragma unroll
             for (int k = 0; k < BK / 16; ++k) {
               const uint64_t ad = sdesc_sw128(sa + k * a_step, a_lbo);
               const uint64_t bd = sdesc_sw128(sb + k * b_step, b_lbo);
-              umma_bf16(d_tmem, ad, bd, idesc, (kb != kb_lo || k != 0) ? 1u : 0u);
+              if (CG == 2) umma_bf16_pair(d_tmem, ad, bd, idesc, (kb != kb_lo || k != 0) ? 1u : 0u);
+              else umma_bf16(d_tmem, ad, bd, idesc, (kb != kb_lo || k != 0) ? 1u : 0u);
             }
-            if (p.cluster > 1) umma_commit_mc(&tail->empty[s], cmask); else umma_commit(&tail->empty[s]);
+            if (CG == 2) umma_commit_pair_mc(&tail->empty[s], 0x3);
+            else if (p.cluster > 1) umma_commit_mc(&tail->empty[s], cmask);
+            else umma_commit(&tail->empty[s]);
           }
-          if (ok) umma_commit(&tail->tfull[a]);
+          if (ok) {
+            if (CG == 2) umma_commit_pair_mc(&tail->tfull[a], 0x3); else umma_commit(&tail->tfull[a]);
+          }
         }
       }
       // Drain: every MMA issued above has completed once this arrives.
-      umma_commit(&tail->drain);
+      if (CG == 2) umma_commit_pair_mc(&tail->drain, 0x1); else umma_commit(&tail->drain);
       volatile uint32_t never = 0;
       mbar_wait(&tail->drain, 0, &never, p.err, 0x400u);
     }
@@ -464,7 +518,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
           }
         }
         tc_fence_before();
-        mbar_arrive(&tail->tempty[a]);
+        if (CG == 2 && crank != 0) mbar_arrive_remote(mapa_u32(&tail->tempty[a], 0));
+        else mbar_arrive(&tail->tempty[a]);
       }
       if ((EPI == EPI_LSE || EPI == EPI_LSE_Z) && ok && row < p.rows) {
         const int g = n_first / p.n_group;
@@ -480,7 +535,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   if (p.cluster > 1) cluster_sync();  // no multicast or remote arrival can still target this CTA
   tc_fence_after();
   if (warp == 1) {
-    tmem_dealloc(tmem_base, TMEM_COLS);
+    if (CG == 2) tmem_dealloc_pair(tmem_base, TMEM_COLS); else tmem_dealloc(tmem_base, TMEM_COLS);
   }
 }
 
@@ -496,21 +551,21 @@ int gemm_max_grid() {
   return g_num_sms;
 }
 
-template <int EPI>
+template <int EPI, int CG>
 static cudaError_t launch_one(const GemmProblem& p, const CUtensorMap& ta, const CUtensorMap& tb,
                               const CUtensorMap& tc, int grid, cudaStream_t s) {
   static bool attr_set = false;
   static int max_pairs = 0;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kd_gemm_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         int(GEMM_SMEM_BYTES));
+    cudaError_t e = cudaFuncSetAttribute(kd_gemm_kernel<EPI, CG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         int(Geo<CG>::kSmem));
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   cfg.blockDim = dim3(GEMM_THREADS, 1, 1);
-  cfg.dynamicSmemBytes = GEMM_SMEM_BYTES;
+  cfg.dynamicSmemBytes = Geo<CG>::kSmem;
   cfg.stream = s;
   if (p.cluster > 1) {
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -523,7 +578,7 @@ static cudaError_t launch_one(const GemmProblem& p, const CUtensorMap& ta, const
       // persistent grid: as many pairs as can be resident at once
       cfg.gridDim = dim3(unsigned((gemm_max_grid() / p.cluster) * p.cluster), 1, 1);
       int n = 0;
-      if (cudaOccupancyMaxActiveClusters(&n, kd_gemm_kernel<EPI>, &cfg) != cudaSuccess || n < 1) n = 1;
+      if (cudaOccupancyMaxActiveClusters(&n, kd_gemm_kernel<EPI, CG>, &cfg) != cudaSuccess || n < 1) n = 1;
       max_pairs = n;
     }
     int pairs = grid / p.cluster;
@@ -536,7 +591,7 @@ static cudaError_t launch_one(const GemmProblem& p, const CUtensorMap& ta, const
     cfg.attrs = nullptr;
     cfg.numAttrs = 0;
   }
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kd_gemm_kernel<EPI>, ta, tb, tc, p);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kd_gemm_kernel<EPI, CG>, ta, tb, tc, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -558,12 +613,23 @@ cudaError_t launch_gemm(const GemmProblem& p, const CUtensorMap& ta, const CUten
   if (p.cluster == 1 && grid > p.n_units) grid = p.n_units;
   prof_before(gemm_name(p.epi, p.a_mn, p.b_mn), s);
   cudaError_t e;
-  switch (p.epi) {
-    case EPI_LSE: e = launch_one<EPI_LSE>(p, ta, tb, tc, grid, s); break;
-    case EPI_LSE_Z: e = launch_one<EPI_LSE_Z>(p, ta, tb, tc, grid, s); break;
-    case EPI_DZ: e = launch_one<EPI_DZ>(p, ta, tb, tc, grid, s); break;
-    case EPI_STORE: e = launch_one<EPI_STORE>(p, ta, tb, tc, grid, s); break;
-    default: e = launch_one<EPI_ACCUM>(p, ta, tb, tc, grid, s); break;
+  if (p.cta_pair) {
+    if (p.cluster != 2) return cudaErrorInvalidValue;
+    switch (p.epi) {
+      case EPI_LSE: e = launch_one<EPI_LSE, 2>(p, ta, tb, tc, grid, s); break;
+      case EPI_LSE_Z: e = launch_one<EPI_LSE_Z, 2>(p, ta, tb, tc, grid, s); break;
+      case EPI_DZ: e = launch_one<EPI_DZ, 2>(p, ta, tb, tc, grid, s); break;
+      case EPI_STORE: e = launch_one<EPI_STORE, 2>(p, ta, tb, tc, grid, s); break;
+      default: e = launch_one<EPI_ACCUM, 2>(p, ta, tb, tc, grid, s); break;
+    }
+  } else {
+    switch (p.epi) {
+      case EPI_LSE: e = launch_one<EPI_LSE, 1>(p, ta, tb, tc, grid, s); break;
+      case EPI_LSE_Z: e = launch_one<EPI_LSE_Z, 1>(p, ta, tb, tc, grid, s); break;
+      case EPI_DZ: e = launch_one<EPI_DZ, 1>(p, ta, tb, tc, grid, s); break;
+      case EPI_STORE: e = launch_one<EPI_STORE, 1>(p, ta, tb, tc, grid, s); break;
+      default: e = launch_one<EPI_ACCUM, 1>(p, ta, tb, tc, grid, s); break;
+    }
   }
   prof_after(s);
   return e;

@@ -73,6 +73,9 @@ struct GemmProblem {
   // multicast to all of them.  n_units then counts clusters' units.  cluster = 1: every
   // CTA loads its own operands.
   int cluster;
+  // cta_pair = 1 (requires cluster = 2): each pair computes one 256 x 256 tile with
+  // tcgen05 cta_group::2 MMAs (A split by rows, B by columns between the two CTAs).
+  int cta_pair;
   // EPI_STORE / EPI_ACCUM
   void* C;
   int64_t ldc;

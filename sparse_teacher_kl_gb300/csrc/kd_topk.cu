@@ -28,9 +28,13 @@ namespace kd {
 constexpr int TK_THREADS = 512;
 constexpr int TK_VEC = 8;                      // bf16 per 16-byte load
 constexpr int TK_SEG = TK_THREADS * TK_VEC;    // elements per segment
-constexpr int TK_CAP = 2 * TK_SEG;             // candidate buffer entries
+constexpr int TK_CHECK = 1;                    // segments between two looks at the buffer fill
+constexpr int TK_CAP = 2 * TK_SEG;             // candidate buffer entries (a power of two: sort_desc)
 constexpr int TK_PIPE = 4;                     // segments in flight per thread
-constexpr int TK_HOLD = TK_CAP / TK_THREADS;   // buffer entries per thread
+constexpr int TK_ROUND = 8;                    // entries per thread per compaction round
+
+static_assert((TK_CAP & (TK_CAP - 1)) == 0, "the bitonic sort pads the buffer to a power of two");
+static_assert(TK_CAP >= (TK_CHECK + 1) * TK_SEG, "room for one check window after a compaction");
 
 struct TopkSmem {
   unsigned long long buf[TK_CAP];
@@ -124,23 +128,27 @@ __device__ __forceinline__ void warp_append(TopkSmem& sm, bool take, unsigned lo
   if (take) sm.buf[base + __popc(ballot & ((1u << lane) - 1u))] = c;
 }
 
-// Keep only the entries with key >= T (in place).
+// Keep only the entries with key >= T, in place: rounds of TK_ROUND entries per
+// thread are read into registers before any survivor of that round is written, and
+// survivors never outnumber the entries read so far, so no unread entry is overwritten.
 __device__ void filter_ge(TopkSmem& sm, uint32_t count, uint32_t T) {
-  unsigned long long held[TK_HOLD];
-#pragma unroll
-  for (int j = 0; j < TK_HOLD; ++j) {
-    const uint32_t i = threadIdx.x + j * TK_THREADS;
-    held[j] = (i < count) ? sm.buf[i] : 0ull;
-  }
   __syncthreads();
   if (threadIdx.x == 0) sm.count = 0;
-  __syncthreads();
+  for (uint32_t base = 0; base < count; base += TK_ROUND * TK_THREADS) {
+    unsigned long long held[TK_ROUND];
 #pragma unroll
-  for (int j = 0; j < TK_HOLD; ++j) {
-    const uint32_t i = threadIdx.x + j * TK_THREADS;
-    warp_append(sm, i < count && comp_key(held[j]) >= T, held[j]);
+    for (int j = 0; j < TK_ROUND; ++j) {
+      const uint32_t i = base + threadIdx.x + j * TK_THREADS;
+      held[j] = (i < count) ? sm.buf[i] : 0ull;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < TK_ROUND; ++j) {
+      const uint32_t i = base + threadIdx.x + j * TK_THREADS;
+      warp_append(sm, i < count && comp_key(held[j]) >= T, held[j]);
+    }
+    __syncthreads();
   }
-  __syncthreads();
 }
 
 // Sort buf[0, count) descending (bitonic over the next power of two, padded
@@ -168,13 +176,13 @@ __device__ void sort_desc(TopkSmem& sm, uint32_t count) {
   }
 }
 
-// Bring the buffer back to at most TK_CAP - TK_SEG entries, all of them able
+// Bring the buffer back to at most TK_CAP - TK_CHECK * TK_SEG entries, all of them able
 // to reach the top K; returns the new acceptance threshold (key must exceed it).
 __device__ int compact(TopkSmem& sm, uint32_t K) {
   const uint32_t count = sm.count;
   uint32_t count_ge = 0;
   const uint32_t T = kth_largest_key(sm, count, K, count_ge);
-  if (count_ge <= uint32_t(TK_CAP - TK_SEG)) {
+  if (count_ge <= uint32_t(TK_CAP - TK_CHECK * TK_SEG)) {
     if (count_ge < count) filter_ge(sm, count, T);
     return int(T);
   }
@@ -214,22 +222,101 @@ __global__ void __launch_bounds__(TK_THREADS, 2)
       if (j < nseg) pipe[j] = load_seg(xr, V, j);
     __syncthreads();
 
+    // Candidate test in the float domain: key(x) > T  <=>  x > value(T) for ordinary
+    // values (-0 and +0 compare equal either way); !(x <= tv) also lets NaN through to
+    // the exact key test.  tv = NaN before the first compaction accepts everything.
+    float tv = __int_as_float(0x7fc00000);
+    int seg_start = 0;
+    if (K <= TK_THREADS / 2 && nseg >= 2) {
+      // Quick start: the K-th largest of the 512 per-thread maxima over the first two
+      // segments is a key that at least K elements reach, so every element of the top K
+      // has a key >= it.  Keep the elements of those segments that reach it; later
+      // elements need a strictly larger key (an equal key with a larger column ranks
+      // below those K).  This replaces compacting a buffer of 8192 entries.
+      const int64_t i0a = int64_t(threadIdx.x) * TK_VEC;
+      const int64_t i0b = int64_t(TK_SEG) + i0a;
+      const uint32_t wa[4] = {pipe[0].x, pipe[0].y, pipe[0].z, pipe[0].w};
+      const uint32_t wb[4] = {pipe[1].x, pipe[1].y, pipe[1].z, pipe[1].w};
+      uint32_t ka[TK_VEC], kb[TK_VEC];
+      uint32_t tmax = 0;
+#pragma unroll
+      for (int e = 0; e < TK_VEC; ++e) {
+        ka[e] = (i0a + e < V) ? bf16_key(wa[e >> 1] >> (16 * (e & 1))) : 0u;
+        kb[e] = (i0b + e < V) ? bf16_key(wb[e >> 1] >> (16 * (e & 1))) : 0u;
+        tmax = max(tmax, max(ka[e], kb[e]));
+      }
+      if (lse_out != nullptr) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t* w = h ? wb : wa;
+          const int64_t i0 = h ? i0b : i0a;
+          float x2[TK_VEC];
+          float vm = -INFINITY;
+#pragma unroll
+          for (int e = 0; e < TK_VEC; ++e) {
+            const float xv = __uint_as_float((e & 1) ? (w[e >> 1] & 0xFFFF0000u) : (w[e >> 1] << 16));
+            x2[e] = (i0 + e < V) ? xv * 1.4426950408889634f : -INFINITY;
+            vm = fmaxf(vm, x2[e]);
+          }
+          const float nm = fmaxf(lm, vm);
+          if (nm != -INFINITY) {
+            float acc = ls * ex2_approx(lm - nm);
+#pragma unroll
+            for (int e = 0; e < TK_VEC; ++e) acc += ex2_approx(x2[e] - nm);
+            ls = acc;
+            lm = nm;
+          }
+        }
+      }
+      sm.buf[threadIdx.x] = static_cast<unsigned long long>(tmax) << 32;
+      __syncthreads();
+      uint32_t count_ge = 0;
+      const uint32_t T = kth_largest_key(sm, TK_THREADS, uint32_t(K), count_ge);
+      if (threadIdx.x == 0) sm.count = 0;
+      __syncthreads();
+#pragma unroll
+      for (int e = 0; e < TK_VEC; ++e)
+        warp_append(sm, (i0a + e < V) && ka[e] >= T,
+                    (static_cast<unsigned long long>(ka[e]) << 32) | uint32_t(~uint32_t(i0a + e)));
+#pragma unroll
+      for (int e = 0; e < TK_VEC; ++e)
+        warp_append(sm, (i0b + e < V) && kb[e] >= T,
+                    (static_cast<unsigned long long>(kb[e]) << 32) | uint32_t(~uint32_t(i0b + e)));
+      thresh = int(T);
+      const uint32_t tb = (T & 0x8000u) ? (T & 0x7FFFu) : (~T & 0xFFFFu);
+      tv = __uint_as_float(tb << 16);
+      if (TK_PIPE < nseg) pipe[0] = load_seg(xr, V, TK_PIPE);
+      if (TK_PIPE + 1 < nseg) pipe[1] = load_seg(xr, V, TK_PIPE + 1);
+      seg_start = 2;
+      __syncthreads();
+      const uint32_t cnt = sm.count;
+      __syncthreads();
+      if (cnt > uint32_t(TK_CAP - TK_CHECK * TK_SEG)) {  // many ties at T: make room first
+        thresh = compact(sm, uint32_t(K));
+        const uint32_t tb2 = (uint32_t(thresh) & 0x8000u) ? (uint32_t(thresh) & 0x7FFFu)
+                                                          : (~uint32_t(thresh) & 0xFFFFu);
+        tv = __uint_as_float(tb2 << 16);
+      }
+    }
     for (int base = 0; base < nseg; base += TK_PIPE) {
 #pragma unroll
       for (int j = 0; j < TK_PIPE; ++j) {
         const int seg = base + j;
-        if (seg < nseg) {
+        if (seg < nseg && seg >= seg_start) {
           const uint4 v = pipe[j];
           if (seg + TK_PIPE < nseg) pipe[j] = load_seg(xr, V, seg + TK_PIPE);
           const uint32_t w[4] = {v.x, v.y, v.z, v.w};
           const int64_t i0 = int64_t(seg) * TK_SEG + int64_t(threadIdx.x) * TK_VEC;
+          float xf[TK_VEC];
+#pragma unroll
+          for (int e = 0; e < TK_VEC; ++e)
+            xf[e] = __uint_as_float((e & 1) ? (w[e >> 1] & 0xFFFF0000u) : (w[e >> 1] << 16));
           if (lse_out != nullptr) {
-            float x2[TK_VEC];
             float vm = -INFINITY;
+            float x2[TK_VEC];
 #pragma unroll
             for (int e = 0; e < TK_VEC; ++e) {
-              const float xv = __uint_as_float((w[e >> 1] >> (16 * (e & 1))) << 16) * 1.4426950408889634f;
-              x2[e] = (i0 + e < V) ? xv : -INFINITY;
+              x2[e] = (i0 + e < V) ? xf[e] * 1.4426950408889634f : -INFINITY;
               vm = fmaxf(vm, x2[e]);
             }
             const float nm = fmaxf(lm, vm);
@@ -241,18 +328,35 @@ __global__ void __launch_bounds__(TK_THREADS, 2)
               lm = nm;
             }
           }
+          uint32_t take = 0;
 #pragma unroll
           for (int e = 0; e < TK_VEC; ++e) {
-            const uint32_t key = bf16_key(w[e >> 1] >> (16 * (e & 1)));
-            const bool take = (i0 + e < V) && int(key) > thresh;
-            const unsigned long long c =
-                (static_cast<unsigned long long>(key) << 32) | uint32_t(~uint32_t(i0 + e));
-            warp_append(sm, take, c);
+            if (!(xf[e] <= tv) && i0 + e < V) {
+              const uint32_t key = bf16_key(w[e >> 1] >> (16 * (e & 1)));
+              if (int(key) > thresh) take |= 1u << e;
+            }
           }
-          __syncthreads();
-          const uint32_t cnt = sm.count;
-          __syncthreads();  // every thread has read the count before anyone appends again
-          if (cnt > uint32_t(TK_CAP - TK_SEG)) thresh = compact(sm, uint32_t(K));
+          if (__any_sync(0xffffffffu, take != 0)) {
+#pragma unroll
+            for (int e = 0; e < TK_VEC; ++e) {
+              const uint32_t key = bf16_key(w[e >> 1] >> (16 * (e & 1)));
+              const unsigned long long c =
+                  (static_cast<unsigned long long>(key) << 32) | uint32_t(~uint32_t(i0 + e));
+              warp_append(sm, (take >> e) & 1u, c);
+            }
+          }
+          if ((seg % TK_CHECK) == TK_CHECK - 1 || seg == nseg - 1) {
+            __syncthreads();
+            const uint32_t cnt = sm.count;
+            __syncthreads();  // every thread has read the count before anyone appends again
+            if (cnt > uint32_t(TK_CAP - TK_CHECK * TK_SEG)) {
+              thresh = compact(sm, uint32_t(K));
+              // float form of the new threshold key (its bf16 value)
+              const uint32_t tb = (uint32_t(thresh) & 0x8000u) ? (uint32_t(thresh) & 0x7FFFu)
+                                                               : (~uint32_t(thresh) & 0xFFFFu);
+              tv = __uint_as_float(tb << 16);
+            }
+          }
         }
       }
     }
