@@ -93,10 +93,21 @@ __device__ void find_bin_from_top(TopkSmem& sm, uint32_t target) {
 
 // K-th largest key among buf[0, count) (count >= K); also returns how many
 // entries have key >= that value.
+// hist[bin] += 1 for every lane with a valid bin, one atomic per distinct bin per warp
+// (the keys near the top of a row fall in very few bins).  All 32 lanes call it.
+__device__ __forceinline__ void hist_add_warp(uint32_t* hist, bool valid, uint32_t bin) {
+  const uint32_t b = valid ? bin : 0xFFFFFFFFu;
+  const uint32_t peers = __match_any_sync(0xffffffffu, b);
+  if (valid && lane_id() == uint32_t(__ffs(peers) - 1)) atomicAdd(&hist[bin], uint32_t(__popc(peers)));
+}
+
 __device__ uint32_t kth_largest_key(TopkSmem& sm, uint32_t count, uint32_t K, uint32_t& count_ge) {
   for (int i = threadIdx.x; i < 256; i += TK_THREADS) sm.hist[i] = 0;
   __syncthreads();
-  for (uint32_t i = threadIdx.x; i < count; i += TK_THREADS) atomicAdd(&sm.hist[comp_key(sm.buf[i]) >> 8], 1u);
+  for (uint32_t base = threadIdx.x & ~31u; base < count; base += TK_THREADS) {
+    const uint32_t i = base + lane_id();
+    hist_add_warp(sm.hist, i < count, i < count ? comp_key(sm.buf[i]) >> 8 : 0u);
+  }
   __syncthreads();
   find_bin_from_top(sm, K);
   __syncthreads();
@@ -104,9 +115,10 @@ __device__ uint32_t kth_largest_key(TopkSmem& sm, uint32_t count, uint32_t K, ui
   __syncthreads();
   for (int i = threadIdx.x; i < 256; i += TK_THREADS) sm.hist[i] = 0;
   __syncthreads();
-  for (uint32_t i = threadIdx.x; i < count; i += TK_THREADS) {
-    const uint32_t k = comp_key(sm.buf[i]);
-    if ((k >> 8) == b1) atomicAdd(&sm.hist[k & 255u], 1u);
+  for (uint32_t base = threadIdx.x & ~31u; base < count; base += TK_THREADS) {
+    const uint32_t i = base + lane_id();
+    const uint32_t k = i < count ? comp_key(sm.buf[i]) : 0u;
+    hist_add_warp(sm.hist, i < count && (k >> 8) == b1, k & 255u);
   }
   __syncthreads();
   find_bin_from_top(sm, need);
@@ -410,6 +422,378 @@ __global__ void __launch_bounds__(TK_THREADS, 2)
   }
 }
 
+// ---------------------------------------------------------------------------
+// Fast path for K <= 256 (the pages' top-100 cache): the same selection, with no
+// block-wide barrier while the row streams.  After the quick start (a block-wide
+// threshold every warp uses), each warp appends its candidates to its own region of
+// the buffer with warp votes only, and compacts that region by itself when it fills
+// (raising its own threshold, which is valid for its later elements for the same
+// reason as above: at least K kept entries reach it, all with smaller columns).
+
+constexpr int TF_WARPS = TK_THREADS / 32;    // 16
+constexpr int TF_WCAP = TK_CAP / TF_WARPS;   // 512 entries per warp region
+constexpr int TF_WSEG = 32 * TK_VEC;         // at most 256 new entries per warp per segment
+constexpr int TF_MAXK = TF_WCAP - TF_WSEG;   // a region compacts with at least this many entries
+
+struct TopkFastSmem {
+  TopkSmem base;                             // buf = the 16 warp regions, then the row's final buffer
+  uint32_t whist[TF_WARPS][256];
+  uint32_t wcount[TF_WARPS];
+};
+
+// Warp: where, scanning the warp's 256 bins from the top, the running count reaches target.
+__device__ __forceinline__ void warp_find_bin(const uint32_t* h, uint32_t target, uint32_t& bin, uint32_t& need,
+                                              uint32_t& above) {
+  const uint32_t lane = lane_id();
+  uint32_t local[8];
+  uint32_t sum = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    local[j] = h[255 - (lane * 8 + j)];
+    sum += local[j];
+  }
+  uint32_t incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= uint32_t(o)) incl += t;
+  }
+  const uint32_t excl = incl - sum;
+  uint32_t b = 0, nd = 0, ab = 0;
+  const bool mine = excl < target && target <= incl;
+  if (mine) {
+    uint32_t run = excl;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (run < target && target <= run + local[j] && nd == 0) {
+        b = 255 - (lane * 8 + j);
+        nd = target - run;
+        ab = run;
+      }
+      run += local[j];
+    }
+  }
+  const uint32_t owner = __ffs(__ballot_sync(0xffffffffu, mine)) - 1;
+  bin = __shfl_sync(0xffffffffu, b, owner);
+  need = __shfl_sync(0xffffffffu, nd, owner);
+  above = __shfl_sync(0xffffffffu, ab, owner);
+}
+
+// Warp: K-th largest key among reg[0, cnt) (cnt >= K) and how many keys reach it.
+__device__ uint32_t warp_kth_largest(const unsigned long long* reg, uint32_t cnt, uint32_t K, uint32_t* h,
+                                     uint32_t& count_ge) {
+  const uint32_t lane = lane_id();
+  for (uint32_t i = lane; i < 256; i += 32) h[i] = 0;
+  __syncwarp();
+  for (uint32_t base = 0; base < cnt; base += 32) {
+    const uint32_t i = base + lane;
+    hist_add_warp(h, i < cnt, i < cnt ? comp_key(reg[i]) >> 8 : 0u);
+  }
+  __syncwarp();
+  uint32_t b1, need, above1;
+  warp_find_bin(h, K, b1, need, above1);
+  __syncwarp();
+  for (uint32_t i = lane; i < 256; i += 32) h[i] = 0;
+  __syncwarp();
+  for (uint32_t base = 0; base < cnt; base += 32) {
+    const uint32_t i = base + lane;
+    const uint32_t k = i < cnt ? comp_key(reg[i]) : 0u;
+    hist_add_warp(h, i < cnt && (k >> 8) == b1, k & 255u);
+  }
+  __syncwarp();
+  uint32_t b2, need2, above2;
+  warp_find_bin(h, need, b2, need2, above2);
+  count_ge = above1 + above2 + h[b2];
+  __syncwarp();
+  return (b1 << 8) | b2;
+}
+
+// Warp: keep the entries of reg[0, cnt) with key >= T, in place; returns the new count.
+__device__ uint32_t warp_filter_ge(unsigned long long* reg, uint32_t cnt, uint32_t T) {
+  const uint32_t lane = lane_id();
+  uint32_t out = 0;
+  for (uint32_t base = 0; base < cnt; base += 256) {
+    unsigned long long held[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const uint32_t i = base + lane + 32u * j;
+      held[j] = i < cnt ? reg[i] : 0ull;
+    }
+    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const uint32_t i = base + lane + 32u * j;
+      const bool take = i < cnt && comp_key(held[j]) >= T;
+      const uint32_t bal = __ballot_sync(0xffffffffu, take);
+      if (take) reg[out + __popc(bal & ((1u << lane) - 1u))] = held[j];
+      out += __popc(bal);
+    }
+    __syncwarp();
+  }
+  return out;
+}
+
+// Warp: sort reg[0, cnt) descending (bitonic, padded with 0 up to a power of two <= TF_WCAP).
+__device__ void warp_sort_desc(unsigned long long* reg, uint32_t cnt) {
+  const uint32_t lane = lane_id();
+  uint32_t P = 32;
+  while (P < cnt) P <<= 1;
+  for (uint32_t i = cnt + lane; i < P; i += 32) reg[i] = 0ull;
+  __syncwarp();
+  for (uint32_t k = 2; k <= P; k <<= 1) {
+    for (uint32_t j = k >> 1; j > 0; j >>= 1) {
+      for (uint32_t i = lane; i < P; i += 32) {
+        const uint32_t ixj = i ^ j;
+        if (ixj > i) {
+          const unsigned long long a = reg[i], b = reg[ixj];
+          if (((i & k) == 0) ? (a < b) : (a > b)) {
+            reg[i] = b;
+            reg[ixj] = a;
+          }
+        }
+      }
+      __syncwarp();
+    }
+  }
+}
+
+__device__ __forceinline__ float key_to_float(uint32_t key) {
+  const uint32_t b = (key & 0x8000u) ? (key & 0x7FFFu) : (~key & 0xFFFFu);
+  return __uint_as_float(b << 16);
+}
+
+__global__ void __launch_bounds__(TK_THREADS, 2)
+    kd_topk_fast_kernel(const uint16_t* __restrict__ X, int64_t N, int64_t V, int64_t ld, int K,
+                        int32_t* __restrict__ ids_out, float* __restrict__ vals_out, float* __restrict__ lse_out) {
+  extern __shared__ __align__(16) uint8_t tkf_smem_raw[];
+  TopkFastSmem& fs = *reinterpret_cast<TopkFastSmem*>(tkf_smem_raw);
+  TopkSmem& sm = fs.base;
+  const int nseg = int((V + TK_SEG - 1) / TK_SEG);  // >= 2 on this path
+  const uint32_t warp = threadIdx.x >> 5, lane = lane_id();
+  unsigned long long* reg = sm.buf + warp * TF_WCAP;
+  const uint32_t V32 = uint32_t(V);
+
+  for (int64_t row = blockIdx.x; row < N; row += gridDim.x) {
+    const uint16_t* xr = X + row * ld;
+    float lm = -INFINITY, ls = 0.f;
+    uint4 pipe[TK_PIPE];
+#pragma unroll
+    for (int j = 0; j < TK_PIPE; ++j)
+      if (j < nseg) pipe[j] = load_seg(xr, V, j);
+
+    // quick start over segments 0 and 1 (block-wide)
+    const uint32_t i0a = threadIdx.x * TK_VEC;
+    const uint32_t i0b = TK_SEG + i0a;
+    uint32_t ka[TK_VEC], kb[TK_VEC];
+    uint32_t tmax = 0;
+    {
+      const uint32_t wa[4] = {pipe[0].x, pipe[0].y, pipe[0].z, pipe[0].w};
+      const uint32_t wb[4] = {pipe[1].x, pipe[1].y, pipe[1].z, pipe[1].w};
+#pragma unroll
+      for (int e = 0; e < TK_VEC; ++e) {
+        ka[e] = (i0a + e < V32) ? bf16_key(wa[e >> 1] >> (16 * (e & 1))) : 0u;
+        kb[e] = (i0b + e < V32) ? bf16_key(wb[e >> 1] >> (16 * (e & 1))) : 0u;
+        tmax = max(tmax, max(ka[e], kb[e]));
+      }
+      if (lse_out != nullptr) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t* w = h ? wb : wa;
+          const uint32_t i0 = h ? i0b : i0a;
+          float x2[TK_VEC];
+          float vm = -INFINITY;
+#pragma unroll
+          for (int e = 0; e < TK_VEC; ++e) {
+            const float xv = __uint_as_float((e & 1) ? (w[e >> 1] & 0xFFFF0000u) : (w[e >> 1] << 16));
+            x2[e] = (i0 + e < V32) ? xv * 1.4426950408889634f : -INFINITY;
+            vm = fmaxf(vm, x2[e]);
+          }
+          const float nm = fmaxf(lm, vm);
+          if (nm != -INFINITY) {
+            float acc = ls * ex2_approx(lm - nm);
+#pragma unroll
+            for (int e = 0; e < TK_VEC; ++e) acc += ex2_approx(x2[e] - nm);
+            ls = acc;
+            lm = nm;
+          }
+        }
+      }
+    }
+    __syncthreads();  // the previous row's buffer is no longer read
+    sm.buf[threadIdx.x] = static_cast<unsigned long long>(tmax) << 32;
+    __syncthreads();
+    uint32_t count_ge = 0;
+    const uint32_t T0 = kth_largest_key(sm, TK_THREADS, uint32_t(K), count_ge);  // ends with a barrier
+    // each warp keeps, in its own region, the quick-start elements that reach T0
+    uint32_t cnt = 0;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+#pragma unroll
+      for (int e = 0; e < TK_VEC; ++e) {
+        const uint32_t key = h ? kb[e] : ka[e];
+        const uint32_t idx = (h ? i0b : i0a) + e;
+        const bool take = idx < V32 && key >= T0;
+        const uint32_t bal = __ballot_sync(0xffffffffu, take);
+        if (take)
+          reg[cnt + __popc(bal & ((1u << lane) - 1u))] = (static_cast<unsigned long long>(key) << 32) | uint32_t(~idx);
+        cnt += __popc(bal);
+      }
+    }
+    __syncwarp();
+    uint32_t wth = T0;  // this warp's later elements need key > wth
+    float tv = key_to_float(T0);
+    auto compact_region = [&]() {
+      uint32_t cge = 0;
+      const uint32_t T = warp_kth_largest(reg, cnt, uint32_t(K), fs.whist[warp], cge);
+      if (cge <= uint32_t(TF_MAXK)) {
+        cnt = warp_filter_ge(reg, cnt, T);
+        wth = T;
+      } else {  // many ties at T: keep exactly the K best
+        warp_sort_desc(reg, cnt);
+        cnt = uint32_t(K);
+        wth = comp_key(reg[K - 1]);
+      }
+      tv = key_to_float(wth);
+    };
+    if (cnt > uint32_t(TF_MAXK)) compact_region();
+    if (TK_PIPE < nseg) pipe[0] = load_seg(xr, V, TK_PIPE);
+    if (TK_PIPE + 1 < nseg) pipe[1] = load_seg(xr, V, TK_PIPE + 1);
+
+    // streaming: no block barrier from here to the end of the row
+    for (int base = 0; base < nseg; base += TK_PIPE) {
+#pragma unroll
+      for (int j = 0; j < TK_PIPE; ++j) {
+        const int seg = base + j;
+        if (seg >= 2 && seg < nseg) {
+          const uint4 v = pipe[j];
+          if (seg + TK_PIPE < nseg) pipe[j] = load_seg(xr, V, seg + TK_PIPE);
+          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+          const uint32_t i0 = uint32_t(seg) * TK_SEG + threadIdx.x * TK_VEC;
+          float xf[TK_VEC];
+#pragma unroll
+          for (int e = 0; e < TK_VEC; ++e)
+            xf[e] = __uint_as_float((e & 1) ? (w[e >> 1] & 0xFFFF0000u) : (w[e >> 1] << 16));
+          if (lse_out != nullptr) {
+            float vm = -INFINITY;
+            float x2[TK_VEC];
+#pragma unroll
+            for (int e = 0; e < TK_VEC; ++e) {
+              x2[e] = (i0 + e < V32) ? xf[e] * 1.4426950408889634f : -INFINITY;
+              vm = fmaxf(vm, x2[e]);
+            }
+            const float nm = fmaxf(lm, vm);
+            if (nm != -INFINITY) {
+              float acc = ls * ex2_approx(lm - nm);
+#pragma unroll
+              for (int e = 0; e < TK_VEC; ++e) acc += ex2_approx(x2[e] - nm);
+              ls = acc;
+              lm = nm;
+            }
+          }
+          uint32_t take = 0;
+#pragma unroll
+          for (int e = 0; e < TK_VEC; ++e) {
+            if (!(xf[e] <= tv) && i0 + e < V32) {
+              const uint32_t key = bf16_key(w[e >> 1] >> (16 * (e & 1)));
+              if (key > wth) take |= 1u << e;
+            }
+          }
+          if (__any_sync(0xffffffffu, take != 0)) {
+#pragma unroll
+            for (int e = 0; e < TK_VEC; ++e) {
+              const bool t = (take >> e) & 1u;
+              const uint32_t bal = __ballot_sync(0xffffffffu, t);
+              if (t) {
+                const uint32_t key = bf16_key(w[e >> 1] >> (16 * (e & 1)));
+                reg[cnt + __popc(bal & ((1u << lane) - 1u))] =
+                    (static_cast<unsigned long long>(key) << 32) | uint32_t(~(i0 + e));
+              }
+              cnt += __popc(bal);
+            }
+            __syncwarp();
+            if (cnt > uint32_t(TF_MAXK)) compact_region();
+          }
+        }
+      }
+    }
+
+    // row end.  The highest warp threshold G is reached by at least K entries of that
+    // warp's region, so every entry of the top K has key >= G: drop the rest per warp,
+    // then gather the regions into one contiguous buffer and select as above.
+    if (lane == 0) fs.wcount[warp] = wth;
+    __syncthreads();
+    uint32_t G = 0;
+    for (uint32_t w = 0; w < uint32_t(TF_WARPS); ++w) G = max(G, fs.wcount[w]);
+    __syncthreads();
+    if (G > wth) cnt = warp_filter_ge(reg, cnt, G);
+    if (lane == 0) fs.wcount[warp] = cnt;
+    unsigned long long held[TF_WCAP / 32];
+#pragma unroll
+    for (int j = 0; j < TF_WCAP / 32; ++j) {
+      const uint32_t i = lane + 32u * j;
+      held[j] = i < cnt ? reg[i] : 0ull;
+    }
+    __syncthreads();
+    uint32_t off = 0, total = 0;
+    for (uint32_t w = 0; w < uint32_t(TF_WARPS); ++w) {
+      const uint32_t c = fs.wcount[w];
+      if (w < warp) off += c;
+      total += c;
+    }
+    if (lse_out != nullptr) {
+      for (int o = 16; o > 0; o >>= 1) {
+        const float om = __shfl_xor_sync(0xffffffffu, lm, o);
+        const float os = __shfl_xor_sync(0xffffffffu, ls, o);
+        const float nm = fmaxf(lm, om);
+        if (nm != -INFINITY) {
+          ls = ls * ex2_approx(lm - nm) + os * ex2_approx(om - nm);
+          lm = nm;
+        }
+      }
+      if (lane == 0) {
+        sm.red_m[warp] = lm;
+        sm.red_s[warp] = ls;
+      }
+    }
+    __syncthreads();  // every region is in registers, counts and lse partials are published
+#pragma unroll
+    for (int j = 0; j < TF_WCAP / 32; ++j) {
+      const uint32_t i = lane + 32u * j;
+      if (i < cnt) sm.buf[off + i] = held[j];
+    }
+    if (threadIdx.x == 0) {
+      sm.count = total;
+      if (lse_out != nullptr) {
+        float M = -INFINITY, S = 0.f;
+        for (int i = 0; i < TF_WARPS; ++i) {
+          const float nm = fmaxf(M, sm.red_m[i]);
+          if (nm != -INFINITY) {
+            S = S * exp2f(M - nm) + sm.red_s[i] * exp2f(sm.red_m[i] - nm);
+            M = nm;
+          }
+        }
+        lse_out[row] = (M + log2f(S)) * 0.69314718055994531f;
+      }
+    }
+    __syncthreads();
+    uint32_t count = total;
+    if (count > uint32_t(K)) {
+      uint32_t cge = 0;
+      const uint32_t T = kth_largest_key(sm, count, uint32_t(K), cge);
+      if (cge < count) filter_ge(sm, count, T);
+      __syncthreads();
+      count = sm.count;
+      __syncthreads();
+    }
+    sort_desc(sm, count);
+    for (int j = threadIdx.x; j < K; j += TK_THREADS) {
+      const uint32_t col = ~uint32_t(sm.buf[j]);
+      ids_out[row * K + j] = int32_t(col);
+      vals_out[row * K + j] = __uint_as_float(uint32_t(xr[col]) << 16);
+    }
+  }
+}
+
 cudaError_t launch_topk(const uint16_t* X, int64_t N, int64_t V, int64_t ld, int K, int32_t* ids, float* vals,
                         float* lse, uint32_t* err, cudaStream_t s) {
   (void)err;
@@ -424,7 +808,18 @@ cudaError_t launch_topk(const uint16_t* X, int64_t N, int64_t V, int64_t ld, int
   if (int64_t(grid) > N) grid = int(N);
   if (grid <= 0) return cudaSuccess;
   prof_before("kd_topk_cache", s);
-  kd_topk_kernel<<<grid, TK_THREADS, smem, s>>>(X, N, V, ld, K, ids, vals, lse);
+  if (K <= TF_MAXK && V > int64_t(TK_SEG)) {
+    static bool fast_attr = false;
+    const int fsmem = int(sizeof(TopkFastSmem));
+    if (!fast_attr) {
+      cudaError_t e = cudaFuncSetAttribute(kd_topk_fast_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, fsmem);
+      if (e != cudaSuccess) return e;
+      fast_attr = true;
+    }
+    kd_topk_fast_kernel<<<grid, TK_THREADS, fsmem, s>>>(X, N, V, ld, K, ids, vals, lse);
+  } else {
+    kd_topk_kernel<<<grid, TK_THREADS, smem, s>>>(X, N, V, ld, K, ids, vals, lse);
+  }
   prof_after(s);
   return cudaGetLastError();
 }
