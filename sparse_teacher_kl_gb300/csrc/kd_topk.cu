@@ -423,25 +423,53 @@ __global__ void __launch_bounds__(TK_THREADS, 2)
 }
 
 // ---------------------------------------------------------------------------
-// Fast path for K <= 256 (the pages' top-100 cache): the same selection, with no
-// block-wide barrier while the row streams.  After the quick start (a block-wide
-// threshold every warp uses), each warp appends its candidates to its own region of
-// the buffer with warp votes only, and compacts that region by itself when it fills
-// (raising its own threshold, which is valid for its later elements for the same
-// reason as above: at least K kept entries reach it, all with smaller columns).
+// Warp-per-row path for K <= TW_MAXK (the pages' top-100 cache).  The same selection,
+// run by one warp per row so that no block barrier is ever taken:
+//  * a lane reads 16 bytes per step (256 elements per warp step), TW_PIPE steps ahead,
+//    and the next row's first steps while it finishes the current row;
+//  * its 8 values are tested with one packed bf16 max against the warp's threshold,
+//    TW_GROUP steps at a time with one vote;
+//    a vector that passes is queued whole in shared memory, and the warp filters the
+//    queue 32 vectors at a time (one vector per lane) with the exact keys;
+//  * the candidate buffer is compacted by the warp (two byte histograms) once it holds
+//    more than 2K + 64 entries, raising the threshold to the K-th largest key seen so
+//    far: one warp sees the whole row, so the threshold is as tight as the prefix allows.
+// Until the first compaction every element is a candidate (key >= 0).  Elements past V
+// read as -inf and are dropped by their column.
 
-constexpr int TF_WARPS = TK_THREADS / 32;    // 16
-constexpr int TF_WCAP = TK_CAP / TF_WARPS;   // 512 entries per warp region
-constexpr int TF_WSEG = 32 * TK_VEC;         // at most 256 new entries per warp per segment
-constexpr int TF_MAXK = TF_WCAP - TF_WSEG;   // a region compacts with at least this many entries
+constexpr int TW_MAXK = 256;
+constexpr int TW_STEP = 32 * TK_VEC;         // elements per warp step
+constexpr int TW_PIPE = 8;                   // steps in flight per warp (registers)
+constexpr int TW_GROUP = 4;                  // steps tested together (one vote)
+constexpr int TW_QUEUE = 64;                 // queued vectors per warp (ring)
+constexpr float TW_LOG2E = 1.4426950408889634f;
+static_assert(TW_PIPE % TW_GROUP == 0, "groups tile the pipeline");
 
-struct TopkFastSmem {
-  TopkSmem base;                             // buf = the 16 warp regions, then the row's final buffer
-  uint32_t whist[TF_WARPS][256];
-  uint32_t wcount[TF_WARPS];
+// A configuration: CAP candidate entries per warp, WARPS rows in flight per block (one
+// block per SM), BATCH queued vectors filtered per drain (at most 8 * BATCH new entries).
+// A compaction leaves at most KEEP entries and the trigger 2K + 64 stays within KEEP, so
+// a drain always fits.  The smaller buffer lets more warps share an SM.
+template <int CAP_, int WARPS_, int BATCH_>
+struct TwCfg {
+  static constexpr int CAP = CAP_;
+  static constexpr int WARPS = WARPS_;
+  static constexpr int BATCH = BATCH_;
+  static constexpr int KEEP = CAP - 8 * BATCH;
+  static constexpr int MAXK = (KEEP - 64) / 2 < TW_MAXK ? (KEEP - 64) / 2 : TW_MAXK;
+  static_assert((CAP & (CAP - 1)) == 0, "the bitonic sort pads to a power of two within the buffer");
+  static_assert(BATCH <= 32 && BATCH + 32 <= TW_QUEUE, "one vector per lane; the queue holds a batch and a step");
+};
+using TwSmallK = TwCfg<512, 20, 16>;   // K <= 160
+using TwLargeK = TwCfg<1024, 16, 32>;  // K <= 256
+
+template <int CAP>
+struct TopkWarpSmem {
+  unsigned long long buf[CAP];
+  uint4 qv[TW_QUEUE];
+  uint32_t qcol[TW_QUEUE];
+  uint32_t hist[256];
 };
 
-// Warp: where, scanning the warp's 256 bins from the top, the running count reaches target.
 __device__ __forceinline__ void warp_find_bin(const uint32_t* h, uint32_t target, uint32_t& bin, uint32_t& need,
                                               uint32_t& above) {
   const uint32_t lane = lane_id();
@@ -508,7 +536,8 @@ __device__ uint32_t warp_kth_largest(const unsigned long long* reg, uint32_t cnt
   return (b1 << 8) | b2;
 }
 
-// Warp: keep the entries of reg[0, cnt) with key >= T, in place; returns the new count.
+// Warp: keep the entries of reg[0, cnt) with key >= T, in place (each round of 256 is
+// read before any survivor of it is written); returns the new count.
 __device__ uint32_t warp_filter_ge(unsigned long long* reg, uint32_t cnt, uint32_t T) {
   const uint32_t lane = lane_id();
   uint32_t out = 0;
@@ -533,7 +562,7 @@ __device__ uint32_t warp_filter_ge(unsigned long long* reg, uint32_t cnt, uint32
   return out;
 }
 
-// Warp: sort reg[0, cnt) descending (bitonic, padded with 0 up to a power of two <= TF_WCAP).
+// Warp: sort reg[0, cnt) descending (bitonic, padded with 0 up to a power of two).
 __device__ void warp_sort_desc(unsigned long long* reg, uint32_t cnt) {
   const uint32_t lane = lane_id();
   uint32_t P = 32;
@@ -557,241 +586,316 @@ __device__ void warp_sort_desc(unsigned long long* reg, uint32_t cnt) {
   }
 }
 
+// 16 bytes of warp step `st` for this lane; elements past V read as -inf.  Out of
+// line: only the ragged end of a row and the next row's first steps come here.
+__device__ __noinline__ uint4 load_step(const uint16_t* xr, int64_t V, int st) {
+  const int64_t i0 = int64_t(st) * TW_STEP + int64_t(lane_id()) * TK_VEC;
+  if (i0 + TK_VEC <= V) return __ldcs(reinterpret_cast<const uint4*>(xr + i0));
+  uint32_t w[4] = {0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u};
+#pragma unroll
+  for (int e = 0; e < TK_VEC; ++e)
+    if (i0 + e < V) {
+      const int sh = 16 * (e & 1);
+      w[e >> 1] = (w[e >> 1] & ~(0xFFFFu << sh)) | (uint32_t(xr[i0 + e]) << sh);
+    }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+__device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// Largest of the 8 bf16 in v, widened to float (NaN if one of them is NaN).
+__device__ __forceinline__ float vec_max(const uint4& v) {
+  uint32_t m = bmax2(bmax2(v.x, v.y), bmax2(v.z, v.w));
+  m = bmax2(m, __byte_perm(m, 0u, 0x1032));
+  return __uint_as_float(m & 0xFFFF0000u);
+}
+
 __device__ __forceinline__ float key_to_float(uint32_t key) {
   const uint32_t b = (key & 0x8000u) ? (key & 0x7FFFu) : (~key & 0xFFFFu);
   return __uint_as_float(b << 16);
 }
 
-__global__ void __launch_bounds__(TK_THREADS, 2)
-    kd_topk_fast_kernel(const uint16_t* __restrict__ X, int64_t N, int64_t V, int64_t ld, int K,
-                        int32_t* __restrict__ ids_out, float* __restrict__ vals_out, float* __restrict__ lse_out) {
-  extern __shared__ __align__(16) uint8_t tkf_smem_raw[];
-  TopkFastSmem& fs = *reinterpret_cast<TopkFastSmem*>(tkf_smem_raw);
-  TopkSmem& sm = fs.base;
-  const int nseg = int((V + TK_SEG - 1) / TK_SEG);  // >= 2 on this path
-  const uint32_t warp = threadIdx.x >> 5, lane = lane_id();
-  unsigned long long* reg = sm.buf + warp * TF_WCAP;
-  const uint32_t V32 = uint32_t(V);
+// Per-warp selection state (warp-uniform).
+struct WarpSel {
+  uint32_t cnt;   // entries in buf
+  uint32_t qh;    // queue head (ring index of the oldest queued vector)
+  uint32_t nq;    // queued vectors
+  uint32_t wth;   // threshold key
+  bool ge;        // before the first compaction: key >= wth (= 0, every element) is a candidate
+  float tv;       // float value of wth, for the pre-tests
+};
 
-  for (int64_t row = blockIdx.x; row < N; row += gridDim.x) {
-    const uint16_t* xr = X + row * ld;
-    float lm = -INFINITY, ls = 0.f;
-    uint4 pipe[TK_PIPE];
-#pragma unroll
-    for (int j = 0; j < TK_PIPE; ++j)
-      if (j < nseg) pipe[j] = load_seg(xr, V, j);
+// Warp: raise the threshold to the K-th largest key in the buffer and drop what
+// cannot reach the top K.
+template <class C>
+__device__ __forceinline__ void warp_compact(TopkWarpSmem<C::CAP>& ws, WarpSel& st, uint32_t K) {
+  uint32_t cge = 0;
+  const uint32_t T = warp_kth_largest(ws.buf, st.cnt, K, ws.hist, cge);
+  if (cge <= uint32_t(C::KEEP)) {
+    if (cge < st.cnt) st.cnt = warp_filter_ge(ws.buf, st.cnt, T);
+    st.wth = T;
+  } else {  // many ties at T: order fully and keep exactly the K best
+    warp_sort_desc(ws.buf, st.cnt);
+    st.cnt = K;
+    st.wth = comp_key(ws.buf[K - 1]);
+    __syncwarp();
+  }
+  st.ge = false;
+  st.tv = key_to_float(st.wth);
+}
 
-    // quick start over segments 0 and 1 (block-wide)
-    const uint32_t i0a = threadIdx.x * TK_VEC;
-    const uint32_t i0b = TK_SEG + i0a;
-    uint32_t ka[TK_VEC], kb[TK_VEC];
-    uint32_t tmax = 0;
-    {
-      const uint32_t wa[4] = {pipe[0].x, pipe[0].y, pipe[0].z, pipe[0].w};
-      const uint32_t wb[4] = {pipe[1].x, pipe[1].y, pipe[1].z, pipe[1].w};
+// Warp: filter the nb (<= BATCH) oldest queued vectors, one per lane.  For values other
+// than NaN, key(x) > wth exactly when x > tv (-0 and +0 have one key), so the test is a
+// float compare; a vector holding a NaN takes the key path.  Out of line: it runs once
+// per BATCH queued vectors, and one copy of it (and of the compaction) keeps the
+// streaming loop small in the instruction cache.
+template <class C>
+__device__ __noinline__ WarpSel warp_drain(TopkWarpSmem<C::CAP>& ws, WarpSel st, uint32_t nb, uint32_t V32,
+                                           uint32_t K, uint32_t trig) {
+  const uint32_t lane = lane_id();
+  uint32_t take = 0, col0 = 0;
+  unsigned long long lo = 0, hi = 0;
+  if (lane < nb) {
+    const uint32_t q = (st.qh + lane) & (TW_QUEUE - 1);
+    const uint4 v = ws.qv[q];
+    col0 = ws.qcol[q];
+    lo = (static_cast<unsigned long long>(v.y) << 32) | v.x;
+    hi = (static_cast<unsigned long long>(v.w) << 32) | v.z;
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    if (st.ge) {
+      take = 0xFFu;  // every element (the threshold key is 0)
+    } else if (vec_max(v) == vec_max(v)) {
 #pragma unroll
-      for (int e = 0; e < TK_VEC; ++e) {
-        ka[e] = (i0a + e < V32) ? bf16_key(wa[e >> 1] >> (16 * (e & 1))) : 0u;
-        kb[e] = (i0b + e < V32) ? bf16_key(wb[e >> 1] >> (16 * (e & 1))) : 0u;
-        tmax = max(tmax, max(ka[e], kb[e]));
+      for (int h = 0; h < 4; ++h) {
+        if (__uint_as_float(w[h] << 16) > st.tv) take |= 1u << (2 * h);
+        if (__uint_as_float(w[h] & 0xFFFF0000u) > st.tv) take |= 2u << (2 * h);
       }
-      if (lse_out != nullptr) {
+    } else {
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const uint32_t* w = h ? wb : wa;
-          const uint32_t i0 = h ? i0b : i0a;
-          float x2[TK_VEC];
-          float vm = -INFINITY;
+      for (int e = 0; e < TK_VEC; ++e)
+        if (bf16_key(w[e >> 1] >> (16 * (e & 1))) > st.wth) take |= 1u << e;
+    }
+    if (col0 + TK_VEC > V32) take &= (V32 > col0 ? (1u << (V32 - col0)) - 1u : 0u);
+  }
+  // exclusive prefix of the per-lane counts (<= 8: four bits) and the warp total
+  const uint32_t c = __popc(take);
+  const uint32_t lt = (1u << lane) - 1u;
+  uint32_t pre = 0, tot = 0;
 #pragma unroll
-          for (int e = 0; e < TK_VEC; ++e) {
-            const float xv = __uint_as_float((e & 1) ? (w[e >> 1] & 0xFFFF0000u) : (w[e >> 1] << 16));
-            x2[e] = (i0 + e < V32) ? xv * 1.4426950408889634f : -INFINITY;
-            vm = fmaxf(vm, x2[e]);
-          }
-          const float nm = fmaxf(lm, vm);
-          if (nm != -INFINITY) {
-            float acc = ls * ex2_approx(lm - nm);
+  for (int b = 0; b < 4; ++b) {
+    const uint32_t bb = __ballot_sync(0xffffffffu, (c >> b) & 1u);
+    pre += uint32_t(__popc(bb & lt)) << b;
+    tot += uint32_t(__popc(bb)) << b;
+  }
+  uint32_t pos = st.cnt + pre;
+  while (take) {
+    const uint32_t e = __ffs(take) - 1;
+    take &= take - 1;
+    const uint32_t bits = uint32_t(((e & 4) ? hi : lo) >> (16 * (e & 3))) & 0xFFFFu;
+    ws.buf[pos++] = (static_cast<unsigned long long>(bf16_key(bits)) << 32) | uint32_t(~(col0 + e));
+  }
+  st.cnt += tot;
+  st.qh = (st.qh + nb) & (TW_QUEUE - 1);
+  st.nq -= nb;
+  __syncwarp();
+  if (st.cnt > trig) warp_compact<C>(ws, st, K);
+  return st;
+}
+
+// Warp: the exact top K of the candidates, in order, to the row's outputs.
+template <class C>
+__device__ __noinline__ void warp_finish(TopkWarpSmem<C::CAP>& ws, uint32_t cnt, uint32_t K, const uint16_t* xr,
+                                         int32_t* ids_row, float* vals_row) {
+  if (cnt > K) {
+    uint32_t cge = 0;
+    const uint32_t T = warp_kth_largest(ws.buf, cnt, K, ws.hist, cge);
+    if (cge < cnt) cnt = warp_filter_ge(ws.buf, cnt, T);
+  }
+  warp_sort_desc(ws.buf, cnt);
+  for (uint32_t j = lane_id(); j < K; j += 32) {
+    const uint32_t col = ~uint32_t(ws.buf[j]);
+    ids_row[j] = int32_t(col);
+    vals_row[j] = __uint_as_float(uint32_t(xr[col]) << 16);
+  }
+}
+
+// Adds the 8 values of v to a running sum of 2^((x - lm) log2 e), b = lm log2 e.
+__device__ __forceinline__ float lse_terms(const uint4& v, float b) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  float acc = 0.f;
 #pragma unroll
-            for (int e = 0; e < TK_VEC; ++e) acc += ex2_approx(x2[e] - nm);
-            ls = acc;
-            lm = nm;
-          }
+  for (int h = 0; h < 4; ++h) {
+    acc += ex2_approx(fmaf(__uint_as_float(w[h] << 16), TW_LOG2E, -b));
+    acc += ex2_approx(fmaf(__uint_as_float(w[h] & 0xFFFF0000u), TW_LOG2E, -b));
+  }
+  return acc;
+}
+
+// One group of TW_GROUP steps of a lane, vectors pipe[g0 ..]: the packed pre-test of each
+// against the warp's threshold (st.tv is NaN before the first compaction: all pass), one
+// vote for the group, and, when a vector passed, its queueing and a drain every BATCH
+// queued.  s0 = the group's first step; `live` = the group's steps that exist.
+template <class C, bool WITH_LSE>
+__device__ __forceinline__ void test_group(TopkWarpSmem<C::CAP>& ws, WarpSel& st, const uint4* v, int s0,
+                                           uint32_t live, float& lm, float& ls, uint32_t V32, uint32_t K,
+                                           uint32_t trig) {
+  const uint32_t lane = lane_id();
+  float vm[TW_GROUP];
+  uint32_t pass = 0;
+#pragma unroll
+  for (int k = 0; k < TW_GROUP; ++k) {
+    vm[k] = vec_max(v[k]);
+    if (((live >> k) & 1u) && !(vm[k] <= st.tv)) pass |= 1u << k;
+  }
+  if (WITH_LSE) {
+    float gm = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < TW_GROUP; ++k)
+      if ((live >> k) & 1u) gm = fmaxf(gm, vm[k]);
+    if (gm > lm) {
+      ls *= ex2_approx((lm - gm) * TW_LOG2E);
+      lm = gm;
+    }
+    if (lm != -INFINITY) {
+      const float b = lm * TW_LOG2E;
+#pragma unroll
+      for (int k = 0; k < TW_GROUP; ++k)
+        if ((live >> k) & 1u) ls += lse_terms(v[k], b);
+    }
+  }
+  if (__any_sync(0xffffffffu, pass != 0)) {
+#pragma unroll
+    for (int k = 0; k < TW_GROUP; ++k) {
+      const bool p = (pass >> k) & 1u;
+      const uint32_t bal = __ballot_sync(0xffffffffu, p);
+      if (bal != 0) {
+        if (p) {
+          const uint32_t q = (st.qh + st.nq + __popc(bal & ((1u << lane) - 1u))) & (TW_QUEUE - 1);
+          ws.qv[q] = v[k];
+          ws.qcol[q] = uint32_t(s0 + k) * TW_STEP + lane * TK_VEC;
+        }
+        st.nq += __popc(bal);  // < BATCH + 32 <= TW_QUEUE
+        if (st.nq >= uint32_t(C::BATCH)) {
+          __syncwarp();
+          do {
+            st = warp_drain<C>(ws, st, C::BATCH, V32, K, trig);
+          } while (st.nq >= uint32_t(C::BATCH));
         }
       }
     }
-    __syncthreads();  // the previous row's buffer is no longer read
-    sm.buf[threadIdx.x] = static_cast<unsigned long long>(tmax) << 32;
-    __syncthreads();
-    uint32_t count_ge = 0;
-    const uint32_t T0 = kth_largest_key(sm, TK_THREADS, uint32_t(K), count_ge);  // ends with a barrier
-    // each warp keeps, in its own region, the quick-start elements that reach T0
-    uint32_t cnt = 0;
+  }
+}
+
+template <class C, bool WITH_LSE>
+__global__ void __launch_bounds__(C::WARPS * 32, 1)
+    kd_topk_warp_kernel(const uint16_t* __restrict__ X, int64_t N, int64_t V, int64_t ld, int K,
+                        int32_t* __restrict__ ids_out, float* __restrict__ vals_out, float* __restrict__ lse_out) {
+  extern __shared__ __align__(16) uint8_t tkw_smem_raw[];
+  const uint32_t lane = lane_id();
+  TopkWarpSmem<C::CAP>& ws = reinterpret_cast<TopkWarpSmem<C::CAP>*>(tkw_smem_raw)[threadIdx.x >> 5];
+  const int64_t nwarps = int64_t(gridDim.x) * C::WARPS;
+  const int nst = int((V + TW_STEP - 1) / TW_STEP);
+  const int nsp = (nst + TW_PIPE - 1) / TW_PIPE * TW_PIPE;  // the next row starts in slot 0
+  const uint32_t V32 = uint32_t(V), Ku = uint32_t(K);
+  const uint32_t trig = 2u * Ku + 64u;
+  // steps whose 16 bytes are whole for this lane
+  const int64_t rem = V - 8 - int64_t(lane) * TK_VEC;
+  const int lane_full = rem >= 0 ? int(rem / TW_STEP) + 1 : 0;
+
+  int64_t row = int64_t(blockIdx.x) * C::WARPS + (threadIdx.x >> 5);
+  uint4 pipe[TW_PIPE];
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
+  for (int j = 0; j < TW_PIPE; ++j)
+    if (row < N && j < nst) pipe[j] = load_step(X + row * ld, V, j);
+
+  for (; row < N; row += nwarps) {
+    const uint16_t* xr = X + row * ld;
+    const uint16_t* xn = (row + nwarps < N) ? X + (row + nwarps) * ld : nullptr;
+    WarpSel st;
+    st.cnt = 0;
+    st.qh = 0;
+    st.nq = 0;
+    st.wth = 0;
+    st.ge = true;
+    st.tv = key_to_float(0);
+    float lm = -INFINITY, ls = 0.f;
+
+    // Main part: a group is tested, then its slots are refilled with the steps
+    // TW_PIPE further on, all of this row.
+    const int nmain = nst > TW_PIPE ? (nst - TW_PIPE) / TW_PIPE * TW_PIPE : 0;
+    const uint4* lp = reinterpret_cast<const uint4*>(xr) + lane;
+    for (int base = 0; base < nmain; base += TW_PIPE) {
+      const uint4* pb = lp + int64_t(base + TW_PIPE) * 32;
 #pragma unroll
-      for (int e = 0; e < TK_VEC; ++e) {
-        const uint32_t key = h ? kb[e] : ka[e];
-        const uint32_t idx = (h ? i0b : i0a) + e;
-        const bool take = idx < V32 && key >= T0;
-        const uint32_t bal = __ballot_sync(0xffffffffu, take);
-        if (take)
-          reg[cnt + __popc(bal & ((1u << lane) - 1u))] = (static_cast<unsigned long long>(key) << 32) | uint32_t(~idx);
-        cnt += __popc(bal);
+      for (int g = 0; g < TW_PIPE; g += TW_GROUP) {
+        test_group<C, WITH_LSE>(ws, st, pipe + g, base + g, (1u << TW_GROUP) - 1u, lm, ls, V32, Ku, trig);
+#pragma unroll
+        for (int k = 0; k < TW_GROUP; ++k) {
+          const int j = g + k;
+          pipe[j] = (base + j + TW_PIPE < lane_full) ? __ldcs(pb + j * 32) : load_step(xr, V, base + j + TW_PIPE);
+        }
+      }
+    }
+    // Epilogue: the last steps, the padding up to a multiple of TW_PIPE, and the next
+    // row's first steps.
+    for (int base = nmain; base < nsp; base += TW_PIPE) {
+#pragma unroll
+      for (int g = 0; g < TW_PIPE; g += TW_GROUP) {
+        uint32_t live = 0;
+#pragma unroll
+        for (int k = 0; k < TW_GROUP; ++k)
+          if (base + g + k < nst) live |= 1u << k;
+        if (live) test_group<C, WITH_LSE>(ws, st, pipe + g, base + g, live, lm, ls, V32, Ku, trig);
+#pragma unroll
+        for (int k = 0; k < TW_GROUP; ++k) {
+          const int j = g + k, t = base + j + TW_PIPE;
+          if (t < nst) pipe[j] = load_step(xr, V, t);
+          else if (t >= nsp && xn != nullptr && t - nsp < nst) pipe[j] = load_step(xn, V, t - nsp);
+        }
       }
     }
     __syncwarp();
-    uint32_t wth = T0;  // this warp's later elements need key > wth
-    float tv = key_to_float(T0);
-    auto compact_region = [&]() {
-      uint32_t cge = 0;
-      const uint32_t T = warp_kth_largest(reg, cnt, uint32_t(K), fs.whist[warp], cge);
-      if (cge <= uint32_t(TF_MAXK)) {
-        cnt = warp_filter_ge(reg, cnt, T);
-        wth = T;
-      } else {  // many ties at T: keep exactly the K best
-        warp_sort_desc(reg, cnt);
-        cnt = uint32_t(K);
-        wth = comp_key(reg[K - 1]);
-      }
-      tv = key_to_float(wth);
-    };
-    if (cnt > uint32_t(TF_MAXK)) compact_region();
-    if (TK_PIPE < nseg) pipe[0] = load_seg(xr, V, TK_PIPE);
-    if (TK_PIPE + 1 < nseg) pipe[1] = load_seg(xr, V, TK_PIPE + 1);
+    while (st.nq > 0) st = warp_drain<C>(ws, st, min(st.nq, uint32_t(C::BATCH)), V32, Ku, trig);
 
-    // streaming: no block barrier from here to the end of the row
-    for (int base = 0; base < nseg; base += TK_PIPE) {
-#pragma unroll
-      for (int j = 0; j < TK_PIPE; ++j) {
-        const int seg = base + j;
-        if (seg >= 2 && seg < nseg) {
-          const uint4 v = pipe[j];
-          if (seg + TK_PIPE < nseg) pipe[j] = load_seg(xr, V, seg + TK_PIPE);
-          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-          const uint32_t i0 = uint32_t(seg) * TK_SEG + threadIdx.x * TK_VEC;
-          float xf[TK_VEC];
-#pragma unroll
-          for (int e = 0; e < TK_VEC; ++e)
-            xf[e] = __uint_as_float((e & 1) ? (w[e >> 1] & 0xFFFF0000u) : (w[e >> 1] << 16));
-          if (lse_out != nullptr) {
-            float vm = -INFINITY;
-            float x2[TK_VEC];
-#pragma unroll
-            for (int e = 0; e < TK_VEC; ++e) {
-              x2[e] = (i0 + e < V32) ? xf[e] * 1.4426950408889634f : -INFINITY;
-              vm = fmaxf(vm, x2[e]);
-            }
-            const float nm = fmaxf(lm, vm);
-            if (nm != -INFINITY) {
-              float acc = ls * ex2_approx(lm - nm);
-#pragma unroll
-              for (int e = 0; e < TK_VEC; ++e) acc += ex2_approx(x2[e] - nm);
-              ls = acc;
-              lm = nm;
-            }
-          }
-          uint32_t take = 0;
-#pragma unroll
-          for (int e = 0; e < TK_VEC; ++e) {
-            if (!(xf[e] <= tv) && i0 + e < V32) {
-              const uint32_t key = bf16_key(w[e >> 1] >> (16 * (e & 1)));
-              if (key > wth) take |= 1u << e;
-            }
-          }
-          if (__any_sync(0xffffffffu, take != 0)) {
-#pragma unroll
-            for (int e = 0; e < TK_VEC; ++e) {
-              const bool t = (take >> e) & 1u;
-              const uint32_t bal = __ballot_sync(0xffffffffu, t);
-              if (t) {
-                const uint32_t key = bf16_key(w[e >> 1] >> (16 * (e & 1)));
-                reg[cnt + __popc(bal & ((1u << lane) - 1u))] =
-                    (static_cast<unsigned long long>(key) << 32) | uint32_t(~(i0 + e));
-              }
-              cnt += __popc(bal);
-            }
-            __syncwarp();
-            if (cnt > uint32_t(TF_MAXK)) compact_region();
-          }
-        }
-      }
-    }
-
-    // row end.  The highest warp threshold G is reached by at least K entries of that
-    // warp's region, so every entry of the top K has key >= G: drop the rest per warp,
-    // then gather the regions into one contiguous buffer and select as above.
-    if (lane == 0) fs.wcount[warp] = wth;
-    __syncthreads();
-    uint32_t G = 0;
-    for (uint32_t w = 0; w < uint32_t(TF_WARPS); ++w) G = max(G, fs.wcount[w]);
-    __syncthreads();
-    if (G > wth) cnt = warp_filter_ge(reg, cnt, G);
-    if (lane == 0) fs.wcount[warp] = cnt;
-    unsigned long long held[TF_WCAP / 32];
-#pragma unroll
-    for (int j = 0; j < TF_WCAP / 32; ++j) {
-      const uint32_t i = lane + 32u * j;
-      held[j] = i < cnt ? reg[i] : 0ull;
-    }
-    __syncthreads();
-    uint32_t off = 0, total = 0;
-    for (uint32_t w = 0; w < uint32_t(TF_WARPS); ++w) {
-      const uint32_t c = fs.wcount[w];
-      if (w < warp) off += c;
-      total += c;
-    }
-    if (lse_out != nullptr) {
+    if (WITH_LSE) {
       for (int o = 16; o > 0; o >>= 1) {
         const float om = __shfl_xor_sync(0xffffffffu, lm, o);
         const float os = __shfl_xor_sync(0xffffffffu, ls, o);
         const float nm = fmaxf(lm, om);
         if (nm != -INFINITY) {
-          ls = ls * ex2_approx(lm - nm) + os * ex2_approx(om - nm);
+          ls = ls * ex2_approx((lm - nm) * TW_LOG2E) + os * ex2_approx((om - nm) * TW_LOG2E);
           lm = nm;
         }
       }
-      if (lane == 0) {
-        sm.red_m[warp] = lm;
-        sm.red_s[warp] = ls;
-      }
+      if (lane == 0) lse_out[row] = lm + log2f(ls) * 0.69314718055994531f;
     }
-    __syncthreads();  // every region is in registers, counts and lse partials are published
-#pragma unroll
-    for (int j = 0; j < TF_WCAP / 32; ++j) {
-      const uint32_t i = lane + 32u * j;
-      if (i < cnt) sm.buf[off + i] = held[j];
-    }
-    if (threadIdx.x == 0) {
-      sm.count = total;
-      if (lse_out != nullptr) {
-        float M = -INFINITY, S = 0.f;
-        for (int i = 0; i < TF_WARPS; ++i) {
-          const float nm = fmaxf(M, sm.red_m[i]);
-          if (nm != -INFINITY) {
-            S = S * exp2f(M - nm) + sm.red_s[i] * exp2f(sm.red_m[i] - nm);
-            M = nm;
-          }
-        }
-        lse_out[row] = (M + log2f(S)) * 0.69314718055994531f;
-      }
-    }
-    __syncthreads();
-    uint32_t count = total;
-    if (count > uint32_t(K)) {
-      uint32_t cge = 0;
-      const uint32_t T = kth_largest_key(sm, count, uint32_t(K), cge);
-      if (cge < count) filter_ge(sm, count, T);
-      __syncthreads();
-      count = sm.count;
-      __syncthreads();
-    }
-    sort_desc(sm, count);
-    for (int j = threadIdx.x; j < K; j += TK_THREADS) {
-      const uint32_t col = ~uint32_t(sm.buf[j]);
-      ids_out[row * K + j] = int32_t(col);
-      vals_out[row * K + j] = __uint_as_float(uint32_t(xr[col]) << 16);
-    }
+    warp_finish<C>(ws, st.cnt, Ku, xr, ids_out + row * K, vals_out + row * K);
+    __syncwarp();
   }
+}
+
+template <class C>
+cudaError_t launch_topk_warp(const uint16_t* X, int64_t N, int64_t V, int64_t ld, int K, int32_t* ids, float* vals,
+                             float* lse, cudaStream_t s) {
+  static bool attr = false;
+  const int smem = int(C::WARPS * sizeof(TopkWarpSmem<C::CAP>));
+  if (!attr) {
+    cudaError_t e =
+        cudaFuncSetAttribute(kd_topk_warp_kernel<C, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(kd_topk_warp_kernel<C, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  int grid = gemm_max_grid();  // one block of C::WARPS row-streaming warps per SM
+  if (int64_t(grid) * C::WARPS > N) grid = int((N + C::WARPS - 1) / C::WARPS);
+  if (lse) kd_topk_warp_kernel<C, true><<<grid, C::WARPS * 32, smem, s>>>(X, N, V, ld, K, ids, vals, lse);
+  else kd_topk_warp_kernel<C, false><<<grid, C::WARPS * 32, smem, s>>>(X, N, V, ld, K, ids, vals, lse);
+  return cudaSuccess;
 }
 
 cudaError_t launch_topk(const uint16_t* X, int64_t N, int64_t V, int64_t ld, int K, int32_t* ids, float* vals,
@@ -808,15 +912,12 @@ cudaError_t launch_topk(const uint16_t* X, int64_t N, int64_t V, int64_t ld, int
   if (int64_t(grid) > N) grid = int(N);
   if (grid <= 0) return cudaSuccess;
   prof_before("kd_topk_cache", s);
-  if (K <= TF_MAXK && V > int64_t(TK_SEG)) {
-    static bool fast_attr = false;
-    const int fsmem = int(sizeof(TopkFastSmem));
-    if (!fast_attr) {
-      cudaError_t e = cudaFuncSetAttribute(kd_topk_fast_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, fsmem);
-      if (e != cudaSuccess) return e;
-      fast_attr = true;
-    }
-    kd_topk_fast_kernel<<<grid, TK_THREADS, fsmem, s>>>(X, N, V, ld, K, ids, vals, lse);
+  if (K <= TwSmallK::MAXK) {
+    cudaError_t e = launch_topk_warp<TwSmallK>(X, N, V, ld, K, ids, vals, lse, s);
+    if (e != cudaSuccess) return e;
+  } else if (K <= TwLargeK::MAXK) {
+    cudaError_t e = launch_topk_warp<TwLargeK>(X, N, V, ld, K, ids, vals, lse, s);
+    if (e != cudaSuccess) return e;
   } else {
     kd_topk_kernel<<<grid, TK_THREADS, smem, s>>>(X, N, V, ld, K, ids, vals, lse);
   }

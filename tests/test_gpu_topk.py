@@ -56,6 +56,15 @@ def test_topk_random(kd, cuda_device, N, V, K):
     _check(kd, X, K, cuda_device)
 
 
+@pytest.mark.parametrize("N,V,K", [(700, 4097, 100), (650, 12289, 7), (610, 20483, 256), (400, 33333, 100)])
+def test_topk_many_rows_per_block(kd, cuda_device, N, V, K):
+    """More rows than resident blocks (each block streams several rows, loading the next
+    row's first segments while it sorts the current one), 2 to 9 segments per row with a
+    ragged last segment, K up to the streaming path's limit."""
+    X = make_dense_teacher_logits(N, V, seed=N * 7 + K)
+    _check(kd, X, K, cuda_device)
+
+
 def test_topk_ties_and_signed_zero(kd, cuda_device):
     g = torch.Generator().manual_seed(1)
     N, V = 12, 20000
