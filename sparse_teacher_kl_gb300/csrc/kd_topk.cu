@@ -425,25 +425,27 @@ __global__ void __launch_bounds__(TK_THREADS, 2)
 // ---------------------------------------------------------------------------
 // Warp-per-row path for K <= TW_MAXK (the pages' top-100 cache).  The same selection,
 // run by one warp per row so that no block barrier is ever taken:
-//  * a lane reads 16 bytes per step (256 elements per warp step), TW_PIPE steps ahead,
-//    and the next row's first steps while it finishes the current row;
-//  * its 8 values are tested with one packed bf16 max against the warp's threshold,
-//    TW_GROUP steps at a time with one vote;
-//    a vector that passes is queued whole in shared memory, and the warp filters the
-//    queue 32 vectors at a time (one vector per lane) with the exact keys;
+//  * the copy engine streams the row: each warp owns a ring of RING slots of GRP warp
+//    steps (a step is 256 elements, 16 bytes per lane); lane 0 fills a slot with one bulk
+//    copy completing on the slot's mbarrier, RING groups ahead of its use, running on
+//    into the warp's next row while the current one is finished;
+//  * quick start: when a row begins, the ring holds its first RING x GRP steps; the K-th
+//    largest of their 8-element vector maxima is reached by at least K elements, so it
+//    is a first threshold (key >= it) before any element is kept;
+//  * each lane tests its 8 values with one packed bf16 max against the threshold, GRP
+//    steps at a time with one vote; a vector that passes is queued whole in shared
+//    memory, and the warp filters BATCH queued vectors at a time (one per lane) with
+//    exact comparisons;
 //  * the candidate buffer is compacted by the warp (two byte histograms) once it holds
 //    more than 2K + 64 entries, raising the threshold to the K-th largest key seen so
 //    far: one warp sees the whole row, so the threshold is as tight as the prefix allows.
-// Until the first compaction every element is a candidate (key >= 0).  Elements past V
-// read as -inf and are dropped by their column.
+// Elements past V read as -inf and are dropped by their column.
 
 constexpr int TW_MAXK = 256;
 constexpr int TW_STEP = 32 * TK_VEC;         // elements per warp step
-constexpr int TW_PIPE = 8;                   // steps in flight per warp (registers)
 constexpr int TW_GROUP = 4;                  // steps tested together (one vote)
 constexpr int TW_QUEUE = 64;                 // queued vectors per warp (ring)
 constexpr float TW_LOG2E = 1.4426950408889634f;
-static_assert(TW_PIPE % TW_GROUP == 0, "groups tile the pipeline");
 
 // A configuration: CAP candidate entries per warp, WARPS rows in flight per block (one
 // block per SM), BATCH queued vectors filtered per drain (at most 8 * BATCH new entries).
@@ -459,8 +461,6 @@ struct TwCfg {
   static_assert((CAP & (CAP - 1)) == 0, "the bitonic sort pads to a power of two within the buffer");
   static_assert(BATCH <= 32 && BATCH + 32 <= TW_QUEUE, "one vector per lane; the queue holds a batch and a step");
 };
-using TwSmallK = TwCfg<512, 20, 16>;   // K <= 160
-using TwLargeK = TwCfg<1024, 16, 32>;  // K <= 256
 
 template <int CAP>
 struct TopkWarpSmem {
@@ -586,8 +586,8 @@ __device__ void warp_sort_desc(unsigned long long* reg, uint32_t cnt) {
   }
 }
 
-// 16 bytes of warp step `st` for this lane; elements past V read as -inf.  Out of
-// line: only the ragged end of a row and the next row's first steps come here.
+// 16 bytes of warp step `st` for this lane, read directly; elements past V read as -inf.
+// Out of line: only the lanes at the ragged end of a row come here.
 __device__ __noinline__ uint4 load_step(const uint16_t* xr, int64_t V, int st) {
   const int64_t i0 = int64_t(st) * TW_STEP + int64_t(lane_id()) * TK_VEC;
   if (i0 + TK_VEC <= V) return __ldcs(reinterpret_cast<const uint4*>(xr + i0));
@@ -625,8 +625,8 @@ struct WarpSel {
   uint32_t qh;    // queue head (ring index of the oldest queued vector)
   uint32_t nq;    // queued vectors
   uint32_t wth;   // threshold key
-  bool ge;        // before the first compaction: key >= wth (= 0, every element) is a candidate
-  float tv;       // float value of wth, for the pre-tests
+  bool ge;        // before the first compaction: key >= wth is a candidate (wth = 0: every element)
+  float tv;       // pre-test bound: a vector can hold a candidate only if its maximum is > tv
 };
 
 // Warp: raise the threshold to the K-th largest key in the buffer and drop what
@@ -649,8 +649,9 @@ __device__ __forceinline__ void warp_compact(TopkWarpSmem<C::CAP>& ws, WarpSel& 
 }
 
 // Warp: filter the nb (<= BATCH) oldest queued vectors, one per lane.  For values other
-// than NaN, key(x) > wth exactly when x > tv (-0 and +0 have one key), so the test is a
-// float compare; a vector holding a NaN takes the key path.  Out of line: it runs once
+// than NaN, key(x) > wth exactly when x > value(wth) (-0 and +0 have one key), and the
+// same for >=, so the test is a float compare; a vector holding a NaN, or a threshold
+// key that is a NaN pattern, takes the key path.  Out of line: it runs once
 // per BATCH queued vectors, and one copy of it (and of the compaction) keeps the
 // streaming loop small in the instruction cache.
 template <class C>
@@ -666,18 +667,22 @@ __device__ __noinline__ WarpSel warp_drain(TopkWarpSmem<C::CAP>& ws, WarpSel st,
     lo = (static_cast<unsigned long long>(v.y) << 32) | v.x;
     hi = (static_cast<unsigned long long>(v.w) << 32) | v.z;
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    if (st.ge) {
-      take = 0xFFu;  // every element (the threshold key is 0)
-    } else if (vec_max(v) == vec_max(v)) {
+    const float t = key_to_float(st.wth);
+    if (st.ge && st.wth == 0) {
+      take = 0xFFu;  // every element
+    } else if (vec_max(v) == vec_max(v) && t == t) {
 #pragma unroll
       for (int h = 0; h < 4; ++h) {
-        if (__uint_as_float(w[h] << 16) > st.tv) take |= 1u << (2 * h);
-        if (__uint_as_float(w[h] & 0xFFFF0000u) > st.tv) take |= 2u << (2 * h);
+        const float a = __uint_as_float(w[h] << 16), b = __uint_as_float(w[h] & 0xFFFF0000u);
+        if (st.ge ? a >= t : a > t) take |= 1u << (2 * h);
+        if (st.ge ? b >= t : b > t) take |= 2u << (2 * h);
       }
     } else {
 #pragma unroll
-      for (int e = 0; e < TK_VEC; ++e)
-        if (bf16_key(w[e >> 1] >> (16 * (e & 1))) > st.wth) take |= 1u << e;
+      for (int e = 0; e < TK_VEC; ++e) {
+        const uint32_t key = bf16_key(w[e >> 1] >> (16 * (e & 1)));
+        if (st.ge ? key >= st.wth : key > st.wth) take |= 1u << e;
+      }
     }
     if (col0 + TK_VEC > V32) take &= (V32 > col0 ? (1u << (V32 - col0)) - 1u : 0u);
   }
@@ -723,19 +728,32 @@ __device__ __noinline__ void warp_finish(TopkWarpSmem<C::CAP>& ws, uint32_t cnt,
   }
 }
 
-// Adds the 8 values of v to a running sum of 2^((x - lm) log2 e), b = lm log2 e.
+// Sum over the 8 values x of v of 2^(x log2 e - b), b = lm log2 e: each word's pair of
+// values goes through one packed f32x2 multiply-add and one packed add.
 __device__ __forceinline__ float lse_terms(const uint4& v, float b) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-  float acc = 0.f;
+  unsigned long long l2e2, nb2, acc;
+  asm("mov.b64 %0, {%1, %1};" : "=l"(l2e2) : "r"(__float_as_uint(TW_LOG2E)));
+  asm("mov.b64 %0, {%1, %1};" : "=l"(nb2) : "r"(__float_as_uint(-b)));
+  asm("mov.b64 %0, {%1, %1};" : "=l"(acc) : "r"(0u));
 #pragma unroll
   for (int h = 0; h < 4; ++h) {
-    acc += ex2_approx(fmaf(__uint_as_float(w[h] << 16), TW_LOG2E, -b));
-    acc += ex2_approx(fmaf(__uint_as_float(w[h] & 0xFFFF0000u), TW_LOG2E, -b));
+    unsigned long long x, t, e;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "r"(w[h] << 16), "r"(w[h] & 0xFFFF0000u));
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(t) : "l"(x), "l"(l2e2), "l"(nb2));
+    uint32_t t0, t1;
+    asm("mov.b64 {%0, %1}, %2;" : "=r"(t0), "=r"(t1) : "l"(t));
+    asm("mov.b64 %0, {%1, %2};"
+        : "=l"(e)
+        : "r"(__float_as_uint(ex2_approx(__uint_as_float(t0)))), "r"(__float_as_uint(ex2_approx(__uint_as_float(t1)))));
+    asm("add.rn.f32x2 %0, %0, %1;" : "+l"(acc) : "l"(e));
   }
-  return acc;
+  uint32_t a0, a1;
+  asm("mov.b64 {%0, %1}, %2;" : "=r"(a0), "=r"(a1) : "l"(acc));
+  return __uint_as_float(a0) + __uint_as_float(a1);
 }
 
-// One group of TW_GROUP steps of a lane, vectors pipe[g0 ..]: the packed pre-test of each
+// One group of TW_GROUP steps of a lane, vectors v[0 ..]: the packed pre-test of each
 // against the warp's threshold (st.tv is NaN before the first compaction: all pass), one
 // vote for the group, and, when a vector passed, its queueing and a drain every BATCH
 // queued.  s0 = the group's first step; `live` = the group's steps that exist.
@@ -790,31 +808,95 @@ __device__ __forceinline__ void test_group(TopkWarpSmem<C::CAP>& ws, WarpSel& st
   }
 }
 
+// Ring feeding: (RING - 1) x GRP x 512 bytes per warp stay in flight whatever the
+// register schedule.  A row's last group copies whole 16-byte vectors only; the one lane
+// whose vector straddles the end of the row (and the lanes past it) read theirs directly.
+
+template <int CAP_, int WARPS_, int BATCH_, int RING_, int GRP_>
+struct TmaCfg : TwCfg<CAP_, WARPS_, BATCH_> {
+  static constexpr int RING = RING_;
+  static constexpr int GRP = GRP_;
+  static_assert(GRP == TW_GROUP, "a slot is one tested group");
+  static_assert((RING & (RING - 1)) == 0, "slots wrap with a mask");
+};
+using TmSmallK = TmaCfg<512, 15, 24, 4, 4>;   // K <= 128
+using TmLargeK = TmaCfg<1024, 12, 32, 4, 4>;  // K <= 256
+
+template <class C>
+struct TopkTmaSmem {
+  uint4 ring[C::RING][C::GRP][32];
+  TopkWarpSmem<C::CAP> sel;
+  uint64_t full[C::RING];
+  uint32_t abort;  // set by a timed-out wait
+  uint32_t never;  // stays 0: the flag of the bounded waits after an abort
+};
+
+// Bulk copy global -> shared of `bytes` (a multiple of 16), completing on `bar`.
+// `after` is a value loaded from the slot's previous contents: as an operand it keeps
+// the copy behind that read.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                         uint32_t after) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "r"(after)
+      : "memory");
+}
+
 template <class C, bool WITH_LSE>
 __global__ void __launch_bounds__(C::WARPS * 32, 1)
-    kd_topk_warp_kernel(const uint16_t* __restrict__ X, int64_t N, int64_t V, int64_t ld, int K,
-                        int32_t* __restrict__ ids_out, float* __restrict__ vals_out, float* __restrict__ lse_out) {
-  extern __shared__ __align__(16) uint8_t tkw_smem_raw[];
+    kd_topk_tma_kernel(const uint16_t* __restrict__ X, int64_t N, int64_t V, int64_t ld, int K,
+                       int32_t* __restrict__ ids_out, float* __restrict__ vals_out, float* __restrict__ lse_out,
+                       uint32_t* err) {
+  extern __shared__ __align__(16) uint8_t tkt_smem_raw[];
+  constexpr int GSTEPS = C::GRP;
+  constexpr uint32_t GBYTES = uint32_t(C::GRP) * TW_STEP * 2;
   const uint32_t lane = lane_id();
-  TopkWarpSmem<C::CAP>& ws = reinterpret_cast<TopkWarpSmem<C::CAP>*>(tkw_smem_raw)[threadIdx.x >> 5];
+  TopkTmaSmem<C>& ts = reinterpret_cast<TopkTmaSmem<C>*>(tkt_smem_raw)[threadIdx.x >> 5];
+  TopkWarpSmem<C::CAP>& ws = ts.sel;
   const int64_t nwarps = int64_t(gridDim.x) * C::WARPS;
   const int nst = int((V + TW_STEP - 1) / TW_STEP);
-  const int nsp = (nst + TW_PIPE - 1) / TW_PIPE * TW_PIPE;  // the next row starts in slot 0
+  const int ngr = (nst + GSTEPS - 1) / GSTEPS;  // groups per row
   const uint32_t V32 = uint32_t(V), Ku = uint32_t(K);
   const uint32_t trig = 2u * Ku + 64u;
-  // steps whose 16 bytes are whole for this lane
-  const int64_t rem = V - 8 - int64_t(lane) * TK_VEC;
-  const int lane_full = rem >= 0 ? int(rem / TW_STEP) + 1 : 0;
+  // this lane's vector in a row's last step is not a whole 16 bytes inside the row
+  const bool tail_lane = int64_t(nst - 1) * TW_STEP + int64_t(lane) * TK_VEC + TK_VEC > V;
+
+  if (lane == 0) {
+    for (int r = 0; r < C::RING; ++r) mbar_init(&ts.full[r], 1);
+    ts.abort = 0;
+    ts.never = 0;
+    fence_mbar_init();
+  }
+  __syncwarp();
 
   int64_t row = int64_t(blockIdx.x) * C::WARPS + (threadIdx.x >> 5);
-  uint4 pipe[TW_PIPE];
-#pragma unroll
-  for (int j = 0; j < TW_PIPE; ++j)
-    if (row < N && j < nst) pipe[j] = load_step(X + row * ld, V, j);
+  // Producer: the warp's rows one after another, group by group.
+  int64_t prow = row;
+  int pg = 0;
+  uint32_t issued = 0;
+  auto issue = [&](uint32_t slot, uint32_t after) {
+    if (prow < N) {
+      if (lane == 0) {
+        const int64_t e0 = int64_t(pg) * GSTEPS * TW_STEP;
+        const int64_t left = V - e0;
+        const uint32_t bytes = left >= int64_t(GSTEPS) * TW_STEP ? GBYTES : uint32_t(left * 2) & ~15u;
+        mbar_arrive_expect_tx(&ts.full[slot], bytes);
+        if (bytes != 0) bulk_g2s(&ts.ring[slot][0][0], X + prow * ld + e0, bytes, &ts.full[slot], after);
+      }
+      ++issued;
+      if (++pg == ngr) {
+        pg = 0;
+        prow += nwarps;
+      }
+    }
+  };
+  for (int r = 0; r < C::RING; ++r) issue(uint32_t(r), 0u);
 
+  uint32_t gidx = 0;  // groups consumed
+  bool ok = true;
   for (; row < N; row += nwarps) {
     const uint16_t* xr = X + row * ld;
-    const uint16_t* xn = (row + nwarps < N) ? X + (row + nwarps) * ld : nullptr;
     WarpSel st;
     st.cnt = 0;
     st.qh = 0;
@@ -824,40 +906,71 @@ __global__ void __launch_bounds__(C::WARPS * 32, 1)
     st.tv = key_to_float(0);
     float lm = -INFINITY, ls = 0.f;
 
-    // Main part: a group is tested, then its slots are refilled with the steps
-    // TW_PIPE further on, all of this row.
-    const int nmain = nst > TW_PIPE ? (nst - TW_PIPE) / TW_PIPE * TW_PIPE : 0;
-    const uint4* lp = reinterpret_cast<const uint4*>(xr) + lane;
-    for (int base = 0; base < nmain; base += TW_PIPE) {
-      const uint4* pb = lp + int64_t(base + TW_PIPE) * 32;
+    // Quick start: the ring holds this row's first RING groups (none of them the row's
+    // last).  The K-th largest of their per-lane vector maxima is reached by at least K
+    // elements, so every element of the top K has a key >= it: those groups are then
+    // consumed with that threshold (>=), and the rest of the row with the raised ones.
+    if (ngr > C::RING && K <= C::RING * C::GRP * 32) {
+      for (int r = 0; r < C::RING && ok; ++r) {
+        const uint32_t u = gidx + uint32_t(r);
+        ok = mbar_wait(&ts.full[u & (C::RING - 1)], (u / C::RING) & 1u, &ts.abort, err, 0x72u);
+      }
+      if (!ok) break;
 #pragma unroll
-      for (int g = 0; g < TW_PIPE; g += TW_GROUP) {
-        test_group<C, WITH_LSE>(ws, st, pipe + g, base + g, (1u << TW_GROUP) - 1u, lm, ls, V32, Ku, trig);
+      for (int r = 0; r < C::RING; ++r) {
 #pragma unroll
-        for (int k = 0; k < TW_GROUP; ++k) {
-          const int j = g + k;
-          pipe[j] = (base + j + TW_PIPE < lane_full) ? __ldcs(pb + j * 32) : load_step(xr, V, base + j + TW_PIPE);
+        for (int k = 0; k < C::GRP; ++k) {
+          const uint4 v = ts.ring[(gidx + r) & (C::RING - 1)][k][lane];
+          const float m = vec_max(v);
+          uint32_t key;
+          if (m == m) {
+            key = bf16_key(__float_as_uint(m) >> 16);
+          } else {  // a NaN hides the maximum: take the exact keys
+            key = 0;
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int h = 0; h < 4; ++h) key = max(key, max(bf16_key(w[h]), bf16_key(w[h] >> 16)));
+          }
+          ws.buf[(r * C::GRP + k) * 32 + lane] = static_cast<unsigned long long>(key) << 32;
         }
       }
-    }
-    // Epilogue: the last steps, the padding up to a multiple of TW_PIPE, and the next
-    // row's first steps.
-    for (int base = nmain; base < nsp; base += TW_PIPE) {
-#pragma unroll
-      for (int g = 0; g < TW_PIPE; g += TW_GROUP) {
-        uint32_t live = 0;
-#pragma unroll
-        for (int k = 0; k < TW_GROUP; ++k)
-          if (base + g + k < nst) live |= 1u << k;
-        if (live) test_group<C, WITH_LSE>(ws, st, pipe + g, base + g, live, lm, ls, V32, Ku, trig);
-#pragma unroll
-        for (int k = 0; k < TW_GROUP; ++k) {
-          const int j = g + k, t = base + j + TW_PIPE;
-          if (t < nst) pipe[j] = load_step(xr, V, t);
-          else if (t >= nsp && xn != nullptr && t - nsp < nst) pipe[j] = load_step(xn, V, t - nsp);
-        }
+      __syncwarp();
+      uint32_t cge = 0;
+      const uint32_t T0 = warp_kth_largest(ws.buf, uint32_t(C::RING * C::GRP * 32), Ku, ws.hist, cge);
+      if (T0 != 0) {
+        st.wth = T0;
+        // pre-test bound just below value(T0) (the -0/+0 key is 0x8000: step past -0)
+        st.tv = key_to_float(T0 - 1u == 0x7FFFu ? 0x7FFEu : T0 - 1u);
       }
     }
+
+    for (int g = 0; g < ngr; ++g, ++gidx) {
+      const uint32_t slot = gidx & (C::RING - 1);
+      if (!mbar_wait(&ts.full[slot], (gidx / C::RING) & 1u, &ts.abort, err, 0x70u)) {
+        ok = false;
+        break;
+      }
+      uint4 v[GSTEPS];
+#pragma unroll
+      for (int k = 0; k < GSTEPS; ++k) v[k] = ts.ring[slot][k][lane];
+      const int s0 = g * GSTEPS;
+      uint32_t live = (1u << GSTEPS) - 1u;
+      if (g == ngr - 1) {  // the row's last group
+        live = nst - s0 >= GSTEPS ? live : (1u << (nst - s0)) - 1u;
+        if (tail_lane) {
+#pragma unroll
+          for (int k = 0; k < GSTEPS; ++k)
+            if (s0 + k == nst - 1) v[k] = load_step(xr, V, nst - 1);
+        }
+      }
+      uint32_t after = 0;
+#pragma unroll
+      for (int k = 0; k < GSTEPS; ++k) after ^= v[k].x;
+      __syncwarp();  // every lane has read the slot
+      issue(slot, after);
+      test_group<C, WITH_LSE>(ws, st, v, s0, live, lm, ls, V32, Ku, trig);
+    }
+    if (!ok) break;
     __syncwarp();
     while (st.nq > 0) st = warp_drain<C>(ws, st, min(st.nq, uint32_t(C::BATCH)), V32, Ku, trig);
 
@@ -876,31 +989,34 @@ __global__ void __launch_bounds__(C::WARPS * 32, 1)
     warp_finish<C>(ws, st.cnt, Ku, xr, ids_out + row * K, vals_out + row * K);
     __syncwarp();
   }
+  if (!ok) {  // a wait timed out: let this warp's copies still in flight land (bounded) before leaving
+    for (uint32_t u = gidx; u < issued; ++u)
+      mbar_wait(&ts.full[u & (C::RING - 1)], (u / C::RING) & 1u, &ts.never, err, 0x71u, 10000000ull);
+  }
 }
 
 template <class C>
-cudaError_t launch_topk_warp(const uint16_t* X, int64_t N, int64_t V, int64_t ld, int K, int32_t* ids, float* vals,
-                             float* lse, cudaStream_t s) {
+cudaError_t launch_topk_tma(const uint16_t* X, int64_t N, int64_t V, int64_t ld, int K, int32_t* ids, float* vals,
+                            float* lse, uint32_t* err, cudaStream_t s) {
   static bool attr = false;
-  const int smem = int(C::WARPS * sizeof(TopkWarpSmem<C::CAP>));
+  const int smem = int(C::WARPS * sizeof(TopkTmaSmem<C>));
   if (!attr) {
     cudaError_t e =
-        cudaFuncSetAttribute(kd_topk_warp_kernel<C, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        cudaFuncSetAttribute(kd_topk_tma_kernel<C, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(kd_topk_warp_kernel<C, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      e = cudaFuncSetAttribute(kd_topk_tma_kernel<C, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     attr = true;
   }
   int grid = gemm_max_grid();  // one block of C::WARPS row-streaming warps per SM
   if (int64_t(grid) * C::WARPS > N) grid = int((N + C::WARPS - 1) / C::WARPS);
-  if (lse) kd_topk_warp_kernel<C, true><<<grid, C::WARPS * 32, smem, s>>>(X, N, V, ld, K, ids, vals, lse);
-  else kd_topk_warp_kernel<C, false><<<grid, C::WARPS * 32, smem, s>>>(X, N, V, ld, K, ids, vals, lse);
+  if (lse) kd_topk_tma_kernel<C, true><<<grid, C::WARPS * 32, smem, s>>>(X, N, V, ld, K, ids, vals, lse, err);
+  else kd_topk_tma_kernel<C, false><<<grid, C::WARPS * 32, smem, s>>>(X, N, V, ld, K, ids, vals, lse, err);
   return cudaSuccess;
 }
 
 cudaError_t launch_topk(const uint16_t* X, int64_t N, int64_t V, int64_t ld, int K, int32_t* ids, float* vals,
                         float* lse, uint32_t* err, cudaStream_t s) {
-  (void)err;
   static bool attr_set = false;
   const int smem = int(sizeof(TopkSmem));
   if (!attr_set) {
@@ -912,11 +1028,11 @@ cudaError_t launch_topk(const uint16_t* X, int64_t N, int64_t V, int64_t ld, int
   if (int64_t(grid) > N) grid = int(N);
   if (grid <= 0) return cudaSuccess;
   prof_before("kd_topk_cache", s);
-  if (K <= TwSmallK::MAXK) {
-    cudaError_t e = launch_topk_warp<TwSmallK>(X, N, V, ld, K, ids, vals, lse, s);
+  if (K <= TmSmallK::MAXK) {
+    cudaError_t e = launch_topk_tma<TmSmallK>(X, N, V, ld, K, ids, vals, lse, err, s);
     if (e != cudaSuccess) return e;
-  } else if (K <= TwLargeK::MAXK) {
-    cudaError_t e = launch_topk_warp<TwLargeK>(X, N, V, ld, K, ids, vals, lse, s);
+  } else if (K <= TmLargeK::MAXK) {
+    cudaError_t e = launch_topk_tma<TmLargeK>(X, N, V, ld, K, ids, vals, lse, err, s);
     if (e != cudaSuccess) return e;
   } else {
     kd_topk_kernel<<<grid, TK_THREADS, smem, s>>>(X, N, V, ld, K, ids, vals, lse);

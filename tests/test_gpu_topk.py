@@ -56,11 +56,13 @@ def test_topk_random(kd, cuda_device, N, V, K):
     _check(kd, X, K, cuda_device)
 
 
-@pytest.mark.parametrize("N,V,K", [(700, 4097, 100), (650, 12289, 7), (610, 20483, 256), (400, 33333, 100)])
+@pytest.mark.parametrize("N,V,K", [(700, 4097, 100), (650, 12289, 7), (610, 20483, 256), (400, 33333, 100),
+                                   (257, 9000, 128), (333, 16411, 129)])
 def test_topk_many_rows_per_block(kd, cuda_device, N, V, K):
-    """More rows than resident blocks (each block streams several rows, loading the next
-    row's first segments while it sorts the current one), 2 to 9 segments per row with a
-    ragged last segment, K up to the streaming path's limit."""
+    """More rows than resident warps (each warp streams several rows, its copies running
+    on into the next row while it sorts the current one), rows of 17 to 131 warp steps with
+    a ragged end, K on both sides of the boundary between the two buffer sizes and at the
+    streaming path's limit."""
     X = make_dense_teacher_logits(N, V, seed=N * 7 + K)
     _check(kd, X, K, cuda_device)
 
