@@ -98,17 +98,19 @@ class ClockSampler:
 
 
 def ncu_traffic(kernel: str, workload: str):
-    """DRAM bytes per launch of ``kernel`` on ``workload`` from profiles/ncu_traffic.json,
-    or None when absent or taken from different kernel sources than the ones built now."""
+    """DRAM bytes (read + write) per launch of ``kernel`` on ``workload`` from
+    profiles/ncu_traffic.json, or None when absent or captured from other sources than the
+    ones built now (each record names the source files that define its kernel and their
+    digest at capture time)."""
     from sparse_teacher_kl_gb300.build import source_digest
     try:
         with open(os.path.join(ROOT, "profiles", "ncu_traffic.json")) as f:
-            rec = json.load(f)
+            rec = json.load(f)["kernels"][workload][kernel]
+        if rec["digest"] != source_digest(rec["sources"]):
+            return None
+        return rec["bytes_per_launch"]
     except Exception:
         return None
-    if rec.get("source_digest") != source_digest():
-        return None
-    return rec.get("kernels", {}).get(workload, {}).get(kernel)
 
 
 def bench_topk(kd, dev, stream, peaks, steps):
@@ -146,7 +148,7 @@ def bench_topk(kd, dev, stream, peaks, steps):
         out[name] = {"ms": ms, "achieved_gbs": gbs, "peak_gbs": peaks["hbm"], "frac": gbs / peaks["hbm"],
                      "bytes_per_launch": byts}
     out["roofline"] = {"bound": "hbm", "achieved": out["ids+vals"]["achieved_gbs"], "peak": peaks["hbm"],
-                       "unit": "GB/s", "frac": out["ids+vals"]["frac"],
+                       "unit": "GB/s", "frac": out["ids+vals"]["frac"], "traffic": ncu_traffic("kd_topk_cache", "mid"),
                        "peak_source": f"{peaks['source']} copy bandwidth"}
     del X
     torch.cuda.empty_cache()

@@ -46,11 +46,13 @@ def _digest(extra) -> str:
     return h.hexdigest()
 
 
-def source_digest() -> str:
-    """Digest of the CUDA sources and the public header (not of build flags): identifies
-    the kernels that an ncu capture was taken from."""
+def source_digest(files=None) -> str:
+    """Digest of CUDA sources (not of build flags): identifies the kernels that an ncu
+    capture was taken from.  ``files``: names under csrc/ to digest (default: all of them
+    and the public header)."""
     h = hashlib.sha256()
-    for f in sorted(os.listdir(CSRC)) + ["../../include/kdkl.h"]:
+    names = sorted(files) if files is not None else sorted(os.listdir(CSRC)) + ["../../include/kdkl.h"]
+    for f in names:
         path = os.path.normpath(os.path.join(CSRC, f))
         with open(path, "rb") as fh:
             h.update(os.path.basename(path).encode())
