@@ -436,9 +436,11 @@ __global__ void __launch_bounds__(TK_THREADS, 2)
 //    steps at a time with one vote; a vector that passes is queued whole in shared
 //    memory, and the warp filters BATCH queued vectors at a time (one per lane) with
 //    exact comparisons;
-//  * the candidate buffer is compacted by the warp (two byte histograms) once it holds
-//    more than 2K + 64 entries, raising the threshold to the K-th largest key seen so
-//    far: one warp sees the whole row, so the threshold is as tight as the prefix allows.
+//  * the warp keeps the row's best K so far as a sorted list and merges each drained
+//    batch into it (a bitonic sort across the lanes and a rank merge); once it holds K
+//    entries its last key is the threshold, exact after every drain: one warp sees the
+//    whole row, so the threshold is as tight as the prefix allows, and the list is the
+//    answer when the row ends.
 // Elements past V read as -inf and are dropped by their column.
 
 constexpr int TW_MAXK = 256;
@@ -448,17 +450,17 @@ constexpr int TW_QUEUE = 64;                 // queued vectors per warp (ring)
 constexpr float TW_LOG2E = 1.4426950408889634f;
 
 // A configuration: CAP candidate entries per warp, WARPS rows in flight per block (one
-// block per SM), BATCH queued vectors filtered per drain (at most 8 * BATCH new entries).
-// A compaction leaves at most KEEP entries and the trigger 2K + 64 stays within KEEP, so
-// a drain always fits.  The smaller buffer lets more warps share an SM.
-template <int CAP_, int WARPS_, int BATCH_>
+// block per SM), BATCH queued vectors filtered per drain (at most 8 * BATCH new
+// entries), MAXK the largest K it serves.  The top list (<= MAXK) and one drain's
+// entries fit in the buffer, and its bitonic sort pads to a power of two within it.
+template <int CAP_, int WARPS_, int BATCH_, int MAXK_>
 struct TwCfg {
   static constexpr int CAP = CAP_;
   static constexpr int WARPS = WARPS_;
   static constexpr int BATCH = BATCH_;
-  static constexpr int KEEP = CAP - 8 * BATCH;
-  static constexpr int MAXK = (KEEP - 64) / 2 < TW_MAXK ? (KEEP - 64) / 2 : TW_MAXK;
+  static constexpr int MAXK = MAXK_;
   static_assert((CAP & (CAP - 1)) == 0, "the bitonic sort pads to a power of two within the buffer");
+  static_assert(MAXK + 8 * BATCH <= CAP && MAXK <= TW_MAXK && MAXK % 32 == 0, "a drain fits after the list");
   static_assert(BATCH <= 32 && BATCH + 32 <= TW_QUEUE, "one vector per lane; the queue holds a batch and a step");
 };
 
@@ -625,38 +627,77 @@ struct WarpSel {
   uint32_t qh;    // queue head (ring index of the oldest queued vector)
   uint32_t nq;    // queued vectors
   uint32_t wth;   // threshold key
-  bool ge;        // before the first compaction: key >= wth is a candidate (wth = 0: every element)
+  bool ge;        // until the list holds K entries: key >= wth is a candidate (wth = 0: every element)
   float tv;       // pre-test bound: a vector can hold a candidate only if its maximum is > tv
 };
 
-// Warp: raise the threshold to the K-th largest key in the buffer and drop what
-// cannot reach the top K.
-template <class C>
-__device__ __forceinline__ void warp_compact(TopkWarpSmem<C::CAP>& ws, WarpSel& st, uint32_t K) {
-  uint32_t cge = 0;
-  const uint32_t T = warp_kth_largest(ws.buf, st.cnt, K, ws.hist, cge);
-  if (cge <= uint32_t(C::KEEP)) {
-    if (cge < st.cnt) st.cnt = warp_filter_ge(ws.buf, st.cnt, T);
-    st.wth = T;
-  } else {  // many ties at T: order fully and keep exactly the K best
-    warp_sort_desc(ws.buf, st.cnt);
-    st.cnt = K;
-    st.wth = comp_key(ws.buf[K - 1]);
-    __syncwarp();
+// Warp: merge the T (<= 32) unsorted candidates buf[nt, nt + T) into the top list
+// buf[0, nt) (sorted descending, nt <= K <= 32 * SLOTS), keeping the K best, in place:
+// the candidates are sorted across the lanes (bitonic, zeros last), every element's new
+// place is its index plus the number of elements of the other list above it (binary
+// searches; composites are unique), and nothing is written until everything is read.
+// Returns the new length, min(nt + T, K).
+template <int SLOTS>
+__device__ uint32_t warp_merge_top(unsigned long long* buf, uint32_t nt, uint32_t T, uint32_t K) {
+  const uint32_t lane = lane_id();
+  unsigned long long c = lane < T ? buf[nt + lane] : 0ull;
+#pragma unroll
+  for (uint32_t k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+    for (uint32_t j = k >> 1; j > 0; j >>= 1) {
+      const unsigned long long o = __shfl_xor_sync(0xffffffffu, c, j);
+      const bool desc = (lane & k) == 0;
+      const bool low = (lane & j) == 0;
+      c = (low == desc) ? (c > o ? c : o) : (c < o ? c : o);
+    }
   }
-  st.ge = false;
-  st.tv = key_to_float(st.wth);
+  // place of candidate `lane` (the lane-th largest): lane + #top entries above it
+  uint32_t lo = 0, hi = nt;
+  while (lo < hi) {
+    const uint32_t mid = (lo + hi) >> 1;
+    if (buf[mid] > c) lo = mid + 1; else hi = mid;
+  }
+  const uint32_t cpos = lane + lo;
+  __syncwarp();
+  if (lane < T) buf[nt + lane] = c;  // the candidates, sorted, for the searches below
+  __syncwarp();
+  unsigned long long tv[SLOTS];
+  uint32_t tpos[SLOTS];
+#pragma unroll
+  for (int m = 0; m < SLOTS; ++m) {
+    const uint32_t j = lane + 32u * m;
+    tv[m] = 0ull;
+    tpos[m] = K;
+    if (j < nt) {
+      tv[m] = buf[j];
+      uint32_t a = 0, b = T;  // #candidates above top[j]
+      while (a < b) {
+        const uint32_t mid = (a + b) >> 1;
+        if (buf[nt + mid] > tv[m]) a = mid + 1; else b = mid;
+      }
+      tpos[m] = j + a;
+    }
+  }
+  __syncwarp();
+  if (lane < T && cpos < K) buf[cpos] = c;
+#pragma unroll
+  for (int m = 0; m < SLOTS; ++m)
+    if (tpos[m] < K) buf[tpos[m]] = tv[m];
+  __syncwarp();
+  return nt + T < K ? nt + T : K;
 }
 
-// Warp: filter the nb (<= BATCH) oldest queued vectors, one per lane.  For values other
-// than NaN, key(x) > wth exactly when x > value(wth) (-0 and +0 have one key), and the
-// same for >=, so the test is a float compare; a vector holding a NaN, or a threshold
-// key that is a NaN pattern, takes the key path.  Out of line: it runs once
-// per BATCH queued vectors, and one copy of it (and of the compaction) keeps the
-// streaming loop small in the instruction cache.
+// Warp: filter the nb (<= BATCH) oldest queued vectors, one per lane, and merge what
+// passes into the top list.  For values other than NaN, key(x) > wth exactly when
+// x > value(wth) (-0 and +0 have one key), and the same for >=, so the test is a float
+// compare; a vector holding a NaN, or a threshold key that is a NaN pattern, takes the
+// key path.  Once the list holds K entries its last key is the threshold (later
+// elements need a larger key: an equal key comes with a larger column).  Out of line:
+// it runs once per BATCH queued vectors, and one copy of it keeps the streaming loop
+// small in the instruction cache.
 template <class C>
 __device__ __noinline__ WarpSel warp_drain(TopkWarpSmem<C::CAP>& ws, WarpSel st, uint32_t nb, uint32_t V32,
-                                           uint32_t K, uint32_t trig) {
+                                           uint32_t K) {
   const uint32_t lane = lane_id();
   uint32_t take = 0, col0 = 0;
   unsigned long long lo = 0, hi = 0;
@@ -696,35 +737,50 @@ __device__ __noinline__ WarpSel warp_drain(TopkWarpSmem<C::CAP>& ws, WarpSel st,
     pre += uint32_t(__popc(bb & lt)) << b;
     tot += uint32_t(__popc(bb)) << b;
   }
-  uint32_t pos = st.cnt + pre;
+  uint32_t pos = st.cnt + pre;  // after the top list
   while (take) {
     const uint32_t e = __ffs(take) - 1;
     take &= take - 1;
     const uint32_t bits = uint32_t(((e & 4) ? hi : lo) >> (16 * (e & 3))) & 0xFFFFu;
     ws.buf[pos++] = (static_cast<unsigned long long>(bf16_key(bits)) << 32) | uint32_t(~(col0 + e));
   }
-  st.cnt += tot;
   st.qh = (st.qh + nb) & (TW_QUEUE - 1);
   st.nq -= nb;
   __syncwarp();
-  if (st.cnt > trig) warp_compact<C>(ws, st, K);
+  if (tot == 0) return st;
+  if (tot <= 32) {
+    st.cnt = warp_merge_top<C::MAXK / 32>(ws.buf, st.cnt, tot, K);
+  } else {  // a large batch: select and sort the whole list
+    uint32_t cnt = st.cnt + tot;
+    if (cnt > K) {
+      uint32_t cge = 0;
+      const uint32_t T = warp_kth_largest(ws.buf, cnt, K, ws.hist, cge);
+      if (cge < cnt) cnt = warp_filter_ge(ws.buf, cnt, T);
+    }
+    warp_sort_desc(ws.buf, cnt);
+    st.cnt = cnt < K ? cnt : K;
+  }
+  if (st.cnt >= K) {
+    st.wth = comp_key(ws.buf[K - 1]);
+    st.ge = false;
+    st.tv = key_to_float(st.wth);
+  }
   return st;
 }
 
-// Warp: the exact top K of the candidates, in order, to the row's outputs.
-template <class C>
-__device__ __noinline__ void warp_finish(TopkWarpSmem<C::CAP>& ws, uint32_t cnt, uint32_t K, const uint16_t* xr,
+// Warp: the top list (sorted; K entries whenever V >= K) to the row's outputs; values
+// are read back from the row (exact bits, -0 kept).
+__device__ __noinline__ void warp_finish(const unsigned long long* top, uint32_t cnt, uint32_t K, const uint16_t* xr,
                                          int32_t* ids_row, float* vals_row) {
-  if (cnt > K) {
-    uint32_t cge = 0;
-    const uint32_t T = warp_kth_largest(ws.buf, cnt, K, ws.hist, cge);
-    if (cge < cnt) cnt = warp_filter_ge(ws.buf, cnt, T);
-  }
-  warp_sort_desc(ws.buf, cnt);
   for (uint32_t j = lane_id(); j < K; j += 32) {
-    const uint32_t col = ~uint32_t(ws.buf[j]);
-    ids_row[j] = int32_t(col);
-    vals_row[j] = __uint_as_float(uint32_t(xr[col]) << 16);
+    if (j < cnt) {
+      const uint32_t col = ~uint32_t(top[j]);
+      ids_row[j] = int32_t(col);
+      vals_row[j] = __uint_as_float(uint32_t(xr[col]) << 16);
+    } else {
+      ids_row[j] = -1;
+      vals_row[j] = -INFINITY;
+    }
   }
 }
 
@@ -754,13 +810,12 @@ __device__ __forceinline__ float lse_terms(const uint4& v, float b) {
 }
 
 // One group of TW_GROUP steps of a lane, vectors v[0 ..]: the packed pre-test of each
-// against the warp's threshold (st.tv is NaN before the first compaction: all pass), one
+// against the warp's threshold (st.tv is NaN while every element is a candidate), one
 // vote for the group, and, when a vector passed, its queueing and a drain every BATCH
 // queued.  s0 = the group's first step; `live` = the group's steps that exist.
 template <class C, bool WITH_LSE>
 __device__ __forceinline__ void test_group(TopkWarpSmem<C::CAP>& ws, WarpSel& st, const uint4* v, int s0,
-                                           uint32_t live, float& lm, float& ls, uint32_t V32, uint32_t K,
-                                           uint32_t trig) {
+                                           uint32_t live, float& lm, float& ls, uint32_t V32, uint32_t K) {
   const uint32_t lane = lane_id();
   float vm[TW_GROUP];
   uint32_t pass = 0;
@@ -800,7 +855,7 @@ __device__ __forceinline__ void test_group(TopkWarpSmem<C::CAP>& ws, WarpSel& st
         if (st.nq >= uint32_t(C::BATCH)) {
           __syncwarp();
           do {
-            st = warp_drain<C>(ws, st, C::BATCH, V32, K, trig);
+            st = warp_drain<C>(ws, st, C::BATCH, V32, K);
           } while (st.nq >= uint32_t(C::BATCH));
         }
       }
@@ -812,15 +867,15 @@ __device__ __forceinline__ void test_group(TopkWarpSmem<C::CAP>& ws, WarpSel& st
 // register schedule.  A row's last group copies whole 16-byte vectors only; the one lane
 // whose vector straddles the end of the row (and the lanes past it) read theirs directly.
 
-template <int CAP_, int WARPS_, int BATCH_, int RING_, int GRP_>
-struct TmaCfg : TwCfg<CAP_, WARPS_, BATCH_> {
+template <int CAP_, int WARPS_, int BATCH_, int MAXK_, int RING_, int GRP_>
+struct TmaCfg : TwCfg<CAP_, WARPS_, BATCH_, MAXK_> {
   static constexpr int RING = RING_;
   static constexpr int GRP = GRP_;
   static_assert(GRP == TW_GROUP, "a slot is one tested group");
   static_assert((RING & (RING - 1)) == 0, "slots wrap with a mask");
 };
-using TmSmallK = TmaCfg<512, 15, 24, 4, 4>;   // K <= 128
-using TmLargeK = TmaCfg<1024, 12, 32, 4, 4>;  // K <= 256
+using TmSmallK = TmaCfg<512, 15, 24, 128, 4, 4>;   // K <= 128
+using TmLargeK = TmaCfg<1024, 12, 32, 256, 4, 4>;  // K <= 256
 
 template <class C>
 struct TopkTmaSmem {
@@ -858,7 +913,6 @@ __global__ void __launch_bounds__(C::WARPS * 32, 1)
   const int nst = int((V + TW_STEP - 1) / TW_STEP);
   const int ngr = (nst + GSTEPS - 1) / GSTEPS;  // groups per row
   const uint32_t V32 = uint32_t(V), Ku = uint32_t(K);
-  const uint32_t trig = 2u * Ku + 64u;
   // this lane's vector in a row's last step is not a whole 16 bytes inside the row
   const bool tail_lane = int64_t(nst - 1) * TW_STEP + int64_t(lane) * TK_VEC + TK_VEC > V;
 
@@ -968,11 +1022,11 @@ __global__ void __launch_bounds__(C::WARPS * 32, 1)
       for (int k = 0; k < GSTEPS; ++k) after ^= v[k].x;
       __syncwarp();  // every lane has read the slot
       issue(slot, after);
-      test_group<C, WITH_LSE>(ws, st, v, s0, live, lm, ls, V32, Ku, trig);
+      test_group<C, WITH_LSE>(ws, st, v, s0, live, lm, ls, V32, Ku);
     }
     if (!ok) break;
     __syncwarp();
-    while (st.nq > 0) st = warp_drain<C>(ws, st, min(st.nq, uint32_t(C::BATCH)), V32, Ku, trig);
+    while (st.nq > 0) st = warp_drain<C>(ws, st, min(st.nq, uint32_t(C::BATCH)), V32, Ku);
 
     if (WITH_LSE) {
       for (int o = 16; o > 0; o >>= 1) {
@@ -986,7 +1040,7 @@ __global__ void __launch_bounds__(C::WARPS * 32, 1)
       }
       if (lane == 0) lse_out[row] = lm + log2f(ls) * 0.69314718055994531f;
     }
-    warp_finish<C>(ws, st.cnt, Ku, xr, ids_out + row * K, vals_out + row * K);
+    warp_finish(ws.buf, st.cnt, Ku, xr, ids_out + row * K, vals_out + row * K);
     __syncwarp();
   }
   if (!ok) {  // a wait timed out: let this warp's copies still in flight land (bounded) before leaving
