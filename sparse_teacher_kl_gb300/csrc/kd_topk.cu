@@ -3,17 +3,20 @@
 // the first fix; [DAI] "As duas inovações" item 1; [EPO] "Los dos cambios
 // propuestos", first item).
 //
-// HBM-bound: every logit is read exactly once, in 16-byte vectors, by one CTA
-// per row (grid-strided over rows).  Each element becomes a 48-bit composite
+// HBM-bound: every logit is read exactly once.  Each element becomes a 48-bit
+// composite
 //   (order-preserving 16-bit key of the bf16 value) << 32 | (~column)
 // which is unique per element and orders by value descending, then column
-// ascending; the top-K are the K largest composites.  The row streams through
-// in segments of 4096 elements; a candidate buffer in shared memory receives
-// every element that can still make the top K.  When the buffer passes half
-// full, the K-th largest key T in it is found with two byte histograms and
-// only entries with key >= T are kept; from then on an element needs key > T
-// (any later element with key == T has a larger column and ranks below the K
-// kept ones).  The survivors are sorted once at the end.
+// ascending; the top-K are the K largest composites, so the result is exact with
+// any number of ties.  A threshold key T is valid once at least K elements seen so
+// far reach it: later elements then need key > T (an equal key comes with a larger
+// column and ranks below those K).  Two kernels:
+//  * K <= 256 (the pages' top-100): one warp per row, no block barrier (the
+//    warp-per-row section below);
+//  * 256 < K <= 1024: one CTA per row (grid-strided): the row streams through in
+//    segments of 4096 elements into a shared candidate buffer; when it passes half
+//    full, the K-th largest key in it is found with two byte histograms and only
+//    what reaches it is kept; the survivors are sorted once at the end.
 //
 // Optionally the same pass also takes the full-row logsumexp of the teacher
 // logits, so that the probability mass the cache drops, 1 - sum_k e^(t_k - lse),
