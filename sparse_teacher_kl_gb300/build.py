@@ -8,6 +8,7 @@ from __future__ import annotations
 
 import concurrent.futures
 import hashlib
+import re
 import os
 import shutil
 import subprocess
@@ -46,17 +47,24 @@ def _digest(extra) -> str:
     return h.hexdigest()
 
 
+def _code_only(text: bytes) -> bytes:
+    """Source text without comments and blank space, so that a digest follows the code."""
+    t = re.sub(rb"/\*.*?\*/", b"", text, flags=re.S)
+    t = re.sub(rb"//[^\n]*", b"", t)
+    return b"\n".join(line.strip() for line in t.splitlines() if line.strip())
+
+
 def source_digest(files=None) -> str:
-    """Digest of CUDA sources (not of build flags): identifies the kernels that an ncu
-    capture was taken from.  ``files``: names under csrc/ to digest (default: all of them
-    and the public header)."""
+    """Digest of CUDA sources, comments and blank space left out (not of build flags):
+    identifies the kernels that an ncu capture was taken from.  ``files``: names under
+    csrc/ to digest (default: all of them and the public header)."""
     h = hashlib.sha256()
     names = sorted(files) if files is not None else sorted(os.listdir(CSRC)) + ["../../include/kdkl.h"]
     for f in names:
         path = os.path.normpath(os.path.join(CSRC, f))
         with open(path, "rb") as fh:
             h.update(os.path.basename(path).encode())
-            h.update(fh.read())
+            h.update(_code_only(fh.read()))
     return h.hexdigest()[:16]
 
 
