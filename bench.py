@@ -155,6 +155,50 @@ def bench_topk(kd, dev, stream, peaks, steps):
     return out
 
 
+def bench_teacher_topk(kd, dev, stream, peaks, steps):
+    """kd_teacher_topk on the gpt-oss shape (32768 teacher positions, dt = 2880, V = 201088,
+    K = 100, chunk = 4096): the teacher logits are formed a chunk at a time by the projection
+    engine (2*N*dt*V flops, tensor-bound) and reduced to their top K at once (HBM-bound);
+    the dense [N, V] teacher logits never exist."""
+    import torch
+    from synth import WORKLOADS, make_inputs
+    w = WORKLOADS["gptoss"]
+    N, dt, V, K, c = w.N, w.d, w.V, w.K, w.chunk
+    Ht, Wt, _, _, _ = make_inputs(w, device=dev)
+    ids = torch.empty((N, K), dtype=torch.int32, device=dev)
+    vals = torch.empty((N, K), dtype=torch.float32, device=dev)
+    ws = kd.workspace(kd._abi.kd_teacher_topk_workspace(N, dt, V, K, c), dev)
+
+    def run():
+        st = kd._abi.kd_teacher_topk(Ht.data_ptr(), Wt.data_ptr(), N, dt, V, K, c, ids.data_ptr(), vals.data_ptr(),
+                                     None, ws.data_ptr(), ws.numel(), stream.cuda_stream)
+        assert st == 0
+    for _ in range(2):
+        run()
+    torch.cuda.synchronize(dev)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    with kd.Profile(capacity=4 * steps * (N // c + 2)) as prof:
+        a.record(stream)
+        for _ in range(steps):
+            run()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+    ms = a.elapsed_time(b) / steps
+    flops = 2.0 * N * dt * V
+    kernels = {k: {"launches": n, "avg_ms": t / n, "ms_per_call": t / steps}
+               for k, (n, t) in prof.summary().items()}
+    out = {"workload": f"gpt-oss shape: N={N}, dt={dt}, V={V}, K={K}, chunk={c}",
+           "ms": ms, "positions_per_s": N / (ms * 1e-3),
+           "projection_tflops": flops / (ms * 1e-3) / 1e12,
+           "frac_of_bf16_peak": flops / (ms * 1e-3) / 1e12 / peaks["bf16_sustained"],
+           "peak_source": f"{peaks['source']} bf16 sustained", "kernels": kernels,
+           "workspace_gb": ws.numel() / 1e9}
+    del Ht, Wt, ids, vals, ws
+    torch.cuda.empty_cache()
+    return out
+
+
 def dense_torch_reference(H, W, ids, tlog, mask, dev):
     """Peak device memory and time of one fwd+bwd of the dense formulation in plain PyTorch
     (full [N, V] student logits and a full-vocabulary teacher grid), for the memory comparison
@@ -254,6 +298,7 @@ def main():
     ap.add_argument("--no-modes", action="store_true", help="skip the forward-chunked and dense comparisons")
     ap.add_argument("--no-topk", action="store_true", help="skip the top-K cache measurement")
     ap.add_argument("--topk-only", action="store_true", help="only the top-K cache measurement (profiling)")
+    ap.add_argument("--no-teacher", action="store_true", help="skip the teacher projection + top-K measurement")
     ap.add_argument("--rows", type=int, default=None, help="override B*T (profiling a reduced case)")
     ap.add_argument("--vocab", type=int, default=None, help="override V (profiling a reduced case)")
     args = ap.parse_args()
@@ -421,6 +466,9 @@ def main():
     topk = None
     if not args.no_topk and rank == 0:
         topk = bench_topk(kd, dev, stream, peaks, args.steps)
+    teacher = None
+    if not args.no_teacher and rank == 0:
+        teacher = bench_teacher_topk(kd, dev, stream, peaks, args.steps)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -453,6 +501,7 @@ def main():
                          "peak_source": f"{peaks['source']} bf16 sustained",
                          "flops_per_launch": gemm_flops_per_chunk},
             "topk_cache": topk,
+            "teacher_topk": teacher,
             "forward_chunked": fc,
             "dense_torch_reference": dense,
             "kernels": kernels,

@@ -319,8 +319,12 @@ int kd_teacher_topk(const void* Ht_bf16, const void* Wt_bf16, int64_t N, int64_t
     set_cluster(p);
     p.n_units = ((p.m_tiles + p.cluster - 1) / p.cluster) * p.n_tiles;
     p.C = zbuf; p.ldc = ldz; p.c_bf16 = 1; p.err = &ctrl->err;
+    p.c_tma = 1;   // bf16 logits written as TMA boxes into the row-major chunk buffer
+    p.m_fast = 1;  // Wt (larger than L2) read once per chunk, the chunk of Ht kept in L2
+    alignas(64) CUtensorMap tz;
+    if (!make_tmap_2d_bf16(&tz, zbuf, uint64_t(V), uint64_t(n), uint64_t(ldz) * 2, 64, 32)) return KD_ERR_CUDA;
     const int ci = p.cluster == 4 ? 2 : (p.cluster == 2 ? 1 : 0);
-    cudaError_t e = launch_gemm(p, th, tw[ci], tw[0], grid_max, s);
+    cudaError_t e = launch_gemm(p, th, tw[ci], tz, grid_max, s);
     if (e != cudaSuccess) return KD_ERR_CUDA;
     // exact top-K (and row logsumexp) of those bf16 logits
     e = launch_topk(zbuf, n, V, ldz, K, ids_out + c0 * K, vals_out + c0 * K, lse_out ? lse_out + c0 : nullptr,
@@ -620,6 +624,7 @@ int kd_gemm_bf16(const void* A, const void* B, float* C, int64_t M, int64_t N, i
   p.n_tiles = int((N + BN - 1) / BN);
   p.n_group = 1;
   p.k_splits = 1;
+  p.m_fast = N > M ? 1 : 0;  // B larger than A: share B tiles in flight, read B once
   p.n_units = ((p.m_tiles + p.cluster - 1) / p.cluster) * p.n_tiles;
   p.C = C; p.ldc = N; p.c_bf16 = 0;
   p.err = &static_cast<Ctrl*>(ws)->err;

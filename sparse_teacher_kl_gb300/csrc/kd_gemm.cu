@@ -69,6 +69,16 @@ __device__ __forceinline__ void unit_coords(const GemmProblem& p, int u, uint32_
     kb_lo = 0;
     kb_hi = k_blocks;
     split = 0;
+  } else if (p.m_fast) {
+    // n slowest, m fastest (no split): the CTAs in flight share a few B tiles, each
+    // read from HBM once, and the A operand stays in L2
+    const int n = u / m_groups;
+    m_blk = (u - n * m_groups) * p.cluster + int(crank);
+    n_first = n;
+    n_count = 1;
+    kb_lo = 0;
+    kb_hi = k_blocks;
+    split = 0;
   } else {
     // split slowest, then m, then n: the CTAs in flight share one K range, so each
     // A slab is read by all n tiles and each B slab by all m tiles from L2.
@@ -484,6 +494,34 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                   red_add_v4(dst + g4 * 4, x[g4 * 4 + 0], x[g4 * 4 + 1], x[g4 * 4 + 2], x[g4 * 4 + 3]);
               }
             }
+          } else if (p.c_tma) {
+            // EPI_STORE through TMA: two 32-column chunks fill one 32 x 64 bf16 box of this
+            // warp's 32 rows (128-byte rows, 128-byte swizzle); the store clips rows past M
+            // and columns past N.
+            uint8_t* box = my_staging + sbuf * 4096u;
+            if ((c & 1) == 0) {
+              if (lane == 0) bulk_wait_read<1>();
+              __syncwarp();
+            }
+#pragma unroll
+            for (int g8 = 0; g8 < 4; ++g8) {
+              uint4 v;
+              v.x = pack_bf16x2(x[g8 * 8 + 0], x[g8 * 8 + 1]);
+              v.y = pack_bf16x2(x[g8 * 8 + 2], x[g8 * 8 + 3]);
+              v.z = pack_bf16x2(x[g8 * 8 + 4], x[g8 * 8 + 5]);
+              v.w = pack_bf16x2(x[g8 * 8 + 6], x[g8 * 8 + 7]);
+              const uint32_t j = uint32_t((c & 1) * 4 + g8);
+              *reinterpret_cast<uint4*>(box + lane * 128u + ((j ^ (lane & 7u)) * 16u)) = v;
+            }
+            if (c & 1) {
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                tma_store_2d(&tmap_c, box, col0 - 32, m_blk * BM + int(quarter) * 32);
+                bulk_commit();
+              }
+              sbuf ^= 1u;
+            }
           } else {
             // EPI_STORE: C[row, col0 + i]
             if (row < p.M) {
@@ -527,7 +565,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             make_float4(run_m * scale2, run_s, run_g * p.inv_tau, 0.f);
       }
     }
-    if ((EPI == EPI_DZ || EPI == EPI_LSE_Z) && lane == 0) bulk_wait_all();  // output boxes done before exit
+    if ((EPI == EPI_DZ || EPI == EPI_LSE_Z || (EPI == EPI_STORE && p.c_tma)) && lane == 0)
+      bulk_wait_all();  // output boxes done before exit
   }
 
   tc_fence_before();

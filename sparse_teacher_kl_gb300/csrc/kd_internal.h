@@ -80,6 +80,14 @@ struct GemmProblem {
   void* C;
   int64_t ldc;
   int c_bf16;
+  // c_tma = 1 (EPI_STORE, bf16 C, k_splits = 1): the epilogue writes 32 x 64 boxes staged
+  // in shared memory with TMA stores through tmap_c (row-major C, box 64 x 32, 128-byte
+  // swizzle), clipped at the matrix edges; 0: direct 16-byte stores.
+  int c_tma;
+  // m_fast = 1 (EPI_STORE / EPI_ACCUM with k_splits = 1): units walk m fastest, so the CTAs
+  // in flight share one B tile while the A operand stays in L2 (for a small A and a B
+  // larger than L2, as in the teacher projection); 0: n fastest (they share one A slab).
+  int m_fast;
   // EPI_LSE / EPI_DZ (rows = tokens of the chunk, cols = vocabulary)
   const int32_t* ids_sorted;  // [rows, K] ascending
   const float* p_sorted;      // [rows, K] teacher probabilities matching ids_sorted
