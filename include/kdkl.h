@@ -232,7 +232,10 @@ KD_API int kd_fused_kl_fwd_static(const void* H_bf16, const void* W_bf16,
  * Reads (synchronising `stream`) and clears the device error word of a
  * workspace used by the calls above.  Returns KD_OK, KD_ERR_TIMEOUT or
  * KD_ERR_DEVICE; *detail_out (may be NULL) receives a call-specific detail
- * (for KD_ERR_DEVICE: the first offending row).
+ * (for a bad teacher id: the first offending row).  A library built with
+ * KD_DEBUG (libkdkl_debug.so) also checks the indices its kernels compute and
+ * reports one out of range as KD_ERR_DEVICE with the place of the check as the
+ * detail (0x7xxx: top-K), after skipping the access.
  */
 KD_API int kd_get_device_error(void* ws, void* stream, int64_t* detail_out);
 

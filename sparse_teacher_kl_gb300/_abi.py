@@ -11,7 +11,8 @@ import os
 import re
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libkdkl.so")
+# KD_DEBUG=1 in the environment selects the checked build (see build.build_library(debug=True))
+LIB_PATH = os.path.join(_HERE, "libkdkl_debug.so" if os.environ.get("KD_DEBUG") == "1" else "libkdkl.so")
 HEADER = os.path.join(os.path.dirname(_HERE), "include", "kdkl.h")
 
 KD_OK = 0
@@ -86,7 +87,8 @@ def load():
     global _lib
     if _lib is None:
         if not os.path.exists(LIB_PATH):
-            raise RuntimeError(f"libkdkl.so not built at {LIB_PATH}: run sparse_teacher_kl_gb300.build.build_library()")
+            raise RuntimeError(f"{os.path.basename(LIB_PATH)} not built at {LIB_PATH}: run "
+                               "sparse_teacher_kl_gb300.build.build_library()")
         L = ctypes.CDLL(LIB_PATH)
         for name, (res, args) in _SIGNATURES.items():
             f = getattr(L, name)

@@ -19,6 +19,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libkdkl.so")
+BUILD_DEBUG = os.path.join(ROOT, "_build_debug")
+LIB_DEBUG = os.path.join(PKG, "libkdkl_debug.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
@@ -68,20 +70,25 @@ def source_digest(files=None) -> str:
     return h.hexdigest()[:16]
 
 
-def build_library(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
-    extra = ["-Xptxas", "-v"] if ptxas_info else []
-    os.makedirs(BUILD, exist_ok=True)
-    stamp = os.path.join(BUILD, "libkdkl.stamp")
+def build_library(force: bool = False, verbose: bool = False, ptxas_info: bool = False, debug: bool = False) -> str:
+    """Compile and link libkdkl.so (or, with ``debug``, the checked libkdkl_debug.so:
+    KD_DEBUG, kernels check their computed indices and report a bad one through the
+    workspace error word instead of accessing it).  Returns the library path."""
+    extra = (["-Xptxas", "-v"] if ptxas_info else []) + (["-DKD_DEBUG=1"] if debug else [])
+    bdir = BUILD_DEBUG if debug else BUILD
+    lib = LIB_DEBUG if debug else LIB
+    os.makedirs(bdir, exist_ok=True)
+    stamp = os.path.join(bdir, os.path.basename(lib) + ".stamp")
     digest = _digest(extra)
-    if not force and os.path.exists(LIB) and os.path.exists(stamp):
+    if not force and os.path.exists(lib) and os.path.exists(stamp):
         with open(stamp) as f:
             if f.read().strip() == digest:
-                return LIB
+                return lib
     nvcc = _nvcc()
     srcs = _sources()
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src) + ".o")
+        obj = os.path.join(bdir, os.path.basename(src) + ".o")
         cmd = [nvcc, *ARCH, *CFLAGS, *extra, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -94,15 +101,15 @@ def build_library(force: bool = False, verbose: bool = False, ptxas_info: bool =
         for obj, log in results:
             if log.strip():
                 sys.stderr.write(f"--- {os.path.basename(obj)}\n{log}\n")
-    tmp = LIB + ".tmp"
+    tmp = lib + ".tmp"
     cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *[o for o, _ in results], "-cudart", "static"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
+    os.replace(tmp, lib)
     with open(stamp, "w") as f:
         f.write(digest)
-    return LIB
+    return lib
 
 
 if __name__ == "__main__":

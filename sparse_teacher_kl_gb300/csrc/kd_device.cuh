@@ -47,6 +47,16 @@ __device__ __forceinline__ void raise_error(uint32_t* err, uint32_t code, uint32
   }
 }
 
+// Checked builds (KD_DEBUG): KD_DCHECK(cond, err, where) is cond, and when cond is false
+// it also records KD_DEVERR_BOUNDS with `where` in the error word; the caller skips the
+// access it guards.  In other builds it is the constant true and costs nothing.
+#ifdef KD_DEBUG
+#define KD_DCHECK(cond, err, where) \
+  ((cond) ? true : (raise_error((err), KD_DEVERR_BOUNDS, uint32_t(where)), false))
+#else
+#define KD_DCHECK(cond, err, where) true
+#endif
+
 // ------------------------------------------------------------- mbarrier ---
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {

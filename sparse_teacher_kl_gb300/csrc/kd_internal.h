@@ -15,6 +15,7 @@ namespace kd {
 constexpr uint32_t KD_DEVERR_NONE = 0;
 constexpr uint32_t KD_DEVERR_TIMEOUT = 1;
 constexpr uint32_t KD_DEVERR_BAD_ID = 2;
+constexpr uint32_t KD_DEVERR_BOUNDS = 3;  // KD_DEBUG builds: a computed index out of range (skipped)
 
 // Upper bound on any single wait inside a kernel.  A healthy wait lasts
 // microseconds; this only stops a kernel that would otherwise hang.

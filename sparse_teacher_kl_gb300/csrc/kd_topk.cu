@@ -48,6 +48,7 @@ struct TopkSmem {
   uint32_t sel_bin;
   uint32_t sel_need;
   uint32_t sel_above;
+  uint32_t* err;  // the workspace error word (checked builds report bad indices there)
 };
 
 // bf16 bits -> unsigned key with the same order as the values (-0 == +0).
@@ -140,7 +141,8 @@ __device__ __forceinline__ void warp_append(TopkSmem& sm, bool take, unsigned lo
   uint32_t base = 0;
   if (lane == 0) base = atomicAdd(&sm.count, uint32_t(__popc(ballot)));
   base = __shfl_sync(0xffffffffu, base, 0);
-  if (take) sm.buf[base + __popc(ballot & ((1u << lane) - 1u))] = c;
+  const uint32_t at = base + __popc(ballot & ((1u << lane) - 1u));
+  if (take && KD_DCHECK(at < uint32_t(TK_CAP), sm.err, 0x7001)) sm.buf[at] = c;
 }
 
 // Keep only the entries with key >= T, in place: rounds of TK_ROUND entries per
@@ -220,9 +222,11 @@ __device__ __forceinline__ uint4 load_seg(const uint16_t* xr, int64_t V, int seg
 
 __global__ void __launch_bounds__(TK_THREADS, 2)
     kd_topk_kernel(const uint16_t* __restrict__ X, int64_t N, int64_t V, int64_t ld, int K,
-                   int32_t* __restrict__ ids_out, float* __restrict__ vals_out, float* __restrict__ lse_out) {
+                   int32_t* __restrict__ ids_out, float* __restrict__ vals_out, float* __restrict__ lse_out,
+                   uint32_t* err) {
   extern __shared__ __align__(16) uint8_t tk_smem_raw[];
   TopkSmem& sm = *reinterpret_cast<TopkSmem*>(tk_smem_raw);
+  if (threadIdx.x == 0) sm.err = err;  // read after the first barrier below
   const int nseg = int((V + TK_SEG - 1) / TK_SEG);
 
   for (int64_t row = blockIdx.x; row < N; row += gridDim.x) {
@@ -419,7 +423,7 @@ __global__ void __launch_bounds__(TK_THREADS, 2)
     for (int j = threadIdx.x; j < K; j += TK_THREADS) {
       const uint32_t col = ~uint32_t(sm.buf[j]);
       ids_out[row * K + j] = int32_t(col);
-      vals_out[row * K + j] = __uint_as_float(uint32_t(xr[col]) << 16);
+      if (KD_DCHECK(int64_t(col) < V, sm.err, 0x7002)) vals_out[row * K + j] = __uint_as_float(uint32_t(xr[col]) << 16);
     }
     __syncthreads();
   }
@@ -473,6 +477,7 @@ struct TopkWarpSmem {
   uint4 qv[TW_QUEUE];
   uint32_t qcol[TW_QUEUE];
   uint32_t hist[256];
+  uint32_t* err;  // the workspace error word (checked builds report bad indices there)
 };
 
 __device__ __forceinline__ void warp_find_bin(const uint32_t* h, uint32_t target, uint32_t& bin, uint32_t& need,
@@ -745,12 +750,15 @@ __device__ __noinline__ WarpSel warp_drain(TopkWarpSmem<C::CAP>& ws, WarpSel st,
     const uint32_t e = __ffs(take) - 1;
     take &= take - 1;
     const uint32_t bits = uint32_t(((e & 4) ? hi : lo) >> (16 * (e & 3))) & 0xFFFFu;
-    ws.buf[pos++] = (static_cast<unsigned long long>(bf16_key(bits)) << 32) | uint32_t(~(col0 + e));
+    if (KD_DCHECK(pos < uint32_t(C::CAP), ws.err, 0x7101))
+      ws.buf[pos] = (static_cast<unsigned long long>(bf16_key(bits)) << 32) | uint32_t(~(col0 + e));
+    ++pos;
   }
   st.qh = (st.qh + nb) & (TW_QUEUE - 1);
   st.nq -= nb;
   __syncwarp();
   if (tot == 0) return st;
+  if (!KD_DCHECK(st.cnt + tot <= uint32_t(C::CAP), ws.err, 0x7102)) return st;
   if (tot <= 32) {
     st.cnt = warp_merge_top<C::MAXK / 32>(ws.buf, st.cnt, tot, K);
   } else {  // a large batch: select and sort the whole list
@@ -774,12 +782,14 @@ __device__ __noinline__ WarpSel warp_drain(TopkWarpSmem<C::CAP>& ws, WarpSel st,
 // Warp: the top list (sorted; K entries whenever V >= K) to the row's outputs; values
 // are read back from the row (exact bits, -0 kept).
 __device__ __noinline__ void warp_finish(const unsigned long long* top, uint32_t cnt, uint32_t K, const uint16_t* xr,
-                                         int32_t* ids_row, float* vals_row) {
+                                         uint32_t V32, uint32_t* err, int32_t* ids_row, float* vals_row) {
+  (void)V32;
+  (void)err;
   for (uint32_t j = lane_id(); j < K; j += 32) {
     if (j < cnt) {
       const uint32_t col = ~uint32_t(top[j]);
       ids_row[j] = int32_t(col);
-      vals_row[j] = __uint_as_float(uint32_t(xr[col]) << 16);
+      if (KD_DCHECK(col < V32, err, 0x7301)) vals_row[j] = __uint_as_float(uint32_t(xr[col]) << 16);
     } else {
       ids_row[j] = -1;
       vals_row[j] = -INFINITY;
@@ -923,6 +933,7 @@ __global__ void __launch_bounds__(C::WARPS * 32, 1)
     for (int r = 0; r < C::RING; ++r) mbar_init(&ts.full[r], 1);
     ts.abort = 0;
     ts.never = 0;
+    ws.err = err;
     fence_mbar_init();
   }
   __syncwarp();
@@ -937,8 +948,9 @@ __global__ void __launch_bounds__(C::WARPS * 32, 1)
       if (lane == 0) {
         const int64_t e0 = int64_t(pg) * GSTEPS * TW_STEP;
         const int64_t left = V - e0;
-        const uint32_t bytes = left >= int64_t(GSTEPS) * TW_STEP ? GBYTES : uint32_t(left * 2) & ~15u;
-        mbar_arrive_expect_tx(&ts.full[slot], bytes);
+        uint32_t bytes = left >= int64_t(GSTEPS) * TW_STEP ? GBYTES : uint32_t(left * 2) & ~15u;
+        if (!KD_DCHECK(e0 >= 0 && e0 + bytes / 2 <= V && bytes <= GBYTES, err, 0x7401)) bytes = 0;
+        mbar_arrive_expect_tx(&ts.full[slot], bytes);  // 0 bytes: the phase completes on the arrival
         if (bytes != 0) bulk_g2s(&ts.ring[slot][0][0], X + prow * ld + e0, bytes, &ts.full[slot], after);
       }
       ++issued;
@@ -1043,7 +1055,7 @@ __global__ void __launch_bounds__(C::WARPS * 32, 1)
       }
       if (lane == 0) lse_out[row] = lm + log2f(ls) * 0.69314718055994531f;
     }
-    warp_finish(ws.buf, st.cnt, Ku, xr, ids_out + row * K, vals_out + row * K);
+    warp_finish(ws.buf, st.cnt, Ku, xr, V32, err, ids_out + row * K, vals_out + row * K);
     __syncwarp();
   }
   if (!ok) {  // a wait timed out: let this warp's copies still in flight land (bounded) before leaving
@@ -1092,7 +1104,7 @@ cudaError_t launch_topk(const uint16_t* X, int64_t N, int64_t V, int64_t ld, int
     cudaError_t e = launch_topk_tma<TmLargeK>(X, N, V, ld, K, ids, vals, lse, err, s);
     if (e != cudaSuccess) return e;
   } else {
-    kd_topk_kernel<<<grid, TK_THREADS, smem, s>>>(X, N, V, ld, K, ids, vals, lse);
+    kd_topk_kernel<<<grid, TK_THREADS, smem, s>>>(X, N, V, ld, K, ids, vals, lse, err);
   }
   prof_after(s);
   return cudaGetLastError();
