@@ -639,35 +639,40 @@ struct WarpSel {
   float tv;       // pre-test bound: a vector can hold a candidate only if its maximum is > tv
 };
 
-// Warp: merge the T (<= 32) unsorted candidates buf[nt, nt + T) into the top list
-// buf[0, nt) (sorted descending, nt <= K <= 32 * SLOTS), keeping the K best, in place:
-// the candidates are sorted across the lanes (bitonic, zeros last), every element's new
+// Warp: merge the T (<= 32) candidates buf[nt, nt + T) into the top list buf[0, nt)
+// (composites, sorted descending, nt <= K <= 32 * SLOTS), keeping the K best, in place.
+// The candidates come from later columns than every list entry and lie in column order,
+// so ranks need only 32-bit keys: a list entry outranks a candidate of equal key, and of
+// two equal candidates the earlier one wins.  The candidates are sorted across the lanes
+// by (key, -index) as one 32-bit word (bitonic, empty lanes last); every element's new
 // place is its index plus the number of elements of the other list above it (binary
-// searches; composites are unique), and nothing is written until everything is read.
-// Returns the new length, min(nt + T, K).
+// searches over 32-bit keys); nothing is written until everything is read.  `keys`
+// (>= 32 words) holds the sorted candidate keys.  Returns min(nt + T, K).
 template <int SLOTS>
-__device__ uint32_t warp_merge_top(unsigned long long* buf, uint32_t nt, uint32_t T, uint32_t K) {
+__device__ uint32_t warp_merge_top(unsigned long long* buf, uint32_t* keys, uint32_t nt, uint32_t T, uint32_t K) {
   const uint32_t lane = lane_id();
-  unsigned long long c = lane < T ? buf[nt + lane] : 0ull;
+  const uint32_t* key_hi = reinterpret_cast<const uint32_t*>(buf) + 1;  // high word of buf[i] at [2 i]
+  uint32_t s = lane < T ? (key_hi[2 * (nt + lane)] << 16) | (0xFFFFu - lane) : 0u;
 #pragma unroll
   for (uint32_t k = 2; k <= 32; k <<= 1) {
 #pragma unroll
     for (uint32_t j = k >> 1; j > 0; j >>= 1) {
-      const unsigned long long o = __shfl_xor_sync(0xffffffffu, c, j);
+      const uint32_t o = __shfl_xor_sync(0xffffffffu, s, j);
       const bool desc = (lane & k) == 0;
       const bool low = (lane & j) == 0;
-      c = (low == desc) ? (c > o ? c : o) : (c < o ? c : o);
+      s = (low == desc) ? max(s, o) : min(s, o);
     }
   }
-  // place of candidate `lane` (the lane-th largest): lane + #top entries above it
-  uint32_t lo = 0, hi = nt;
+  // sorted candidate `lane`: its key, its composite, its place
+  const uint32_t ck = s >> 16;
+  const unsigned long long c = lane < T ? buf[nt + (0xFFFFu - (s & 0xFFFFu))] : 0ull;
+  uint32_t lo = 0, hi = nt;  // list entries with key >= ck
   while (lo < hi) {
     const uint32_t mid = (lo + hi) >> 1;
-    if (buf[mid] > c) lo = mid + 1; else hi = mid;
+    if (key_hi[2 * mid] >= ck) lo = mid + 1; else hi = mid;
   }
   const uint32_t cpos = lane + lo;
-  __syncwarp();
-  if (lane < T) buf[nt + lane] = c;  // the candidates, sorted, for the searches below
+  keys[lane] = ck;
   __syncwarp();
   unsigned long long tv[SLOTS];
   uint32_t tpos[SLOTS];
@@ -678,10 +683,11 @@ __device__ uint32_t warp_merge_top(unsigned long long* buf, uint32_t nt, uint32_
     tpos[m] = K;
     if (j < nt) {
       tv[m] = buf[j];
-      uint32_t a = 0, b = T;  // #candidates above top[j]
+      const uint32_t tk = uint32_t(tv[m] >> 32);
+      uint32_t a = 0, b = T;  // candidates with a key above tk
       while (a < b) {
         const uint32_t mid = (a + b) >> 1;
-        if (buf[nt + mid] > tv[m]) a = mid + 1; else b = mid;
+        if (keys[mid] > tk) a = mid + 1; else b = mid;
       }
       tpos[m] = j + a;
     }
@@ -760,7 +766,7 @@ __device__ __noinline__ WarpSel warp_drain(TopkWarpSmem<C::CAP>& ws, WarpSel st,
   if (tot == 0) return st;
   if (!KD_DCHECK(st.cnt + tot <= uint32_t(C::CAP), ws.err, 0x7102)) return st;
   if (tot <= 32) {
-    st.cnt = warp_merge_top<C::MAXK / 32>(ws.buf, st.cnt, tot, K);
+    st.cnt = warp_merge_top<C::MAXK / 32>(ws.buf, ws.hist, st.cnt, tot, K);
   } else {  // a large batch: select and sort the whole list
     uint32_t cnt = st.cnt + tot;
     if (cnt > K) {
