@@ -446,16 +446,26 @@ def main():
         torch.cuda.synchronize(dev)
         h0 = torch.cuda.Event(enable_timing=True)
         h1 = torch.cuda.Event(enable_timing=True)
-        h0.record(stream)
-        for _ in range(args.steps):
-            fc_step()
-        h1.record(stream)
-        torch.cuda.synchronize(dev)
+        with kd.Profile(capacity=64 * (args.steps + 1) * (N // c + 2)) as fprof:
+            h0.record(stream)
+            for _ in range(args.steps):
+                fc_step()
+            h1.record(stream)
+            torch.cuda.synchronize(dev)
         fms = h0.elapsed_time(h1) / args.steps
+        fk = {k: {"launches": n, "avg_ms": t / n, "share": t / max(1e-9, fms * args.steps)}
+              for k, (n, t) in sorted(fprof.summary().items(), key=lambda kv: -kv[1][1])}
         fc = {"ms_per_step": fms, "tokens_per_s": N / (fms * 1e-3),
               "tflops_executed": w.flops_useful() / (fms * 1e-3) / 1e12,
-              "kept_logits_gb": zb / 1e9, "workspace_gb": ws.numel() / 1e9,
+              "kept_logits_gb": zb / 1e9, "workspace_gb": ws.numel() / 1e9, "kernels": fk,
               "note": "forward keeps bf16 logits [N, V]; backward reads them, no recompute (6*d*V flops/token)"}
+        if "kd_dz_from_z" in fk:
+            # HBM-bound: reads one chunk's kept logits and writes its dZ, bf16 [c, V] each
+            zbytes = 2.0 * 2 * c * V
+            gbs = zbytes / (fk["kd_dz_from_z"]["avg_ms"] * 1e-3) / 1e9
+            fc["dz_from_z_roofline"] = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm"], "unit": "GB/s",
+                                        "frac": gbs / peaks["hbm"], "bytes_per_launch": zbytes,
+                                        "peak_source": f"{peaks['source']} copy bandwidth"}
         del z_store
         torch.cuda.empty_cache()
     dense = None

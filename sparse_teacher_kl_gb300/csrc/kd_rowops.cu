@@ -212,21 +212,27 @@ __device__ __forceinline__ float dz_rowscale(const uint8_t* mask, int t, const f
   return (valid && nv > 0) ? (*grad_loss) * inv_tau / float(nv) : 0.f;
 }
 
-__global__ void kd_dz_from_z_kernel(const uint16_t* __restrict__ z, int64_t N, int64_t c0, int rows, int64_t V,
-                                    int64_t nvb, int64_t rows_pad, const float* __restrict__ lse,
-                                    const uint8_t* __restrict__ mask, const float* __restrict__ grad_loss,
-                                    const int32_t* __restrict__ n_valid, float inv_tau, uint16_t* __restrict__ dz) {
+// dZ of one chunk from its kept bf16 logits: both in the blocked layout [V/64][rows][64].
+// A thread owns one (row, 8-column group) of a 64-column block, so its row constants are
+// computed once, and walks vocabulary blocks gridDim.y apart, four loads in flight;
+// consecutive threads cover consecutive 16-byte pieces of one block (coalesced).
+__global__ void __launch_bounds__(256) kd_dz_from_z_kernel(const uint16_t* __restrict__ z, int64_t N, int64_t c0,
+                                                           int rows, int64_t V, int64_t nvb, int64_t rows_pad,
+                                                           const float* __restrict__ lse,
+                                                           const uint8_t* __restrict__ mask,
+                                                           const float* __restrict__ grad_loss,
+                                                           const int32_t* __restrict__ n_valid, float inv_tau,
+                                                           uint16_t* __restrict__ dz) {
+  const int r = blockIdx.x * blockDim.x + threadIdx.x;
+  if (r >= rows * 8) return;
+  const int t = r >> 3, j8 = r & 7;
   const float scale2 = 1.4426950408889634f * inv_tau;
-  const int64_t total = nvb * int64_t(rows) * 8;
-  for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < total; i += int64_t(gridDim.x) * blockDim.x) {
-    const int64_t vb = i / (int64_t(rows) * 8);
-    const int64_t rem = i - vb * int64_t(rows) * 8;
-    const int t = int(rem >> 3);
-    const int j8 = int(rem & 7);
+  const float lse2 = lse[t] * 1.4426950408889634f;
+  const float rs = dz_rowscale(mask, t, grad_loss, n_valid, inv_tau);
+  const uint16_t* zr = z + (c0 + t) * 64 + j8 * 8;  // + vb * N * 64
+  uint16_t* dr = dz + int64_t(t) * 64 + j8 * 8;     // + vb * rows_pad * 64
+  auto one = [&](int64_t vb, const uint4& zin) {
     const int64_t v0 = vb * 64 + j8 * 8;
-    const uint4 zin = *reinterpret_cast<const uint4*>(z + ((vb * N + c0 + t) * 64 + j8 * 8));
-    const float lse2 = lse[t] * 1.4426950408889634f;
-    const float rs = dz_rowscale(mask, t, grad_loss, n_valid, inv_tau);
     const uint32_t w[4] = {zin.x, zin.y, zin.z, zin.w};
     float q[8];
 #pragma unroll
@@ -239,8 +245,18 @@ __global__ void kd_dz_from_z_kernel(const uint16_t* __restrict__ z, int64_t N, i
     out.y = pack_bf16x2(q[2], q[3]);
     out.z = pack_bf16x2(q[4], q[5]);
     out.w = pack_bf16x2(q[6], q[7]);
-    *reinterpret_cast<uint4*>(dz + ((vb * rows_pad + t) * 64 + j8 * 8)) = out;
+    *reinterpret_cast<uint4*>(dr + vb * rows_pad * 64) = out;
+  };
+  const int64_t step = gridDim.y;
+  int64_t vb = blockIdx.y;
+  for (; vb + 3 * step < nvb; vb += 4 * step) {
+    uint4 zin[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) zin[u] = __ldcs(reinterpret_cast<const uint4*>(zr + (vb + u * step) * N * 64));
+#pragma unroll
+    for (int u = 0; u < 4; ++u) one(vb + u * step, zin[u]);
   }
+  for (; vb < nvb; vb += step) one(vb, __ldcs(reinterpret_cast<const uint4*>(zr + vb * N * 64)));
 }
 
 __global__ void kd_dz_fixup_kernel(const uint16_t* __restrict__ z, int64_t N, int64_t c0, int rows, int64_t V,
@@ -267,10 +283,14 @@ cudaError_t launch_dz_from_z(const uint16_t* z, int64_t N, int64_t c0, int rows,
                              int64_t rows_pad, const float* lse, const uint8_t* mask, const float* grad_loss,
                              const int32_t* n_valid, float inv_tau, const int32_t* ids_sorted, const float* p_sorted,
                              int K, uint16_t* dz, cudaStream_t s) {
-  const int grid = 8 * gemm_max_grid();
+  // rows * 8 threads in x; enough vocabulary-block strides in y for ~8 blocks of 256 per SM
+  const int gx = (rows * 8 + 255) / 256;
+  int gy = (8 * gemm_max_grid() + gx - 1) / gx;
+  if (int64_t(gy) > nvb) gy = int(nvb);
+  if (gy > 65535) gy = 65535;
   prof_before("kd_dz_from_z", s);
-  kd_dz_from_z_kernel<<<grid, 256, 0, s>>>(z, N, c0, rows, V, nvb, rows_pad, lse, mask, grad_loss, n_valid, inv_tau,
-                                            dz);
+  kd_dz_from_z_kernel<<<dim3(gx, gy), 256, 0, s>>>(z, N, c0, rows, V, nvb, rows_pad, lse, mask, grad_loss, n_valid,
+                                                    inv_tau, dz);
   prof_after(s);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
