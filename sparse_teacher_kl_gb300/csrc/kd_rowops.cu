@@ -135,22 +135,56 @@ cudaError_t launch_teacher_prologue(const int32_t* ids, const float* tlog, int r
 //   lse_t = ln 2 * (M + log2 sum_u s_u 2^(m_u - M)),  KL_t = negent_t - G_t + lse_t
 // ([ART] fused-loss paragraph: the running accumulator of the fused loss).
 
-__global__ void kd_lse_combine_kernel(const float4* __restrict__ partials, int n_units, int rows, int rows_pad,
-                                      const float* __restrict__ negent, float* __restrict__ lse_out,
-                                      float* __restrict__ kl_out) {
-  const int r = blockIdx.x * blockDim.x + threadIdx.x;
-  if (r >= rows) return;
-  float M = -INFINITY;
-  for (int u = 0; u < n_units; ++u) M = fmaxf(M, partials[size_t(u) * rows_pad + r].x);
-  float S = 0.f, G = 0.f;
-  for (int u = 0; u < n_units; ++u) {
-    const float4 q = partials[size_t(u) * rows_pad + r];
-    if (q.x != -INFINITY) S += q.y * exp2f(q.x - M);
-    G += q.z;
+// Block = 32 rows x 8 unit phases: thread (x, y) folds the partials of row x from units
+// y, y + 8, ... into one running (max, scaled sum, gather) in a single pass (each load a
+// 512-byte coalesced row of partials across the warp), then the 8 phases are merged in
+// shared memory.
+constexpr int LC_ROWS = 32, LC_PHASES = 8;
+
+__global__ void __launch_bounds__(LC_ROWS * LC_PHASES)
+    kd_lse_combine_kernel(const float4* __restrict__ partials, int n_units, int rows, int rows_pad,
+                          const float* __restrict__ negent, float* __restrict__ lse_out,
+                          float* __restrict__ kl_out) {
+  __shared__ float sm_m[LC_PHASES][LC_ROWS], sm_s[LC_PHASES][LC_ROWS], sm_g[LC_PHASES][LC_ROWS];
+  const int x = threadIdx.x, y = threadIdx.y;
+  const int r = blockIdx.x * LC_ROWS + x;
+  float M = -INFINITY, S = 0.f, G = 0.f;
+  if (r < rows) {
+#pragma unroll 4
+    for (int u = y; u < n_units; u += LC_PHASES) {
+      const float4 q = partials[size_t(u) * rows_pad + r];
+      G += q.z;
+      if (q.x != -INFINITY) {
+        if (q.x > M) {
+          S = S * exp2f(M - q.x) + q.y;
+          M = q.x;
+        } else {
+          S += q.y * exp2f(q.x - M);
+        }
+      }
+    }
   }
-  const float lse = (M + log2f(S)) * 0.69314718055994531f;
-  lse_out[r] = lse;
-  kl_out[r] = negent[r] - G + lse;
+  sm_m[y][x] = M;
+  sm_s[y][x] = S;
+  sm_g[y][x] = G;
+  __syncthreads();
+  if (y == 0 && r < rows) {
+    for (int k = 1; k < LC_PHASES; ++k) {
+      const float m2 = sm_m[k][x], s2 = sm_s[k][x];
+      G += sm_g[k][x];
+      if (m2 != -INFINITY) {
+        if (m2 > M) {
+          S = S * exp2f(M - m2) + s2;
+          M = m2;
+        } else {
+          S += s2 * exp2f(m2 - M);
+        }
+      }
+    }
+    const float lse = (M + log2f(S)) * 0.69314718055994531f;
+    lse_out[r] = lse;
+    kl_out[r] = negent[r] - G + lse;
+  }
 }
 
 cudaError_t launch_lse_combine(const float4* partials, int n_units_per_row, int rows, const float* negent,
@@ -158,8 +192,8 @@ cudaError_t launch_lse_combine(const float4* partials, int n_units_per_row, int 
   (void)inv_tau;
   const int rows_pad = ((rows + BM - 1) / BM) * BM;
   prof_before("kd_lse_combine", s);
-  kd_lse_combine_kernel<<<(rows + 255) / 256, 256, 0, s>>>(partials, n_units_per_row, rows, rows_pad, negent,
-                                                           lse_out, kl_out);
+  kd_lse_combine_kernel<<<(rows + LC_ROWS - 1) / LC_ROWS, dim3(LC_ROWS, LC_PHASES), 0, s>>>(
+      partials, n_units_per_row, rows, rows_pad, negent, lse_out, kl_out);
   prof_after(s);
   return cudaGetLastError();
 }
