@@ -66,12 +66,25 @@ static bool make_tmap_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* b
   return r == CUDA_SUCCESS;
 }
 
+bool make_tmap_mn2_bf16(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows, uint64_t row_stride_bytes,
+                        uint32_t box_rows) {
+  if (!load_encode() || cols % 64 != 0) return false;
+  const cuuint64_t dims[3] = {64, rows, cols / 64};
+  const cuuint64_t strides[2] = {row_stride_bytes, 128};
+  const cuuint32_t box[3] = {64, box_rows, 2};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 bool make_tmap_dz_blocked(CUtensorMap* map, const void* base, uint64_t rows, uint64_t rows_pad, uint64_t nvb,
-                          uint32_t box_rows) {
+                          uint32_t box_rows, uint32_t box_depth) {
   if (!load_encode()) return false;
   const cuuint64_t dims[3] = {64, rows, nvb};
   const cuuint64_t strides[2] = {128, rows_pad * 128};
-  const cuuint32_t box[3] = {64, box_rows, 1};
+  const cuuint32_t box[3] = {64, box_rows, box_depth};
   const cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -437,7 +450,8 @@ static int bwd_impl(const void* H_bf16, const void* W_bf16, const int32_t* t_ids
   const uint16_t* H = static_cast<const uint16_t*>(H_bf16);
   const size_t gh_elt = grad_H_is_fp32 ? 4 : 2;
 
-  alignas(64) CUtensorMap tw_k, tw_k_half, tw_mn, th_k, th_mn, tdz_k, tdz_mn, tdz_st, tgw;
+  alignas(64) CUtensorMap tw_k, tw_k_half, tw_mn, tw_mn2, th_k, th_mn, th_mn2, tdz_k, tdz_mn, tdz_mn2, tdz_st, tgw;
+  const bool d64 = d % 64 == 0;  // 3-D two-block views of W and H need whole 64-column blocks
   if (!make_tmap_2d_bf16(&tw_k, W_bf16, uint64_t(d), uint64_t(V), uint64_t(d) * 2, BK, BN)) return KD_ERR_CUDA;
   if (!make_tmap_2d_bf16(&tw_k_half, W_bf16, uint64_t(d), uint64_t(V), uint64_t(d) * 2, BK, BN / 2))
     return KD_ERR_CUDA;
@@ -446,6 +460,7 @@ static int bwd_impl(const void* H_bf16, const void* W_bf16, const int32_t* t_ids
     return KD_ERR_CUDA;
   if (!make_tmap_2d_f32(&tgw, grad_W, uint64_t(d), uint64_t(V), uint64_t(d) * 4, 32, 32)) return KD_ERR_CUDA;
   if (!make_tmap_2d_bf16(&tw_mn, W_bf16, uint64_t(d), uint64_t(V), uint64_t(d) * 2, 64, BK)) return KD_ERR_CUDA;
+  if (d64 && !make_tmap_mn2_bf16(&tw_mn2, W_bf16, uint64_t(d), uint64_t(V), uint64_t(d) * 2, BK)) return KD_ERR_CUDA;
 
   cudaError_t e = launch_count_valid(mask, N, &ctrl->n_valid, s);
   if (e != cudaSuccess) return KD_ERR_CUDA;
@@ -458,9 +473,12 @@ static int bwd_impl(const void* H_bf16, const void* W_bf16, const int32_t* t_ids
     const uint16_t* Hc = H + c0 * d;
     if (!make_tmap_2d_bf16(&th_k, Hc, uint64_t(d), uint64_t(n), uint64_t(d) * 2, BK, BM)) return KD_ERR_CUDA;
     if (!make_tmap_2d_bf16(&th_mn, Hc, uint64_t(d), uint64_t(n), uint64_t(d) * 2, 64, BK)) return KD_ERR_CUDA;
+    if (d64 && !make_tmap_mn2_bf16(&th_mn2, Hc, uint64_t(d), uint64_t(n), uint64_t(d) * 2, BK)) return KD_ERR_CUDA;
     // dZ in blocked layout [vocab/64][row][64]: each box below is one contiguous run
     if (!make_tmap_dz_blocked(&tdz_k, dz, uint64_t(n), uint64_t(L.rows_pad), uint64_t(L.nvb), BM)) return KD_ERR_CUDA;
     if (!make_tmap_dz_blocked(&tdz_mn, dz, uint64_t(n), uint64_t(L.rows_pad), uint64_t(L.nvb), BK)) return KD_ERR_CUDA;
+    if (!make_tmap_dz_blocked(&tdz_mn2, dz, uint64_t(n), uint64_t(L.rows_pad), uint64_t(L.nvb), BK, 2))
+      return KD_ERR_CUDA;
     if (!make_tmap_dz_blocked(&tdz_st, dz, uint64_t(n), uint64_t(L.rows_pad), uint64_t(L.nvb), 32)) return KD_ERR_CUDA;
 
     if (z_store) {
@@ -509,7 +527,8 @@ static int bwd_impl(const void* H_bf16, const void* W_bf16, const int32_t* t_ids
       q.split_stride = L.rows_pad * d;
     }
     q.err = &ctrl->err;
-    e = launch_gemm(q, tdz_k, tw_mn, tw_mn, grid_max, s);
+    q.b_box2 = q.cta_pair && d64;
+    e = launch_gemm(q, tdz_k, q.b_box2 ? tw_mn2 : tw_mn, tw_mn, grid_max, s);
     if (e != cudaSuccess) return KD_ERR_CUDA;
     if (q.k_splits > 1) {
       e = launch_split_reduce(reinterpret_cast<const float*>(w8 + L.gh_part), q.k_splits, L.rows_pad * d,
@@ -529,7 +548,9 @@ static int bwd_impl(const void* H_bf16, const void* W_bf16, const int32_t* t_ids
     set_cluster(r);
     r.n_units = ((r.m_tiles + r.cluster - 1) / r.cluster) * r.n_tiles;
     r.C = grad_W; r.ldc = d; r.c_bf16 = 0; r.err = &ctrl->err;
-    e = launch_gemm(r, tdz_mn, th_mn, tgw, grid_max, s);
+    r.a_box2 = r.cta_pair;
+    r.b_box2 = r.cta_pair && d64;
+    e = launch_gemm(r, r.a_box2 ? tdz_mn2 : tdz_mn, r.b_box2 ? th_mn2 : th_mn, tgw, grid_max, s);
     if (e != cudaSuccess) return KD_ERR_CUDA;
   }
   return KD_OK;
@@ -615,8 +636,13 @@ int kd_gemm_bf16(const void* A, const void* B, float* C, int64_t M, int64_t N, i
   p.m_tiles = int((M + BM - 1) / BM);
   set_cluster(p);
   const int cluster = p.cluster;
-  ok = ok && (b_mn ? make_tmap_2d_bf16(&tb, B, uint64_t(N), uint64_t(K), uint64_t(N) * 2, 64, BK)
-                   : make_tmap_2d_bf16(&tb, B, uint64_t(K), uint64_t(N), uint64_t(K) * 2, BK, BN / cluster));
+  // MN-major operands of CTA pairs: both 64-column blocks of a stage in one depth-2 box
+  p.a_box2 = p.cta_pair && a_mn && M % 64 == 0;
+  p.b_box2 = p.cta_pair && b_mn && N % 64 == 0;
+  if (p.a_box2) ok = ok && make_tmap_mn2_bf16(&ta, A, uint64_t(M), uint64_t(K), uint64_t(M) * 2, BK);
+  ok = ok && (p.b_box2 ? make_tmap_mn2_bf16(&tb, B, uint64_t(N), uint64_t(K), uint64_t(N) * 2, BK)
+              : b_mn   ? make_tmap_2d_bf16(&tb, B, uint64_t(N), uint64_t(K), uint64_t(N) * 2, 64, BK)
+                       : make_tmap_2d_bf16(&tb, B, uint64_t(K), uint64_t(N), uint64_t(K) * 2, BK, BN / cluster));
   ok = ok && make_tmap_2d_f32(&tc, C, uint64_t(N), uint64_t(M), uint64_t(N) * 4, 32, 32);
   if (!ok) return KD_ERR_CUDA;
   p.M = int(M); p.N = int(N); p.K = int(K);

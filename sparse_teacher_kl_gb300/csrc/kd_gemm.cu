@@ -168,6 +168,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
               if (p.a_blocked) {
                 if (p.a_mn == 0) {
                   tma_load_3d_pair(sa, &tmap_a, bar0, 0, m_blk * BM, kb);
+                } else if (p.a_box2) {
+                  tma_load_3d_pair(sa, &tmap_a, bar0, 0, kb * BK, m_blk * (BM / 64));
                 } else {
 #pragma unroll
                   for (int j = 0; j < BM / 64; ++j)
@@ -175,6 +177,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 }
               } else if (p.a_mn == 0) {
                 tma_load_2d_pair(sa, &tmap_a, bar0, kb * BK, m_blk * BM);
+              } else if (p.a_box2) {
+                tma_load_3d_pair(sa, &tmap_a, bar0, 0, kb * BK, m_blk * (BM / 64));
               } else {
 #pragma unroll
                 for (int j = 0; j < BM / 64; ++j)
@@ -183,6 +187,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
               // this CTA's 128 columns of the pair's 256-column B tile
               if (p.b_mn == 0) {
                 tma_load_2d_pair(sb, &tmap_b, bar0, kb * BK, nb * BN + int(crank) * (BN / 2));
+              } else if (p.b_box2) {
+                tma_load_3d_pair(sb, &tmap_b, bar0, 0, kb * BK, (nb * BN + int(crank) * (BN / 2)) / 64);
               } else {
 #pragma unroll
                 for (int j = 0; j < BN / 128; ++j)

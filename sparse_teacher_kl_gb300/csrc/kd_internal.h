@@ -68,6 +68,10 @@ struct GemmProblem {
   // dZ[vocab / 64][row][vocab % 64] (see make_tmap_dz_blocked), so that every TMA box
   // of it is one contiguous run of memory.
   int a_blocked;
+  // a_box2 / b_box2 (CTA pairs, MN-major operand): the operand's two 64-column blocks of
+  // a stage come in one TMA box of depth 2 from a 3-D map (64, k, blocks), 8 KB apart in
+  // shared memory as the MMA reads them; 0: two boxes from a 2-D (or depth-1) map.
+  int a_box2, b_box2;
   int z_row0;                 // EPI_LSE_Z: row of the stored logits that chunk row 0 maps to
   // cluster = 2 or 4: the CTAs of a cluster take consecutive m tiles of the same n tile
   // and share the B operand: each loads 1/cluster of it (K-major B map box 64 x 256/cluster)
@@ -111,7 +115,11 @@ bool make_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint6
 // dZ chunk in blocked layout: [nvb = ceil(V/64)][rows_pad][64] bf16; dims {64, rows, nvb},
 // box {64, box_rows, 1}, 128-byte swizzle.
 bool make_tmap_dz_blocked(CUtensorMap* map, const void* base, uint64_t rows, uint64_t rows_pad, uint64_t nvb,
-                          uint32_t box_rows);
+                          uint32_t box_rows, uint32_t box_depth = 1);
+// 3-D view (64, rows, cols / 64) of a row-major bf16 matrix whose column count is a
+// multiple of 64, box (64, box_rows, 2): two 64-column blocks per TMA box.
+bool make_tmap_mn2_bf16(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows, uint64_t row_stride_bytes,
+                        uint32_t box_rows);
 bool make_tmap_2d_f32(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
                       uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer);
 

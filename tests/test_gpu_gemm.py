@@ -24,7 +24,7 @@ def _case(M, N, K, a_mn, b_mn, seed, dev):
 
 
 @pytest.mark.parametrize("a_mn,b_mn", [(0, 0), (0, 1), (1, 1), (1, 0)])
-@pytest.mark.parametrize("M,N,K", [(128, 256, 64), (296, 520, 200), (64, 16, 8), (1000, 264, 1096)])
+@pytest.mark.parametrize("M,N,K", [(128, 256, 64), (296, 520, 200), (64, 16, 8), (1000, 264, 1096), (640, 704, 320)])
 def test_gemm_matches_float64(kd, cuda_device, a_mn, b_mn, M, N, K):
     A, B, ref = _case(M, N, K, a_mn, b_mn, seed=M * 7 + N + K, dev=cuda_device)
     C, ws = kd.gemm_bf16(A, B, M, N, K, a_mn, b_mn)
