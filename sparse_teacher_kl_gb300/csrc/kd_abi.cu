@@ -197,6 +197,10 @@ static void set_cluster(GemmProblem& p) {
 // Number of K splits for a product of `tiles` output tiles with `k_blocks` steps of
 // BK each: the fewest waves of `grid` persistent CTAs per unit of work, with a small
 // charge per split for the extra partial traffic.
+// The loss launches below build depth-2 K-major boxes (a_k3d / b_k3d) for CTA pairs.
+static_assert(pair_kblocks(EPI_LSE) == 2 && pair_kblocks(EPI_DZ) == 2 && pair_kblocks(EPI_LSE_Z) == 2,
+              "loss epilogues take two k-blocks per pair stage");
+
 static int choose_splits(int64_t tiles, int k_blocks, int grid) {
   int best = 1;
   double best_cost = 1e300;
@@ -313,14 +317,19 @@ int kd_teacher_topk(const void* Ht_bf16, const void* Wt_bf16, int64_t N, int64_t
   const int64_t ldz = (V + 7) / 8 * 8;
   const uint16_t* Ht = static_cast<const uint16_t*>(Ht_bf16);
   const int grid_max = gemm_max_grid();
-  alignas(64) CUtensorMap tw[3], th;
+  alignas(64) CUtensorMap tw[3], th, tw2, th2;
   for (int i = 0; i < 3; ++i)
     if (!make_tmap_2d_bf16(&tw[i], Wt_bf16, uint64_t(dt), uint64_t(V), uint64_t(dt) * 2, BK, BN >> i))
       return KD_ERR_CUDA;
+  const bool dt64 = dt % 64 == 0;  // two k-blocks per box for CTA pairs
+  if (dt64 && !make_tmap_mn2_bf16(&tw2, Wt_bf16, uint64_t(dt), uint64_t(V), uint64_t(dt) * 2, BN / 2))
+    return KD_ERR_CUDA;
   for (int64_t c0 = 0; c0 < N; c0 += chunk) {
     const int n = int((N - c0) < chunk ? (N - c0) : chunk);
     // the chunk's teacher logits, fp32 on the tensor cores, rounded once to bf16
     if (!make_tmap_2d_bf16(&th, Ht + c0 * dt, uint64_t(dt), uint64_t(n), uint64_t(dt) * 2, BK, BM))
+      return KD_ERR_CUDA;
+    if (dt64 && !make_tmap_mn2_bf16(&th2, Ht + c0 * dt, uint64_t(dt), uint64_t(n), uint64_t(dt) * 2, BM))
       return KD_ERR_CUDA;
     GemmProblem p{};
     p.M = n; p.N = int(V); p.K = int(dt);
@@ -337,7 +346,8 @@ int kd_teacher_topk(const void* Ht_bf16, const void* Wt_bf16, int64_t N, int64_t
     alignas(64) CUtensorMap tz;
     if (!make_tmap_2d_bf16(&tz, zbuf, uint64_t(V), uint64_t(n), uint64_t(ldz) * 2, 64, 32)) return KD_ERR_CUDA;
     const int ci = p.cluster == 4 ? 2 : (p.cluster == 2 ? 1 : 0);
-    cudaError_t e = launch_gemm(p, th, tw[ci], tz, grid_max, s);
+    p.a_k3d = p.b_k3d = p.cta_pair && dt64;
+    cudaError_t e = launch_gemm(p, p.a_k3d ? th2 : th, p.b_k3d ? tw2 : tw[ci], tz, grid_max, s);
     if (e != cudaSuccess) return KD_ERR_CUDA;
     // exact top-K (and row logsumexp) of those bf16 logits
     e = launch_topk(zbuf, n, V, ldz, K, ids_out + c0 * K, vals_out + c0 * K, lse_out ? lse_out + c0 : nullptr,
@@ -384,9 +394,11 @@ static int fwd_impl(const void* H_bf16, const void* W_bf16, const int32_t* t_ids
   if (!make_tmap_2d_bf16(&tw, W_bf16, uint64_t(d), uint64_t(V), uint64_t(d) * 2, BK, BN)) return KD_ERR_CUDA;
   if (!make_tmap_2d_bf16(&tw_half, W_bf16, uint64_t(d), uint64_t(V), uint64_t(d) * 2, BK, BN / 2))
     return KD_ERR_CUDA;
-  alignas(64) CUtensorMap tw_quarter;
+  alignas(64) CUtensorMap tw_quarter, tw2, th2;
   if (!make_tmap_2d_bf16(&tw_quarter, W_bf16, uint64_t(d), uint64_t(V), uint64_t(d) * 2, BK, BN / 4))
     return KD_ERR_CUDA;
+  const bool d64 = d % 64 == 0;  // two k-blocks per box for CTA pairs
+  if (d64 && !make_tmap_mn2_bf16(&tw2, W_bf16, uint64_t(d), uint64_t(V), uint64_t(d) * 2, BN / 2)) return KD_ERR_CUDA;
   if (z_store) {
     (void)z_bytes;
     if (!make_tmap_dz_blocked(&tz, z_store, uint64_t(N), uint64_t(N), uint64_t((V + 63) / 64), 32))
@@ -402,6 +414,8 @@ static int fwd_impl(const void* H_bf16, const void* W_bf16, const int32_t* t_ids
                                 &ctrl->err, c0, s);
     if (e != cudaSuccess) return KD_ERR_CUDA;
     if (!make_tmap_2d_bf16(&th, H + c0 * d, uint64_t(d), uint64_t(n), uint64_t(d) * 2, BK, BM)) return KD_ERR_CUDA;
+    if (d64 && !make_tmap_mn2_bf16(&th2, H + c0 * d, uint64_t(d), uint64_t(n), uint64_t(d) * 2, BM))
+      return KD_ERR_CUDA;
     GemmProblem p{};
     p.M = n; p.N = int(V); p.K = int(d);
     p.a_mn = 0; p.b_mn = 0; p.epi = z_store ? EPI_LSE_Z : EPI_LSE;
@@ -414,8 +428,10 @@ static int fwd_impl(const void* H_bf16, const void* W_bf16, const int32_t* t_ids
     p.k_splits = 1;
     p.ids_sorted = ids_sorted; p.p_sorted = p_sorted; p.Kt = K; p.inv_tau = inv_tau;
     p.partials = partials; p.rows = n; p.err = &ctrl->err;
-    e = launch_gemm(p, th, p.cluster == 4 ? tw_quarter : (p.cluster == 2 ? tw_half : tw), z_store ? tz : tw, grid_max,
-                    s);
+    p.a_k3d = p.b_k3d = p.cta_pair && d64;
+    e = launch_gemm(p, p.a_k3d ? th2 : th,
+                    p.b_k3d ? tw2 : (p.cluster == 4 ? tw_quarter : (p.cluster == 2 ? tw_half : tw)), z_store ? tz : tw,
+                    grid_max, s);
     if (e != cudaSuccess) return KD_ERR_CUDA;
     e = launch_lse_combine(partials, L.n_groups, n, negent, inv_tau, lse_out + c0, kl + c0, s);
     if (e != cudaSuccess) return KD_ERR_CUDA;
@@ -450,7 +466,12 @@ static int bwd_impl(const void* H_bf16, const void* W_bf16, const int32_t* t_ids
   const uint16_t* H = static_cast<const uint16_t*>(H_bf16);
   const size_t gh_elt = grad_H_is_fp32 ? 4 : 2;
 
-  alignas(64) CUtensorMap tw_k, tw_k_half, tw_mn, tw_mn2, th_k, th_mn, th_mn2, tdz_k, tdz_mn, tdz_mn2, tdz_st, tgw;
+  alignas(64) CUtensorMap tw_k, tw_k_half, tw_mn, tw_mn2, th_k, th_mn, th_mn2, tdz_k, tdz_mn, tdz_st, tgw;
+  // CTA-pair launches take pair_kblocks(epi) 64-deep k-blocks per ring stage: boxes of
+  // 64 kq (grad_H) / 64 kr (grad_W) rows for MN-major operands, that depth for K-major
+  // ones (suffix _p); the dZ recompute takes two (tw_k2, th_k2: depth-2 boxes)
+  alignas(64) CUtensorMap tw_k2, tw_mn_p, th_k2, th_mn_p, tdz_k_p, tdz_mn_p;
+  const int kq = pair_kblocks(EPI_STORE), kr = pair_kblocks(EPI_ACCUM);
   const bool d64 = d % 64 == 0;  // 3-D two-block views of W and H need whole 64-column blocks
   if (!make_tmap_2d_bf16(&tw_k, W_bf16, uint64_t(d), uint64_t(V), uint64_t(d) * 2, BK, BN)) return KD_ERR_CUDA;
   if (!make_tmap_2d_bf16(&tw_k_half, W_bf16, uint64_t(d), uint64_t(V), uint64_t(d) * 2, BK, BN / 2))
@@ -460,7 +481,11 @@ static int bwd_impl(const void* H_bf16, const void* W_bf16, const int32_t* t_ids
     return KD_ERR_CUDA;
   if (!make_tmap_2d_f32(&tgw, grad_W, uint64_t(d), uint64_t(V), uint64_t(d) * 4, 32, 32)) return KD_ERR_CUDA;
   if (!make_tmap_2d_bf16(&tw_mn, W_bf16, uint64_t(d), uint64_t(V), uint64_t(d) * 2, 64, BK)) return KD_ERR_CUDA;
-  if (d64 && !make_tmap_mn2_bf16(&tw_mn2, W_bf16, uint64_t(d), uint64_t(V), uint64_t(d) * 2, BK)) return KD_ERR_CUDA;
+  if (d64 && !make_tmap_mn2_bf16(&tw_mn2, W_bf16, uint64_t(d), uint64_t(V), uint64_t(d) * 2, BK * kq))
+    return KD_ERR_CUDA;
+  if (!make_tmap_2d_bf16(&tw_mn_p, W_bf16, uint64_t(d), uint64_t(V), uint64_t(d) * 2, 64, BK * kq)) return KD_ERR_CUDA;
+  if (d64 && !make_tmap_mn2_bf16(&tw_k2, W_bf16, uint64_t(d), uint64_t(V), uint64_t(d) * 2, BN / 2))
+    return KD_ERR_CUDA;
 
   cudaError_t e = launch_count_valid(mask, N, &ctrl->n_valid, s);
   if (e != cudaSuccess) return KD_ERR_CUDA;
@@ -473,11 +498,16 @@ static int bwd_impl(const void* H_bf16, const void* W_bf16, const int32_t* t_ids
     const uint16_t* Hc = H + c0 * d;
     if (!make_tmap_2d_bf16(&th_k, Hc, uint64_t(d), uint64_t(n), uint64_t(d) * 2, BK, BM)) return KD_ERR_CUDA;
     if (!make_tmap_2d_bf16(&th_mn, Hc, uint64_t(d), uint64_t(n), uint64_t(d) * 2, 64, BK)) return KD_ERR_CUDA;
-    if (d64 && !make_tmap_mn2_bf16(&th_mn2, Hc, uint64_t(d), uint64_t(n), uint64_t(d) * 2, BK)) return KD_ERR_CUDA;
+    if (d64 && !make_tmap_mn2_bf16(&th_mn2, Hc, uint64_t(d), uint64_t(n), uint64_t(d) * 2, BK * kr))
+      return KD_ERR_CUDA;
+    if (!make_tmap_2d_bf16(&th_mn_p, Hc, uint64_t(d), uint64_t(n), uint64_t(d) * 2, 64, BK * kr)) return KD_ERR_CUDA;
+    if (d64 && !make_tmap_mn2_bf16(&th_k2, Hc, uint64_t(d), uint64_t(n), uint64_t(d) * 2, BM)) return KD_ERR_CUDA;
     // dZ in blocked layout [vocab/64][row][64]: each box below is one contiguous run
     if (!make_tmap_dz_blocked(&tdz_k, dz, uint64_t(n), uint64_t(L.rows_pad), uint64_t(L.nvb), BM)) return KD_ERR_CUDA;
     if (!make_tmap_dz_blocked(&tdz_mn, dz, uint64_t(n), uint64_t(L.rows_pad), uint64_t(L.nvb), BK)) return KD_ERR_CUDA;
-    if (!make_tmap_dz_blocked(&tdz_mn2, dz, uint64_t(n), uint64_t(L.rows_pad), uint64_t(L.nvb), BK, 2))
+    if (!make_tmap_dz_blocked(&tdz_k_p, dz, uint64_t(n), uint64_t(L.rows_pad), uint64_t(L.nvb), BM, kq))
+      return KD_ERR_CUDA;
+    if (!make_tmap_dz_blocked(&tdz_mn_p, dz, uint64_t(n), uint64_t(L.rows_pad), uint64_t(L.nvb), BK * kr, 2))
       return KD_ERR_CUDA;
     if (!make_tmap_dz_blocked(&tdz_st, dz, uint64_t(n), uint64_t(L.rows_pad), uint64_t(L.nvb), 32)) return KD_ERR_CUDA;
 
@@ -501,8 +531,10 @@ static int bwd_impl(const void* H_bf16, const void* W_bf16, const int32_t* t_ids
     p.ids_sorted = ids_sorted; p.p_sorted = p_sorted; p.Kt = K; p.inv_tau = inv_tau;
     p.lse = lse + c0; p.mask = mask ? mask + c0 : nullptr; p.grad_loss = grad_loss; p.n_valid = &ctrl->n_valid;
     p.dz = dz; p.ldz = L.ldz; p.rows = n; p.err = &ctrl->err;
-    e = launch_gemm(p, th_k, p.cluster == 4 ? tw_k_quarter : (p.cluster == 2 ? tw_k_half : tw_k), tdz_st, grid_max,
-                    s);
+    p.a_k3d = p.b_k3d = p.cta_pair && d64;
+    e = launch_gemm(p, p.a_k3d ? th_k2 : th_k,
+                    p.b_k3d ? tw_k2 : (p.cluster == 4 ? tw_k_quarter : (p.cluster == 2 ? tw_k_half : tw_k)), tdz_st,
+                    grid_max, s);
     if (e != cudaSuccess) return KD_ERR_CUDA;
     }
 
@@ -528,7 +560,8 @@ static int bwd_impl(const void* H_bf16, const void* W_bf16, const int32_t* t_ids
     }
     q.err = &ctrl->err;
     q.b_box2 = q.cta_pair && d64;
-    e = launch_gemm(q, tdz_k, q.b_box2 ? tw_mn2 : tw_mn, tw_mn, grid_max, s);
+    e = launch_gemm(q, q.cta_pair ? tdz_k_p : tdz_k, q.b_box2 ? tw_mn2 : (q.cta_pair ? tw_mn_p : tw_mn), tw_mn,
+                    grid_max, s);
     if (e != cudaSuccess) return KD_ERR_CUDA;
     if (q.k_splits > 1) {
       e = launch_split_reduce(reinterpret_cast<const float*>(w8 + L.gh_part), q.k_splits, L.rows_pad * d,
@@ -548,9 +581,9 @@ static int bwd_impl(const void* H_bf16, const void* W_bf16, const int32_t* t_ids
     set_cluster(r);
     r.n_units = ((r.m_tiles + r.cluster - 1) / r.cluster) * r.n_tiles;
     r.C = grad_W; r.ldc = d; r.c_bf16 = 0; r.err = &ctrl->err;
-    r.a_box2 = r.cta_pair;
     r.b_box2 = r.cta_pair && d64;
-    e = launch_gemm(r, r.a_box2 ? tdz_mn2 : tdz_mn, r.b_box2 ? th_mn2 : th_mn, tgw, grid_max, s);
+    e = launch_gemm(r, r.cta_pair ? tdz_mn_p : tdz_mn, r.b_box2 ? th_mn2 : (r.cta_pair ? th_mn_p : th_mn), tgw,
+                    grid_max, s);
     if (e != cudaSuccess) return KD_ERR_CUDA;
   }
   return KD_OK;
@@ -629,20 +662,34 @@ int kd_gemm_bf16(const void* A, const void* B, float* C, int64_t M, int64_t N, i
   kd_status st = check_device();
   if (st != KD_OK) return st;
   alignas(64) CUtensorMap ta, tb, tc;
-  bool ok = a_mn ? make_tmap_2d_bf16(&ta, A, uint64_t(M), uint64_t(K), uint64_t(M) * 2, 64, BK)
-                 : make_tmap_2d_bf16(&ta, A, uint64_t(K), uint64_t(M), uint64_t(K) * 2, BK, BM);
   GemmProblem p{};
   p.epi = accumulate ? EPI_ACCUM : EPI_STORE;
   p.m_tiles = int((M + BM - 1) / BM);
   set_cluster(p);
   const int cluster = p.cluster;
-  // MN-major operands of CTA pairs: both 64-column blocks of a stage in one depth-2 box
-  p.a_box2 = p.cta_pair && a_mn && M % 64 == 0;
-  p.b_box2 = p.cta_pair && b_mn && N % 64 == 0;
-  if (p.a_box2) ok = ok && make_tmap_mn2_bf16(&ta, A, uint64_t(M), uint64_t(K), uint64_t(M) * 2, BK);
-  ok = ok && (p.b_box2 ? make_tmap_mn2_bf16(&tb, B, uint64_t(N), uint64_t(K), uint64_t(N) * 2, BK)
-              : b_mn   ? make_tmap_2d_bf16(&tb, B, uint64_t(N), uint64_t(K), uint64_t(N) * 2, 64, BK)
-                       : make_tmap_2d_bf16(&tb, B, uint64_t(K), uint64_t(N), uint64_t(K) * 2, BK, BN / cluster));
+  bool ok;
+  if (p.cta_pair) {
+    // kk 64-deep k-blocks per ring stage; each operand in one box where whole 64-column
+    // blocks allow (MN-major: both column blocks; K-major: kk = 2 k-blocks, depth 2)
+    const int kk = pair_kblocks(p.epi);
+    p.a_box2 = a_mn && M % 64 == 0;
+    p.a_k3d = kk == 2 && !a_mn && K % 64 == 0;
+    p.b_box2 = b_mn && N % 64 == 0;
+    p.b_k3d = kk == 2 && !b_mn && K % 64 == 0;
+    ok = a_mn ? (p.a_box2 ? make_tmap_mn2_bf16(&ta, A, uint64_t(M), uint64_t(K), uint64_t(M) * 2, BK * kk)
+                          : make_tmap_2d_bf16(&ta, A, uint64_t(M), uint64_t(K), uint64_t(M) * 2, 64, BK * kk))
+              : (p.a_k3d ? make_tmap_mn2_bf16(&ta, A, uint64_t(K), uint64_t(M), uint64_t(K) * 2, BM)
+                         : make_tmap_2d_bf16(&ta, A, uint64_t(K), uint64_t(M), uint64_t(K) * 2, BK, BM));
+    ok = ok && (b_mn ? (p.b_box2 ? make_tmap_mn2_bf16(&tb, B, uint64_t(N), uint64_t(K), uint64_t(N) * 2, BK * kk)
+                                 : make_tmap_2d_bf16(&tb, B, uint64_t(N), uint64_t(K), uint64_t(N) * 2, 64, BK * kk))
+                     : (p.b_k3d ? make_tmap_mn2_bf16(&tb, B, uint64_t(K), uint64_t(N), uint64_t(K) * 2, BN / 2)
+                                : make_tmap_2d_bf16(&tb, B, uint64_t(K), uint64_t(N), uint64_t(K) * 2, BK, BN / 2)));
+  } else {
+    ok = a_mn ? make_tmap_2d_bf16(&ta, A, uint64_t(M), uint64_t(K), uint64_t(M) * 2, 64, BK)
+              : make_tmap_2d_bf16(&ta, A, uint64_t(K), uint64_t(M), uint64_t(K) * 2, BK, BM);
+    ok = ok && (b_mn ? make_tmap_2d_bf16(&tb, B, uint64_t(N), uint64_t(K), uint64_t(N) * 2, 64, BK)
+                     : make_tmap_2d_bf16(&tb, B, uint64_t(K), uint64_t(N), uint64_t(K) * 2, BK, BN / cluster));
+  }
   ok = ok && make_tmap_2d_f32(&tc, C, uint64_t(N), uint64_t(M), uint64_t(N) * 4, 32, 32);
   if (!ok) return KD_ERR_CUDA;
   p.M = int(M); p.N = int(N); p.K = int(K);

@@ -40,26 +40,35 @@ struct __align__(8) GemmSmemTail {
 
 // Shared-memory ring per CTA.  One CTA per tile (CG = 1): a stage holds A 128 x 64 and
 // B 256 x 64 (48 KB), 4 stages.  CTA pair per tile (CG = 2, tcgen05 cta_group::2): each
-// CTA holds its 128 rows of A and its 128 columns of B (32 KB), so 6 stages fit and each
-// SM moves a third less operand data per flop.
-template <int CG>
+// CTA holds its 128 rows of A and its 128 columns of B for KKB 64-deep k-blocks: the
+// loss epilogues take two (64 KB, 3 stages; every operand of a stage in one depth-2
+// TMA box), the gradient products one (32 KB, PAIR_PRODUCT_STAGES stages).
+constexpr int PAIR_PRODUCT_STAGES = 6;
+
+template <int CG, int KKB>
 struct Geo {
-  static constexpr int kStages = CG == 2 ? 6 : STAGES;
-  static constexpr int kA = STAGE_A_BYTES;
-  static constexpr int kB = CG == 2 ? STAGE_B_BYTES / 2 : STAGE_B_BYTES;
+  static constexpr int kKB = KKB;  // 64-deep k-blocks per stage
+  static constexpr int kStages = CG == 1 ? STAGES : (KKB == 2 ? 3 : PAIR_PRODUCT_STAGES);
+  static constexpr int kA = STAGE_A_BYTES * kKB;
+  static constexpr int kB = (CG == 2 ? STAGE_B_BYTES / 2 : STAGE_B_BYTES) * kKB;
   static constexpr int kStage = kA + kB;
   static constexpr size_t kSmem =
       1024 /*alignment slack*/ + size_t(kStages) * kStage + STAGING_BYTES + sizeof(GemmSmemTail);
+  static_assert(CG == 2 || KKB == 1, "two k-blocks per stage only for CTA pairs");
   static_assert(kStages <= MAX_STAGES, "barrier arrays");
   static_assert(kSmem <= 232448, "shared memory budget of one CTA");
 };
 
+template <int EPI, int CG>
+using GeoOf = Geo<CG, CG == 2 ? pair_kblocks(EPI) : 1>;
+
 // Unit u -> tile coordinates.  LSE/DZ walk the vocabulary (n) slowly so that
 // every CTA in flight reads the same few W tiles while the small H chunk stays
 // in L2; the gradient products walk n fastest so that CTAs in flight share A.
-__device__ __forceinline__ void unit_coords(const GemmProblem& p, int u, uint32_t crank, int& m_blk, int& n_first,
-                                            int& n_count, int& kb_lo, int& kb_hi, int& split) {
-  const int k_blocks = (p.K + BK - 1) / BK;
+// K ranges are in steps of kkb 64-deep k-blocks (one ring stage each).
+__device__ __forceinline__ void unit_coords(const GemmProblem& p, int u, uint32_t crank, int kkb, int& m_blk,
+                                            int& n_first, int& n_count, int& kb_lo, int& kb_hi, int& split) {
+  const int k_blocks = ((p.K + BK - 1) / BK + kkb - 1) / kkb;
   const int m_groups = (p.m_tiles + p.cluster - 1) / p.cluster;
   if (p.epi == EPI_LSE || p.epi == EPI_DZ || p.epi == EPI_LSE_Z) {
     const int g = u / m_groups;
@@ -100,7 +109,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                    const __grid_constant__ CUtensorMap tmap_c, const GemmProblem p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  using G = Geo<CG>;
+  using G = GeoOf<EPI, CG>;
   uint8_t* stage_base = smem;
   uint8_t* staging = smem + size_t(G::kStages) * G::kStage;  // 1024-aligned output boxes of the epilogue warps
   GemmSmemTail* tail = reinterpret_cast<GemmSmemTail*>(staging + STAGING_BYTES);
@@ -150,7 +159,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       bool ok = true;
       for (int u = u_first; u < p.n_units && ok; u += u_step) {
         int m_blk, n_first, n_count, kb_lo, kb_hi, split;
-        unit_coords(p, u, crank, m_blk, n_first, n_count, kb_lo, kb_hi, split);
+        unit_coords(p, u, crank, G::kKB, m_blk, n_first, n_count, kb_lo, kb_hi, split);
         for (int nb = n_first; nb < n_first + n_count && ok; ++nb) {
           for (int kb = kb_lo; kb < kb_hi; ++kb, ++it) {
             const uint32_t s = it % G::kStages;
@@ -165,35 +174,44 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
               // both CTAs' halves complete on the first CTA's barrier, where the MMA waits
               const uint32_t bar0 = mapa_u32(&tail->full[s], 0);
               if (crank == 0) mbar_arrive_expect_tx(&tail->full[s], 2 * G::kStage);
+              // stage kb = k-blocks kKB kb .. kKB kb + kKB - 1, elements k0 .. k0 + 64 kKB - 1
+              const int k0 = kb * BK * G::kKB;
               if (p.a_blocked) {
-                if (p.a_mn == 0) {
-                  tma_load_3d_pair(sa, &tmap_a, bar0, 0, m_blk * BM, kb);
-                } else if (p.a_box2) {
-                  tma_load_3d_pair(sa, &tmap_a, bar0, 0, kb * BK, m_blk * (BM / 64));
+                // blocked dZ [vocab/64][row][64]: K-major takes 128 rows of kKB vocabulary
+                // blocks, MN-major two vocabulary blocks of 64 kKB rows (tokens)
+                if (p.a_mn == 0) tma_load_3d_pair(sa, &tmap_a, bar0, 0, m_blk * BM, kb * G::kKB);
+                else tma_load_3d_pair(sa, &tmap_a, bar0, 0, k0, m_blk * (BM / 64));
+              } else if (p.a_mn == 0) {
+                if (p.a_k3d) {
+                  tma_load_3d_pair(sa, &tmap_a, bar0, 0, m_blk * BM, kb * G::kKB);
                 } else {
 #pragma unroll
-                  for (int j = 0; j < BM / 64; ++j)
-                    tma_load_3d_pair(sa + j * 8192, &tmap_a, bar0, 0, kb * BK, m_blk * (BM / 64) + j);
+                  for (int j = 0; j < G::kKB; ++j)
+                    tma_load_2d_pair(sa + j * (G::kA / G::kKB), &tmap_a, bar0, k0 + j * BK, m_blk * BM);
                 }
-              } else if (p.a_mn == 0) {
-                tma_load_2d_pair(sa, &tmap_a, bar0, kb * BK, m_blk * BM);
               } else if (p.a_box2) {
-                tma_load_3d_pair(sa, &tmap_a, bar0, 0, kb * BK, m_blk * (BM / 64));
+                tma_load_3d_pair(sa, &tmap_a, bar0, 0, k0, m_blk * (BM / 64));
               } else {
 #pragma unroll
                 for (int j = 0; j < BM / 64; ++j)
-                  tma_load_2d_pair(sa + j * 8192, &tmap_a, bar0, m_blk * BM + j * 64, kb * BK);
+                  tma_load_2d_pair(sa + j * (G::kA / 2), &tmap_a, bar0, m_blk * BM + j * 64, k0);
               }
               // this CTA's 128 columns of the pair's 256-column B tile
+              const int col = nb * BN + int(crank) * (BN / 2);
               if (p.b_mn == 0) {
-                tma_load_2d_pair(sb, &tmap_b, bar0, kb * BK, nb * BN + int(crank) * (BN / 2));
+                if (p.b_k3d) {
+                  tma_load_3d_pair(sb, &tmap_b, bar0, 0, col, kb * G::kKB);
+                } else {
+#pragma unroll
+                  for (int j = 0; j < G::kKB; ++j)
+                    tma_load_2d_pair(sb + j * (G::kB / G::kKB), &tmap_b, bar0, k0 + j * BK, col);
+                }
               } else if (p.b_box2) {
-                tma_load_3d_pair(sb, &tmap_b, bar0, 0, kb * BK, (nb * BN + int(crank) * (BN / 2)) / 64);
+                tma_load_3d_pair(sb, &tmap_b, bar0, 0, k0, col / 64);
               } else {
 #pragma unroll
                 for (int j = 0; j < BN / 128; ++j)
-                  tma_load_2d_pair(sb + j * 8192, &tmap_b, bar0, nb * BN + (int(crank) * (BN / 128) + j) * 64,
-                                   kb * BK);
+                  tma_load_2d_pair(sb + j * (G::kB / 2), &tmap_b, bar0, col + j * 64, k0);
               }
               continue;
             }
@@ -253,15 +271,16 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && (CG == 1 || crank == 0)) {  // a pair's MMAs are issued by its first CTA
       const uint32_t idesc = idesc_bf16_f32(BM * CG, BN, p.a_mn, p.b_mn);
-      const uint32_t a_step = p.a_mn ? 16u * 128u : 32u;
-      const uint32_t b_step = p.b_mn ? 16u * 128u : 32u;
-      const uint32_t a_lbo = p.a_mn ? 8192u : 16u;
-      const uint32_t b_lbo = p.b_mn ? 8192u : 16u;
+      // A 16-deep step kk of a stage: K-major operands hold each k-block as rows of 128 B
+      // (the second k-block kA / 2 or kB / 2 further on), MN-major ones hold each 64-column
+      // block as kKB * 64 rows of 128 B (LBO between the blocks).
+      const uint32_t a_lbo = p.a_mn ? uint32_t(BK * G::kKB * 128) : 16u;
+      const uint32_t b_lbo = p.b_mn ? uint32_t(BK * G::kKB * 128) : 16u;
       uint32_t it = 0, acc_it = 0;
       bool ok = true;
       for (int u = u_first; u < p.n_units && ok; u += u_step) {
         int m_blk, n_first, n_count, kb_lo, kb_hi, split;
-        unit_coords(p, u, crank, m_blk, n_first, n_count, kb_lo, kb_hi, split);
+        unit_coords(p, u, crank, G::kKB, m_blk, n_first, n_count, kb_lo, kb_hi, split);
         for (int nb = n_first; nb < n_first + n_count && ok; ++nb, ++acc_it) {
           const uint32_t a = acc_it & 1u;
           const uint32_t aph = (acc_it >> 1) & 1u;
@@ -281,10 +300,16 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             tc_fence_after();
             const uint32_t sa = smem_u32(stage_base + size_t(s) * G::kStage);
             const uint32_t sb = sa + G::kA;
+            // 16-deep steps of this stage inside K (a pair's last stage may hold one
+            // k-block of zeros past the end of K: skip its MMAs)
+            const int ksteps = (p.K - kb * BK * G::kKB + 15) / 16;
 #pragma unroll
-            for (int k = 0; k < BK / 16; ++k) {
-              const uint64_t ad = sdesc_sw128(sa + k * a_step, a_lbo);
-              const uint64_t bd = sdesc_sw128(sb + k * b_step, b_lbo);
+            for (int k = 0; k < G::kKB * (BK / 16); ++k) {
+              if (CG == 2 && k >= BK / 16 && k >= ksteps) break;
+              const uint32_t a_off = p.a_mn ? uint32_t(k) * 2048u : uint32_t(k >> 2) * (G::kA / G::kKB) + (k & 3) * 32u;
+              const uint32_t b_off = p.b_mn ? uint32_t(k) * 2048u : uint32_t(k >> 2) * (G::kB / G::kKB) + (k & 3) * 32u;
+              const uint64_t ad = sdesc_sw128(sa + a_off, a_lbo);
+              const uint64_t bd = sdesc_sw128(sb + b_off, b_lbo);
               if (CG == 2) umma_bf16_pair(d_tmem, ad, bd, idesc, (kb != kb_lo || k != 0) ? 1u : 0u);
               else umma_bf16(d_tmem, ad, bd, idesc, (kb != kb_lo || k != 0) ? 1u : 0u);
             }
@@ -314,7 +339,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     bool ok = true;
     for (int u = u_first; u < p.n_units && ok; u += u_step) {
       int m_blk, n_first, n_count, kb_lo, kb_hi, split;
-      unit_coords(p, u, crank, m_blk, n_first, n_count, kb_lo, kb_hi, split);
+      unit_coords(p, u, crank, G::kKB, m_blk, n_first, n_count, kb_lo, kb_hi, split);
       const int row = m_blk * BM + r_local;
 
       // Per-row state for the loss epilogues.
@@ -603,14 +628,14 @@ static cudaError_t launch_one(const GemmProblem& p, const CUtensorMap& ta, const
   static int max_pairs = 0;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kd_gemm_kernel<EPI, CG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         int(Geo<CG>::kSmem));
+                                         int(GeoOf<EPI, CG>::kSmem));
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   cfg.blockDim = dim3(GEMM_THREADS, 1, 1);
-  cfg.dynamicSmemBytes = Geo<CG>::kSmem;
+  cfg.dynamicSmemBytes = GeoOf<EPI, CG>::kSmem;
   cfg.stream = s;
   if (p.cluster > 1) {
     attr[0].id = cudaLaunchAttributeClusterDimension;

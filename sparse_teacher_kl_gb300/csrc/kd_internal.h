@@ -53,6 +53,12 @@ enum EpiKind : int {
   EPI_LSE_Z = 4,  // forward-chunked: EPI_LSE plus the raw logits z -> bf16, blocked [V/64][N][64]
 };
 
+// 64-deep k-blocks per ring stage of a CTA-pair launch: two for the loss epilogues
+// (K-major H and W, each stage one depth-2 box per operand), one for the gradient
+// products (MN-major operands; more, shallower stages measured faster there).  The
+// tensor maps of a pair launch are sized for this depth.
+constexpr int pair_kblocks(int epi) { return (epi == EPI_LSE || epi == EPI_DZ || epi == EPI_LSE_Z) ? 2 : 1; }
+
 struct GemmProblem {
   int M, N, K;           // logical GEMM sizes
   int a_mn, b_mn;        // operand major-ness (0 = K-major)
@@ -72,6 +78,9 @@ struct GemmProblem {
   // a stage come in one TMA box of depth 2 from a 3-D map (64, k, blocks), 8 KB apart in
   // shared memory as the MMA reads them; 0: two boxes from a 2-D (or depth-1) map.
   int a_box2, b_box2;
+  // a_k3d / b_k3d (CTA pairs with two k-blocks per stage, K-major operand): both come in
+  // one box of depth 2 from a 3-D view (64, rows, K / 64); 0: one box per k-block.
+  int a_k3d, b_k3d;
   int z_row0;                 // EPI_LSE_Z: row of the stored logits that chunk row 0 maps to
   // cluster = 2 or 4: the CTAs of a cluster take consecutive m tiles of the same n tile
   // and share the B operand: each loads 1/cluster of it (K-major B map box 64 x 256/cluster)
@@ -117,7 +126,8 @@ bool make_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint6
 bool make_tmap_dz_blocked(CUtensorMap* map, const void* base, uint64_t rows, uint64_t rows_pad, uint64_t nvb,
                           uint32_t box_rows, uint32_t box_depth = 1);
 // 3-D view (64, rows, cols / 64) of a row-major bf16 matrix whose column count is a
-// multiple of 64, box (64, box_rows, 2): two 64-column blocks per TMA box.
+// multiple of 64, box (64, box_rows, 2): two 64-column blocks per TMA box (two k-blocks
+// of a K-major operand, or two column blocks of an MN-major one).
 bool make_tmap_mn2_bf16(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows, uint64_t row_stride_bytes,
                         uint32_t box_rows);
 bool make_tmap_2d_f32(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
