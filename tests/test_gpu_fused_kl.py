@@ -94,6 +94,8 @@ def test_grad_H_bf16_output(kd, cuda_device):
     (257, 136, 1001, 33, 256),    # V not a multiple of 8 (padded dZ rows), 2 chunks, 1-row tail
     (128, 64, 256, 256, 128),     # K = V: the sparse teacher is the whole vocabulary
     (640, 520, 2560, 64, 384),    # several tiles in every direction
+    (512, 192, 3000, 20, 256),    # CTA pairs, d = 3 k-blocks: the last stage's depth-2 box half past d
+    (600, 320, 2100, 10, 256),    # CTA pairs over 5 k-blocks, then a single-CTA 88-row chunk
 ])
 def test_ragged_shapes(kd, cuda_device, N, d, V, K, chunk):
     w = Workload("ragged", 1, N, d, V, K, chunk, "normal3", 0.9, 4242 + N)
