@@ -197,9 +197,9 @@ static void set_cluster(GemmProblem& p) {
 // Number of K splits for a product of `tiles` output tiles with `k_blocks` steps of
 // BK each: the fewest waves of `grid` persistent CTAs per unit of work, with a small
 // charge per split for the extra partial traffic.
-// The loss launches below build depth-2 K-major boxes (a_k3d / b_k3d) for CTA pairs.
-static_assert(pair_kblocks(EPI_LSE) == 2 && pair_kblocks(EPI_DZ) == 2 && pair_kblocks(EPI_LSE_Z) == 2,
-              "loss epilogues take two k-blocks per pair stage");
+// The loss sweeps and the teacher projection (both operands K-major) build depth-2
+// K-major boxes (a_k3d / b_k3d) for CTA pairs.
+static_assert(pair_kblocks(0, 0) == 2, "K-major operand pairs take two k-blocks per pair stage");
 
 static int choose_splits(int64_t tiles, int k_blocks, int grid) {
   int best = 1;
@@ -467,11 +467,11 @@ static int bwd_impl(const void* H_bf16, const void* W_bf16, const int32_t* t_ids
   const size_t gh_elt = grad_H_is_fp32 ? 4 : 2;
 
   alignas(64) CUtensorMap tw_k, tw_k_half, tw_mn, tw_mn2, th_k, th_mn, th_mn2, tdz_k, tdz_mn, tdz_st, tgw;
-  // CTA-pair launches take pair_kblocks(epi) 64-deep k-blocks per ring stage: boxes of
+  // CTA-pair launches take pair_kblocks(a_mn, b_mn) 64-deep k-blocks per ring stage: boxes of
   // 64 kq (grad_H) / 64 kr (grad_W) rows for MN-major operands, that depth for K-major
   // ones (suffix _p); the dZ recompute takes two (tw_k2, th_k2: depth-2 boxes)
   alignas(64) CUtensorMap tw_k2, tw_mn_p, th_k2, th_mn_p, tdz_k_p, tdz_mn_p;
-  const int kq = pair_kblocks(EPI_STORE), kr = pair_kblocks(EPI_ACCUM);
+  const int kq = pair_kblocks(0, 1), kr = pair_kblocks(1, 1);  // grad_H, grad_W
   const bool d64 = d % 64 == 0;  // 3-D two-block views of W and H need whole 64-column blocks
   if (!make_tmap_2d_bf16(&tw_k, W_bf16, uint64_t(d), uint64_t(V), uint64_t(d) * 2, BK, BN)) return KD_ERR_CUDA;
   if (!make_tmap_2d_bf16(&tw_k_half, W_bf16, uint64_t(d), uint64_t(V), uint64_t(d) * 2, BK, BN / 2))
@@ -671,7 +671,7 @@ int kd_gemm_bf16(const void* A, const void* B, float* C, int64_t M, int64_t N, i
   if (p.cta_pair) {
     // kk 64-deep k-blocks per ring stage; each operand in one box where whole 64-column
     // blocks allow (MN-major: both column blocks; K-major: kk = 2 k-blocks, depth 2)
-    const int kk = pair_kblocks(p.epi);
+    const int kk = pair_kblocks(a_mn ? 1 : 0, b_mn ? 1 : 0);
     p.a_box2 = a_mn && M % 64 == 0;
     p.a_k3d = kk == 2 && !a_mn && K % 64 == 0;
     p.b_box2 = b_mn && N % 64 == 0;

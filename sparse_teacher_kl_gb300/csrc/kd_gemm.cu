@@ -40,15 +40,15 @@ struct __align__(8) GemmSmemTail {
 
 // Shared-memory ring per CTA.  One CTA per tile (CG = 1): a stage holds A 128 x 64 and
 // B 256 x 64 (48 KB), 4 stages.  CTA pair per tile (CG = 2, tcgen05 cta_group::2): each
-// CTA holds its 128 rows of A and its 128 columns of B for KKB 64-deep k-blocks: the
-// loss epilogues take two (64 KB, 3 stages; every operand of a stage in one depth-2
-// TMA box), the gradient products one (32 KB, PAIR_PRODUCT_STAGES stages).
-constexpr int PAIR_PRODUCT_STAGES = 6;
+// CTA holds its 128 rows of A and its 128 columns of B for KKB 64-deep k-blocks: two
+// when both operands are K-major (64 KB, 3 stages; every operand of a stage in one
+// depth-2 TMA box), else one (32 KB, PAIR_ONE_BLOCK_STAGES stages).
+constexpr int PAIR_ONE_BLOCK_STAGES = 6;
 
 template <int CG, int KKB>
 struct Geo {
   static constexpr int kKB = KKB;  // 64-deep k-blocks per stage
-  static constexpr int kStages = CG == 1 ? STAGES : (KKB == 2 ? 3 : PAIR_PRODUCT_STAGES);
+  static constexpr int kStages = CG == 1 ? STAGES : (KKB == 2 ? 3 : PAIR_ONE_BLOCK_STAGES);
   static constexpr int kA = STAGE_A_BYTES * kKB;
   static constexpr int kB = (CG == 2 ? STAGE_B_BYTES / 2 : STAGE_B_BYTES) * kKB;
   static constexpr int kStage = kA + kB;
@@ -58,9 +58,6 @@ struct Geo {
   static_assert(kStages <= MAX_STAGES, "barrier arrays");
   static_assert(kSmem <= 232448, "shared memory budget of one CTA");
 };
-
-template <int EPI, int CG>
-using GeoOf = Geo<CG, CG == 2 ? pair_kblocks(EPI) : 1>;
 
 // Unit u -> tile coordinates.  LSE/DZ walk the vocabulary (n) slowly so that
 // every CTA in flight reads the same few W tiles while the small H chunk stays
@@ -103,13 +100,13 @@ __device__ __forceinline__ void unit_coords(const GemmProblem& p, int u, uint32_
   }
 }
 
-template <int EPI, int CG>
+template <int EPI, int CG, int KKB>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     kd_gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                    const __grid_constant__ CUtensorMap tmap_c, const GemmProblem p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  using G = GeoOf<EPI, CG>;
+  using G = Geo<CG, KKB>;
   uint8_t* stage_base = smem;
   uint8_t* staging = smem + size_t(G::kStages) * G::kStage;  // 1024-aligned output boxes of the epilogue warps
   GemmSmemTail* tail = reinterpret_cast<GemmSmemTail*>(staging + STAGING_BYTES);
@@ -621,21 +618,21 @@ int gemm_max_grid() {
   return g_num_sms;
 }
 
-template <int EPI, int CG>
+template <int EPI, int CG, int KKB = 1>
 static cudaError_t launch_one(const GemmProblem& p, const CUtensorMap& ta, const CUtensorMap& tb,
                               const CUtensorMap& tc, int grid, cudaStream_t s) {
   static bool attr_set = false;
   static int max_pairs = 0;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kd_gemm_kernel<EPI, CG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         int(GeoOf<EPI, CG>::kSmem));
+    cudaError_t e = cudaFuncSetAttribute(kd_gemm_kernel<EPI, CG, KKB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         int(Geo<CG, KKB>::kSmem));
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   cfg.blockDim = dim3(GEMM_THREADS, 1, 1);
-  cfg.dynamicSmemBytes = GeoOf<EPI, CG>::kSmem;
+  cfg.dynamicSmemBytes = Geo<CG, KKB>::kSmem;
   cfg.stream = s;
   if (p.cluster > 1) {
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -648,7 +645,7 @@ static cudaError_t launch_one(const GemmProblem& p, const CUtensorMap& ta, const
       // persistent grid: as many pairs as can be resident at once
       cfg.gridDim = dim3(unsigned((gemm_max_grid() / p.cluster) * p.cluster), 1, 1);
       int n = 0;
-      if (cudaOccupancyMaxActiveClusters(&n, kd_gemm_kernel<EPI, CG>, &cfg) != cudaSuccess || n < 1) n = 1;
+      if (cudaOccupancyMaxActiveClusters(&n, kd_gemm_kernel<EPI, CG, KKB>, &cfg) != cudaSuccess || n < 1) n = 1;
       max_pairs = n;
     }
     int pairs = grid / p.cluster;
@@ -661,7 +658,7 @@ static cudaError_t launch_one(const GemmProblem& p, const CUtensorMap& ta, const
     cfg.attrs = nullptr;
     cfg.numAttrs = 0;
   }
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kd_gemm_kernel<EPI, CG>, ta, tb, tc, p);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kd_gemm_kernel<EPI, CG, KKB>, ta, tb, tc, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -685,12 +682,18 @@ cudaError_t launch_gemm(const GemmProblem& p, const CUtensorMap& ta, const CUten
   cudaError_t e;
   if (p.cta_pair) {
     if (p.cluster != 2) return cudaErrorInvalidValue;
+    const bool two = pair_kblocks(p.a_mn, p.b_mn) == 2;
     switch (p.epi) {
-      case EPI_LSE: e = launch_one<EPI_LSE, 2>(p, ta, tb, tc, grid, s); break;
-      case EPI_LSE_Z: e = launch_one<EPI_LSE_Z, 2>(p, ta, tb, tc, grid, s); break;
-      case EPI_DZ: e = launch_one<EPI_DZ, 2>(p, ta, tb, tc, grid, s); break;
-      case EPI_STORE: e = launch_one<EPI_STORE, 2>(p, ta, tb, tc, grid, s); break;
-      default: e = launch_one<EPI_ACCUM, 2>(p, ta, tb, tc, grid, s); break;
+      // the loss sweeps read H and W K-major: always two k-blocks per stage
+      case EPI_LSE: e = two ? launch_one<EPI_LSE, 2, 2>(p, ta, tb, tc, grid, s) : cudaErrorInvalidValue; break;
+      case EPI_LSE_Z: e = two ? launch_one<EPI_LSE_Z, 2, 2>(p, ta, tb, tc, grid, s) : cudaErrorInvalidValue; break;
+      case EPI_DZ: e = two ? launch_one<EPI_DZ, 2, 2>(p, ta, tb, tc, grid, s) : cudaErrorInvalidValue; break;
+      case EPI_STORE:
+        e = two ? launch_one<EPI_STORE, 2, 2>(p, ta, tb, tc, grid, s) : launch_one<EPI_STORE, 2, 1>(p, ta, tb, tc, grid, s);
+        break;
+      default:
+        e = two ? launch_one<EPI_ACCUM, 2, 2>(p, ta, tb, tc, grid, s) : launch_one<EPI_ACCUM, 2, 1>(p, ta, tb, tc, grid, s);
+        break;
     }
   } else {
     switch (p.epi) {

@@ -53,11 +53,11 @@ enum EpiKind : int {
   EPI_LSE_Z = 4,  // forward-chunked: EPI_LSE plus the raw logits z -> bf16, blocked [V/64][N][64]
 };
 
-// 64-deep k-blocks per ring stage of a CTA-pair launch: two for the loss epilogues
-// (K-major H and W, each stage one depth-2 box per operand), one for the gradient
-// products (MN-major operands; more, shallower stages measured faster there).  The
-// tensor maps of a pair launch are sized for this depth.
-constexpr int pair_kblocks(int epi) { return (epi == EPI_LSE || epi == EPI_DZ || epi == EPI_LSE_Z) ? 2 : 1; }
+// 64-deep k-blocks per ring stage of a CTA-pair launch: two when both operands are
+// K-major (the loss sweeps and the teacher projection: each stage one depth-2 box per
+// operand), one otherwise (the gradient products, MN-major operands: more, shallower
+// stages measured faster there).  The tensor maps of a pair launch are sized for this.
+constexpr int pair_kblocks(int a_mn, int b_mn) { return (a_mn == 0 && b_mn == 0) ? 2 : 1; }
 
 struct GemmProblem {
   int M, N, K;           // logical GEMM sizes

@@ -131,15 +131,21 @@ def test_topk_dropped_mass(kd, cuda_device):
     assert np.all(ref >= -1e-12)
 
 
-def test_teacher_topk_exact_integer_logits(kd, cuda_device):
-    """Small-integer teacher hidden states and weights make every logit an exact bf16 integer, so the
-    fused projection + top-K must match the oracle's cache of the exact logits bit for bit (with
-    many ties, broken by the lower id)."""
-    g = torch.Generator().manual_seed(21)
-    N, dt, V, K = 300, 64, 5000, 37
+@pytest.mark.parametrize("N,dt,chunk", [
+    (300, 64, 128),   # one row tile per chunk: single-CTA tiles
+    (300, 192, 256),  # CTA pairs, 3 k-blocks, then a 44-row single-CTA chunk
+    (700, 320, 384),  # CTA pairs over 3 row tiles (the pair's phantom tile stores nothing)
+    (600, 200, 256),  # dt not a multiple of 64: a ragged last k-block
+])
+def test_teacher_topk_exact_integer_logits(kd, cuda_device, N, dt, chunk):
+    """Small-integer teacher hidden states and weights make every logit an integer that fp32 holds
+    exactly, rounded once to bf16, so the fused projection + top-K must match the oracle's cache of
+    the logits bit for bit (with many ties, broken by the lower id)."""
+    g = torch.Generator().manual_seed(21 + dt)
+    V, K = 5000, 37
     Ht = torch.randint(-2, 3, (N, dt), generator=g).to(torch.bfloat16)
     Wt = torch.randint(-2, 3, (V, dt), generator=g).to(torch.bfloat16)
-    ids, vals, lse = kd.teacher_topk(Ht.to(cuda_device), Wt.to(cuda_device), K, chunk=128, with_lse=True)
+    ids, vals, lse = kd.teacher_topk(Ht.to(cuda_device), Wt.to(cuda_device), K, chunk=chunk, with_lse=True)
     torch.cuda.synchronize()
     zbits = oracle.teacher_logits_bf16(bf16_bits(Ht), bf16_bits(Wt))
     rid, rval = oracle.topk_cache(zbits, K)
@@ -149,14 +155,15 @@ def test_teacher_topk_exact_integer_logits(kd, cuda_device):
     assert np.max(np.abs(lse.cpu().numpy() - ref_lse)) <= 1e-5 * np.max(np.abs(ref_lse))
 
 
-def test_teacher_topk_random_is_a_valid_topk(kd, cuda_device):
+@pytest.mark.parametrize("N,dt,chunk", [(260, 200, 128), (520, 256, 256)])
+def test_teacher_topk_random_is_a_valid_topk(kd, cuda_device, N, dt, chunk):
     """Random teacher inputs: the kept values are the logits rounded to bf16 (within one bf16 step of the
     float64 product) and no logit left out exceeds the smallest kept one by more than that rounding."""
     g = torch.Generator().manual_seed(22)
-    N, dt, V, K = 260, 200, 3001, 50
+    V, K = 3001, 50
     Ht = torch.randn((N, dt), generator=g).to(torch.bfloat16)
     Wt = (torch.randn((V, dt), generator=g) / 14).to(torch.bfloat16)
-    ids, vals = kd.teacher_topk(Ht.to(cuda_device), Wt.to(cuda_device), K, chunk=128)
+    ids, vals = kd.teacher_topk(Ht.to(cuda_device), Wt.to(cuda_device), K, chunk=chunk)
     torch.cuda.synchronize()
     z = oracle.bf16_to_f64(bf16_bits(Ht)) @ oracle.bf16_to_f64(bf16_bits(Wt)).T
     ids, vals = ids.cpu().numpy(), vals.cpu().numpy().astype(np.float64)
