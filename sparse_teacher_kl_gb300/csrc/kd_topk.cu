@@ -455,6 +455,9 @@ constexpr int TW_STEP = 32 * TK_VEC;         // elements per warp step
 constexpr int TW_GROUP = 4;                  // steps tested together (one vote)
 constexpr int TW_QUEUE = 64;                 // queued vectors per warp (ring)
 constexpr float TW_LOG2E = 1.4426950408889634f;
+// Margin of a guessed threshold below the previous row's K-th value, in units of that
+// row's spacing between its (K/2)-th and K-th values (about rank 2.8 K for normal rows).
+constexpr float TW_GUESS_MARGIN = 1.5f;
 
 // A configuration: CAP candidate entries per warp, WARPS rows in flight per block (one
 // block per SM), BATCH queued vectors filtered per drain (at most 8 * BATCH new
@@ -627,6 +630,14 @@ __device__ __forceinline__ float vec_max(const uint4& v) {
 __device__ __forceinline__ float key_to_float(uint32_t key) {
   const uint32_t b = (key & 0x8000u) ? (key & 0x7FFFu) : (~key & 0xFFFFu);
   return __uint_as_float(b << 16);
+}
+
+// Key of the largest bf16 value <= x (x finite): x rounded toward -infinity.
+__device__ __forceinline__ uint32_t key_floor(float x) {
+  const uint32_t f = __float_as_uint(x);
+  uint32_t b = f >> 16;
+  if ((f & 0x80000000u) && (f & 0xFFFFu)) ++b;  // negative: round the magnitude up
+  return bf16_key(b);
 }
 
 // Per-warp selection state (warp-uniform).
@@ -917,6 +928,44 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
+// The lane's vectors of warp steps s0 .. s0 + TW_GROUP - 1 of a row, read directly
+// (past the row: -inf, nothing read).
+__device__ __forceinline__ void load_group(uint4* v, const uint16_t* xr, int64_t V, int s0) {
+#pragma unroll
+  for (int k = 0; k < TW_GROUP; ++k) {
+    const int64_t i0 = int64_t(s0 + k) * TW_STEP + int64_t(lane_id()) * TK_VEC;
+    v[k] = i0 + TK_VEC <= V ? __ldcs(reinterpret_cast<const uint4*>(xr + i0)) : load_step(xr, V, s0 + k);
+  }
+}
+
+// Warp: the whole selection of one row again, read directly from global memory (the next
+// group's loads in flight while a group is tested), every element a candidate until the
+// list holds K.  Out of line: it runs only after a guessed threshold turned out too high.
+template <class C>
+__device__ __noinline__ WarpSel warp_reselect(TopkWarpSmem<C::CAP>& ws, const uint16_t* xr, int64_t V, int nst,
+                                              uint32_t V32, uint32_t K) {
+  WarpSel st;
+  st.cnt = 0;
+  st.qh = 0;
+  st.nq = 0;
+  st.wth = 0;
+  st.ge = true;
+  st.tv = key_to_float(0);
+  float lm = -INFINITY, ls = 0.f;  // unused: no logsumexp here
+  uint4 a[TW_GROUP], b[TW_GROUP];
+  load_group(a, xr, V, 0);
+  for (int s0 = 0; s0 < nst; s0 += TW_GROUP) {
+    if (s0 + TW_GROUP < nst) load_group(b, xr, V, s0 + TW_GROUP);
+    const uint32_t live = nst - s0 >= TW_GROUP ? (1u << TW_GROUP) - 1u : (1u << (nst - s0)) - 1u;
+    test_group<C, false>(ws, st, a, s0, live, lm, ls, V32, K);
+#pragma unroll
+    for (int k = 0; k < TW_GROUP; ++k) a[k] = b[k];
+  }
+  __syncwarp();
+  while (st.nq > 0) st = warp_drain<C>(ws, st, min(st.nq, uint32_t(C::BATCH)), V32, K);
+  return st;
+}
+
 template <class C, bool WITH_LSE>
 __global__ void __launch_bounds__(C::WARPS * 32, 1)
     kd_topk_tma_kernel(const uint16_t* __restrict__ X, int64_t N, int64_t V, int64_t ld, int K,
@@ -970,6 +1019,9 @@ __global__ void __launch_bounds__(C::WARPS * 32, 1)
 
   uint32_t gidx = 0;  // groups consumed
   bool ok = true;
+  // Guessed threshold for the warp's next row (0: none) and the margin factor behind it.
+  uint32_t guess = 0;
+  float margin = TW_GUESS_MARGIN;
   for (; row < N; row += nwarps) {
     const uint16_t* xr = X + row * ld;
     WarpSel st;
@@ -981,11 +1033,19 @@ __global__ void __launch_bounds__(C::WARPS * 32, 1)
     st.tv = key_to_float(0);
     float lm = -INFINITY, ls = 0.f;
 
-    // Quick start: the ring holds this row's first RING groups (none of them the row's
-    // last).  The K-th largest of their per-lane vector maxima is reached by at least K
-    // elements, so every element of the top K has a key >= it: those groups are then
+    // Guessed start (every row after a warp's first, K >= 16): the threshold is a key taken
+    // from the previous row's best K (below).  If at least K elements reach it, the top K
+    // all do and the row is selected exactly; if not, the list ends short of K and the row
+    // is selected again from its start with no threshold.
+    // Quick start (otherwise): the ring holds this row's first RING groups (none of them the
+    // row's last).  The K-th largest of their per-lane vector maxima is reached by at least
+    // K elements, so every element of the top K has a key >= it: those groups are then
     // consumed with that threshold (>=), and the rest of the row with the raised ones.
-    if (ngr > C::RING && K <= C::RING * C::GRP * 32) {
+    const bool guessed = guess != 0u;
+    if (guessed) {
+      st.wth = guess;
+      st.tv = key_to_float(guess - 1u == 0x7FFFu ? 0x7FFEu : guess - 1u);
+    } else if (ngr > C::RING && K <= C::RING * C::GRP * 32) {
       for (int r = 0; r < C::RING && ok; ++r) {
         const uint32_t u = gidx + uint32_t(r);
         ok = mbar_wait(&ts.full[u & (C::RING - 1)], (u / C::RING) & 1u, &ts.abort, err, 0x72u);
@@ -1048,6 +1108,20 @@ __global__ void __launch_bounds__(C::WARPS * 32, 1)
     if (!ok) break;
     __syncwarp();
     while (st.nq > 0) st = warp_drain<C>(ws, st, min(st.nq, uint32_t(C::BATCH)), V32, Ku);
+    if (guessed && st.cnt < Ku) {
+      // fewer than K elements reach the guess (the logsumexp of the pass is complete)
+      st = warp_reselect<C>(ws, xr, V, nst, V32, Ku);
+      margin *= 4.f;  // a wider margin for the rows after a miss
+    }
+    if (K >= 16) {
+      // Next guess: the K-th best value lowered by margin x (its distance to the (K/2)-th).
+      // For tails like the normal's or the logistic's the top order statistics are spaced
+      // about logarithmically in rank, so margin m lands near rank 2^m K of a row like this.
+      const float vk = key_to_float(comp_key(ws.buf[K - 1]));
+      const float vh = key_to_float(comp_key(ws.buf[K / 2 - 1]));
+      const float g = vk - margin * (vh - vk);
+      guess = (g > -INFINITY && g < INFINITY) ? key_floor(g) : 0u;  // none after a NaN or an infinity
+    }
 
     if (WITH_LSE) {
       for (int o = 16; o > 0; o >>= 1) {

@@ -58,13 +58,40 @@ def test_topk_random(kd, cuda_device, N, V, K):
 
 @pytest.mark.parametrize("N,V,K", [(700, 4097, 100), (650, 12289, 7), (610, 20483, 256), (400, 33333, 100),
                                    (257, 9000, 128), (333, 16411, 129)])
-def test_topk_many_rows_per_block(kd, cuda_device, N, V, K):
-    """More rows than resident warps (each warp streams several rows, its copies running
-    on into the next row while it sorts the current one), rows of 17 to 131 warp steps with
-    a ragged end, K on both sides of the boundary between the two buffer sizes and at the
-    streaming path's limit."""
+def test_topk_rows_of_many_steps(kd, cuda_device, N, V, K):
+    """Rows of 17 to 131 warp steps with a ragged end, K on both sides of the boundary
+    between the two buffer sizes and at the streaming path's limit."""
     X = make_dense_teacher_logits(N, V, seed=N * 7 + K)
     _check(kd, X, K, cuda_device)
+
+
+# Resident row warps of the streaming path: one block of 15 (K <= 128) or 12 (K <= 256)
+# per SM, 152 SMs; the cases below give every warp at least three rows.
+@pytest.mark.parametrize("N,V,K", [(7000, 4097, 100), (5600, 6151, 256), (7001, 2053, 16), (6900, 3001, 7)])
+def test_topk_many_rows_per_warp(kd, cuda_device, N, V, K):
+    """Each warp streams several rows, its copies running on into the next row while it
+    sorts the current one, and (K >= 16) starts every row after its first from a threshold
+    guessed from the row before."""
+    X = make_dense_teacher_logits(N, V, seed=N * 3 + K)
+    _check(kd, X, K, cuda_device)
+
+
+def test_topk_guessed_threshold_misses(kd, cuda_device):
+    """Rows whose scale and offset jump from one row to the next, rows of few distinct
+    values and rows with infinities: the threshold guessed from a warp's previous row is
+    often above the K-th value, and the row is then selected again from its start."""
+    g = torch.Generator().manual_seed(9)
+    N, V = 7000, 3001
+    X = torch.randn((N, V), generator=g)
+    scale = 10.0 ** (torch.rand((N, 1), generator=g) * 6 - 3)
+    shift = torch.randint(-50, 51, (N, 1), generator=g).float()
+    X = X * scale + shift
+    X[1::7] = torch.randint(-3, 4, (len(range(1, N, 7)), V), generator=g).float()  # few distinct values
+    X[2::11, ::97] = float("inf")
+    X[3::13, ::5] = float("-inf")
+    X = X.to(torch.bfloat16)
+    for K in (16, 100, 200):
+        _check(kd, X, K, cuda_device)
 
 
 def test_topk_ties_and_signed_zero(kd, cuda_device):
