@@ -103,7 +103,9 @@ KD_API int kd_topk_cache(const void* logits_bf16, int64_t N, int64_t V, int64_t 
  * (fp32 accumulation, rounded once to bf16 as a bf16 teacher would emit them) into a
  * [chunk, V] workspace buffer and reduced to their top K right away, so the dense
  * [N, V] teacher logits never exist.  Outputs as kd_topk_cache (ids, vals, optional
- * row logsumexp).  dt % 8 == 0; chunk a multiple of 128.
+ * row logsumexp).  dt % 8 == 0; chunk a multiple of 128.  The workspace also holds
+ * 16 KB of per-warp selection thresholds carried from one chunk's rows to the next's
+ * (a start guess, verified per row: results never depend on it).
  */
 KD_API size_t kd_teacher_topk_workspace(int64_t N, int64_t dt, int64_t V, int K, int64_t chunk);
 KD_API int kd_teacher_topk(const void* Ht_bf16, const void* Wt_bf16, int64_t N, int64_t dt, int64_t V, int K,

@@ -287,7 +287,7 @@ static size_t teacher_topk_ws(int64_t N, int64_t V, int64_t chunk) {
   const int64_t c = chunk < N ? chunk : N;
   const int64_t rows_pad = (c + BM - 1) / BM * BM;
   const int64_t ldz = (V + 7) / 8 * 8;
-  return sizeof(Ctrl) + align_up(size_t(rows_pad) * size_t(ldz) * 2, 256);
+  return sizeof(Ctrl) + align_up(size_t(rows_pad) * size_t(ldz) * 2, 256) + size_t(KD_TOPK_MAX_WARPS) * 4;
 }
 
 size_t kd_teacher_topk_workspace(int64_t N, int64_t dt, int64_t V, int K, int64_t chunk) {
@@ -315,6 +315,8 @@ int kd_teacher_topk(const void* Ht_bf16, const void* Wt_bf16, int64_t N, int64_t
   Ctrl* ctrl = reinterpret_cast<Ctrl*>(w8);
   uint16_t* zbuf = reinterpret_cast<uint16_t*>(w8 + sizeof(Ctrl));
   const int64_t ldz = (V + 7) / 8 * 8;
+  uint32_t* guesses = reinterpret_cast<uint32_t*>(
+      w8 + sizeof(Ctrl) + align_up(size_t((((chunk < N ? chunk : N) + BM - 1) / BM) * BM) * size_t(ldz) * 2, 256));
   const uint16_t* Ht = static_cast<const uint16_t*>(Ht_bf16);
   const int grid_max = gemm_max_grid();
   alignas(64) CUtensorMap tw[3], th, tw2, th2;
@@ -350,8 +352,9 @@ int kd_teacher_topk(const void* Ht_bf16, const void* Wt_bf16, int64_t N, int64_t
     cudaError_t e = launch_gemm(p, p.a_k3d ? th2 : th, p.b_k3d ? tw2 : tw[ci], tz, grid_max, s);
     if (e != cudaSuccess) return KD_ERR_CUDA;
     // exact top-K (and row logsumexp) of those bf16 logits
+    // each warp's threshold guess carries from one chunk's rows into the next chunk's
     e = launch_topk(zbuf, n, V, ldz, K, ids_out + c0 * K, vals_out + c0 * K, lse_out ? lse_out + c0 : nullptr,
-                    &ctrl->err, s);
+                    &ctrl->err, s, c0 == 0 ? nullptr : guesses, guesses);
     if (e != cudaSuccess) return KD_ERR_CUDA;
   }
   return KD_OK;

@@ -141,8 +141,13 @@ cudaError_t launch_gemm(const GemmProblem& p, const CUtensorMap& ta, const CUten
                         int grid, cudaStream_t s);
 int gemm_max_grid();
 
+// Row-streaming warps of one top-K launch are at most this many (one block per SM); a
+// guess array (guess_in / guess_out, KD_TOPK_MAX_WARPS words) carries each warp's next-row
+// threshold guess from one launch into the next over rows of the same source (NULL: none).
+constexpr int KD_TOPK_MAX_WARPS = 4096;
 cudaError_t launch_topk(const uint16_t* X, int64_t N, int64_t V, int64_t ld, int K, int32_t* ids,
-                        float* vals, float* lse, uint32_t* err, cudaStream_t s);
+                        float* vals, float* lse, uint32_t* err, cudaStream_t s, const uint32_t* guess_in = nullptr,
+                        uint32_t* guess_out = nullptr);
 
 cudaError_t launch_count_valid(const uint8_t* mask, int64_t N, int32_t* n_valid, cudaStream_t s);
 cudaError_t launch_teacher_prologue(const int32_t* ids, const float* tlog, int rows, int K, int64_t V,

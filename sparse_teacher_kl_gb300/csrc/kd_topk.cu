@@ -970,7 +970,7 @@ template <class C, bool WITH_LSE>
 __global__ void __launch_bounds__(C::WARPS * 32, 1)
     kd_topk_tma_kernel(const uint16_t* __restrict__ X, int64_t N, int64_t V, int64_t ld, int K,
                        int32_t* __restrict__ ids_out, float* __restrict__ vals_out, float* __restrict__ lse_out,
-                       uint32_t* err) {
+                       uint32_t* err, const uint32_t* guess_in, uint32_t* guess_out) {
   extern __shared__ __align__(16) uint8_t tkt_smem_raw[];
   constexpr int GSTEPS = C::GRP;
   constexpr uint32_t GBYTES = uint32_t(C::GRP) * TW_STEP * 2;
@@ -1020,7 +1020,8 @@ __global__ void __launch_bounds__(C::WARPS * 32, 1)
   uint32_t gidx = 0;  // groups consumed
   bool ok = true;
   // Guessed threshold for the warp's next row (0: none) and the margin factor behind it.
-  uint32_t guess = 0;
+  const int64_t gw = int64_t(blockIdx.x) * C::WARPS + (threadIdx.x >> 5);  // this warp's guess word
+  uint32_t guess = (guess_in && gw < KD_TOPK_MAX_WARPS && K >= 16) ? guess_in[gw] : 0u;
   float margin = TW_GUESS_MARGIN;
   for (; row < N; row += nwarps) {
     const uint16_t* xr = X + row * ld;
@@ -1142,11 +1143,12 @@ __global__ void __launch_bounds__(C::WARPS * 32, 1)
     for (uint32_t u = gidx; u < issued; ++u)
       mbar_wait(&ts.full[u & (C::RING - 1)], (u / C::RING) & 1u, &ts.never, err, 0x71u, 10000000ull);
   }
+  if (guess_out && gw < KD_TOPK_MAX_WARPS && lane == 0) guess_out[gw] = guess;
 }
 
 template <class C>
 cudaError_t launch_topk_tma(const uint16_t* X, int64_t N, int64_t V, int64_t ld, int K, int32_t* ids, float* vals,
-                            float* lse, uint32_t* err, cudaStream_t s) {
+                            float* lse, uint32_t* err, cudaStream_t s, const uint32_t* guess_in, uint32_t* guess_out) {
   static bool attr = false;
   const int smem = int(C::WARPS * sizeof(TopkTmaSmem<C>));
   if (!attr) {
@@ -1159,13 +1161,18 @@ cudaError_t launch_topk_tma(const uint16_t* X, int64_t N, int64_t V, int64_t ld,
   }
   int grid = gemm_max_grid();  // one block of C::WARPS row-streaming warps per SM
   if (int64_t(grid) * C::WARPS > N) grid = int((N + C::WARPS - 1) / C::WARPS);
-  if (lse) kd_topk_tma_kernel<C, true><<<grid, C::WARPS * 32, smem, s>>>(X, N, V, ld, K, ids, vals, lse, err);
-  else kd_topk_tma_kernel<C, false><<<grid, C::WARPS * 32, smem, s>>>(X, N, V, ld, K, ids, vals, lse, err);
+  if (grid > KD_TOPK_MAX_WARPS / C::WARPS) guess_in = guess_out = nullptr;  // more warps than guess words
+  if (lse)
+    kd_topk_tma_kernel<C, true><<<grid, C::WARPS * 32, smem, s>>>(X, N, V, ld, K, ids, vals, lse, err, guess_in,
+                                                                   guess_out);
+  else
+    kd_topk_tma_kernel<C, false><<<grid, C::WARPS * 32, smem, s>>>(X, N, V, ld, K, ids, vals, lse, err, guess_in,
+                                                                    guess_out);
   return cudaSuccess;
 }
 
 cudaError_t launch_topk(const uint16_t* X, int64_t N, int64_t V, int64_t ld, int K, int32_t* ids, float* vals,
-                        float* lse, uint32_t* err, cudaStream_t s) {
+                        float* lse, uint32_t* err, cudaStream_t s, const uint32_t* guess_in, uint32_t* guess_out) {
   static bool attr_set = false;
   const int smem = int(sizeof(TopkSmem));
   if (!attr_set) {
@@ -1178,10 +1185,10 @@ cudaError_t launch_topk(const uint16_t* X, int64_t N, int64_t V, int64_t ld, int
   if (grid <= 0) return cudaSuccess;
   prof_before("kd_topk_cache", s);
   if (K <= TmSmallK::MAXK) {
-    cudaError_t e = launch_topk_tma<TmSmallK>(X, N, V, ld, K, ids, vals, lse, err, s);
+    cudaError_t e = launch_topk_tma<TmSmallK>(X, N, V, ld, K, ids, vals, lse, err, s, guess_in, guess_out);
     if (e != cudaSuccess) return e;
   } else if (K <= TmLargeK::MAXK) {
-    cudaError_t e = launch_topk_tma<TmLargeK>(X, N, V, ld, K, ids, vals, lse, err, s);
+    cudaError_t e = launch_topk_tma<TmLargeK>(X, N, V, ld, K, ids, vals, lse, err, s, guess_in, guess_out);
     if (e != cudaSuccess) return e;
   } else {
     kd_topk_kernel<<<grid, TK_THREADS, smem, s>>>(X, N, V, ld, K, ids, vals, lse, err);
