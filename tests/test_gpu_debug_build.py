@@ -4,7 +4,8 @@ and report one out of range through the workspace error word instead of using it
 Runs, in a child process that loads the checked library, the cases that stress those
 indices most: top-K rows where every element becomes a candidate (ascending values),
 rows of one value (ties everywhere), both warp-per-row buffer sizes and the block kernel
-for K > 256, the fused teacher projection, and a fused fwd + bwd.  Every result must
+for K > 256, warps of several rows whose guessed thresholds miss, the fused teacher
+projection, and a fused fwd + bwd.  Every result must
 match the oracle and every error word must stay clean.
 """
 import os
@@ -57,6 +58,13 @@ for (N, V, K) in [(300, 20000, 100), (64, 9000, 200), (8, 40000, 1024)]:
     X[1] = 0.75                           # one value everywhere
     X[2, ::3] = -0.0
     topk_case(X.to(torch.bfloat16), K)
+
+# several rows per warp with scales jumping between rows: guessed thresholds, misses and
+# the reselection of a row from its start
+N, V = 5000, 3001
+X = torch.randn((N, V), generator=g) * 10.0 ** (torch.rand((N, 1), generator=g) * 4 - 2)
+X[1::5] = torch.randint(-2, 3, (len(range(1, N, 5)), V), generator=g).float()
+topk_case(X.to(torch.bfloat16), 100)
 
 # teacher projection + top-K with exact small-integer logits
 N, dt, V, K = 300, 64, 3000, 50
