@@ -287,7 +287,9 @@ static size_t teacher_topk_ws(int64_t N, int64_t V, int64_t chunk) {
   const int64_t c = chunk < N ? chunk : N;
   const int64_t rows_pad = (c + BM - 1) / BM * BM;
   const int64_t ldz = (V + 7) / 8 * 8;
-  return sizeof(Ctrl) + align_up(size_t(rows_pad) * size_t(ldz) * 2, 256) + size_t(KD_TOPK_MAX_WARPS) * 4;
+  const int64_t ldt = ((V + BN - 1) / BN + 7) / 8 * 8;  // per-tile row maxima of the logits
+  return sizeof(Ctrl) + align_up(size_t(rows_pad) * size_t(ldz) * 2, 256) + size_t(KD_TOPK_MAX_WARPS) * 4 +
+         align_up(size_t(rows_pad) * size_t(ldt) * 2, 256);
 }
 
 size_t kd_teacher_topk_workspace(int64_t N, int64_t dt, int64_t V, int K, int64_t chunk) {
@@ -317,6 +319,11 @@ int kd_teacher_topk(const void* Ht_bf16, const void* Wt_bf16, int64_t N, int64_t
   const int64_t ldz = (V + 7) / 8 * 8;
   uint32_t* guesses = reinterpret_cast<uint32_t*>(
       w8 + sizeof(Ctrl) + align_up(size_t((((chunk < N ? chunk : N) + BM - 1) / BM) * BM) * size_t(ldz) * 2, 256));
+  // each chunk row's maximum over every BN-column tile of its logits, from the projection's
+  // epilogue: their K-th largest starts the row's top-K selection
+  const int ntiles = int((V + BN - 1) / BN);
+  const int64_t ldt = (int64_t(ntiles) + 7) / 8 * 8;
+  uint16_t* tmax = reinterpret_cast<uint16_t*>(guesses + KD_TOPK_MAX_WARPS);
   const uint16_t* Ht = static_cast<const uint16_t*>(Ht_bf16);
   const int grid_max = gemm_max_grid();
   alignas(64) CUtensorMap tw[3], th, tw2, th2;
@@ -344,6 +351,8 @@ int kd_teacher_topk(const void* Ht_bf16, const void* Wt_bf16, int64_t N, int64_t
     p.n_units = ((p.m_tiles + p.cluster - 1) / p.cluster) * p.n_tiles;
     p.C = zbuf; p.ldc = ldz; p.c_bf16 = 1; p.err = &ctrl->err;
     p.c_tma = 1;   // bf16 logits written as TMA boxes into the row-major chunk buffer
+    p.tile_max = tmax;
+    p.ld_tile_max = ldt;
     p.m_fast = 1;  // Wt (larger than L2) read once per chunk, the chunk of Ht kept in L2
     alignas(64) CUtensorMap tz;
     if (!make_tmap_2d_bf16(&tz, zbuf, uint64_t(V), uint64_t(n), uint64_t(ldz) * 2, 64, 32)) return KD_ERR_CUDA;
@@ -354,7 +363,7 @@ int kd_teacher_topk(const void* Ht_bf16, const void* Wt_bf16, int64_t N, int64_t
     // exact top-K (and row logsumexp) of those bf16 logits
     // each warp's threshold guess carries from one chunk's rows into the next chunk's
     e = launch_topk(zbuf, n, V, ldz, K, ids_out + c0 * K, vals_out + c0 * K, lse_out ? lse_out + c0 : nullptr,
-                    &ctrl->err, s, c0 == 0 ? nullptr : guesses, guesses);
+                    &ctrl->err, s, c0 == 0 ? nullptr : guesses, guesses, tmax, ldt, ntiles);
     if (e != cudaSuccess) return KD_ERR_CUDA;
   }
   return KD_OK;

@@ -376,6 +376,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
       for (int nb = n_first; nb < n_first + n_count; ++nb, ++acc_it) {
         const uint32_t a = acc_it & 1u;
         const uint32_t aph = (acc_it >> 1) & 1u;
+        float tmax = -INFINITY;  // EPI_STORE with tile_max: the row's largest value in this tile
         // the tensor-memory loads below are warp-collective: decide per warp
         const bool got = mbar_wait(&tail->tfull[a], aph, abort_flag, p.err, 0x500u);
         if (!__all_sync(0xffffffffu, got)) {
@@ -541,6 +542,13 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
               const uint32_t j = uint32_t((c & 1) * 4 + g8);
               *reinterpret_cast<uint4*>(box + lane * 128u + ((j ^ (lane & 7u)) * 16u)) = v;
             }
+            if (p.tile_max) {
+              // rounding to bf16 is monotonic: the largest of the fp32 values, rounded, is the
+              // largest stored value (fmaxf skips NaNs)
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                if (col0 + i < p.N) tmax = fmaxf(tmax, x[i]);
+            }
             if (c & 1) {
               fence_proxy_async_smem();
               __syncwarp();
@@ -586,6 +594,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         tc_fence_before();
         if (CG == 2 && crank != 0) mbar_arrive_remote(mapa_u32(&tail->tempty[a], 0));
         else mbar_arrive(&tail->tempty[a]);
+        if (EPI == EPI_STORE && p.tile_max && ok && row < p.M)
+          p.tile_max[size_t(row) * p.ld_tile_max + nb] = uint16_t(pack_bf16x2(tmax, tmax) & 0xFFFFu);
       }
       if ((EPI == EPI_LSE || EPI == EPI_LSE_Z) && ok && row < p.rows) {
         const int g = n_first / p.n_group;

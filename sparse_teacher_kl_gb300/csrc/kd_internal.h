@@ -98,6 +98,11 @@ struct GemmProblem {
   // in shared memory with TMA stores through tmap_c (row-major C, box 64 x 32, 128-byte
   // swizzle), clipped at the matrix edges; 0: direct 16-byte stores.
   int c_tma;
+  // tile_max (c_tma = 1 only; NULL: none): per row of C and per BN-column tile, the largest
+  // bf16-rounded value of the row inside the tile (columns < N; bf16 bits, -inf for a tile
+  // of NaNs), at tile_max[row * ld_tile_max + tile] for rows < M.
+  uint16_t* tile_max;
+  int64_t ld_tile_max;
   // m_fast = 1 (EPI_STORE / EPI_ACCUM with k_splits = 1): units walk m fastest, so the CTAs
   // in flight share one B tile while the A operand stays in L2 (for a small A and a B
   // larger than L2, as in the teacher projection); 0: n fastest (they share one A slab).
@@ -145,9 +150,13 @@ int gemm_max_grid();
 // guess array (guess_in / guess_out, KD_TOPK_MAX_WARPS words) carries each warp's next-row
 // threshold guess from one launch into the next over rows of the same source (NULL: none).
 constexpr int KD_TOPK_MAX_WARPS = 4096;
+// tile_max (NULL: none): per row, the maxima of ntiles disjoint column ranges of the row
+// (bf16 bits, [N, ld_tile_max]); with ntiles >= K their K-th largest is a lower bound of
+// the row's K-th largest value and starts the row's selection.
 cudaError_t launch_topk(const uint16_t* X, int64_t N, int64_t V, int64_t ld, int K, int32_t* ids,
                         float* vals, float* lse, uint32_t* err, cudaStream_t s, const uint32_t* guess_in = nullptr,
-                        uint32_t* guess_out = nullptr);
+                        uint32_t* guess_out = nullptr, const uint16_t* tile_max = nullptr,
+                        int64_t ld_tile_max = 0, int ntiles = 0);
 
 cudaError_t launch_count_valid(const uint8_t* mask, int64_t N, int32_t* n_valid, cudaStream_t s);
 cudaError_t launch_teacher_prologue(const int32_t* ids, const float* tlog, int rows, int K, int64_t V,

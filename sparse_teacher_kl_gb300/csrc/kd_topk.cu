@@ -549,6 +549,33 @@ __device__ uint32_t warp_kth_largest(const unsigned long long* reg, uint32_t cnt
   return (b1 << 8) | b2;
 }
 
+// Warp: K-th largest key among the bf16 values src[0, cnt) in global memory (cnt >= K).
+__device__ uint32_t warp_kth_largest_bf16(const uint16_t* src, uint32_t cnt, uint32_t K, uint32_t* h) {
+  const uint32_t lane = lane_id();
+  for (uint32_t i = lane; i < 256; i += 32) h[i] = 0;
+  __syncwarp();
+  for (uint32_t base = 0; base < cnt; base += 32) {
+    const uint32_t i = base + lane;
+    hist_add_warp(h, i < cnt, i < cnt ? bf16_key(__ldg(src + i)) >> 8 : 0u);
+  }
+  __syncwarp();
+  uint32_t b1, need, above1;
+  warp_find_bin(h, K, b1, need, above1);
+  __syncwarp();
+  for (uint32_t i = lane; i < 256; i += 32) h[i] = 0;
+  __syncwarp();
+  for (uint32_t base = 0; base < cnt; base += 32) {
+    const uint32_t i = base + lane;
+    const uint32_t k = i < cnt ? bf16_key(__ldg(src + i)) : 0u;
+    hist_add_warp(h, i < cnt && (k >> 8) == b1, k & 255u);
+  }
+  __syncwarp();
+  uint32_t b2, need2, above2;
+  warp_find_bin(h, need, b2, need2, above2);
+  __syncwarp();
+  return (b1 << 8) | b2;
+}
+
 // Warp: keep the entries of reg[0, cnt) with key >= T, in place (each round of 256 is
 // read before any survivor of it is written); returns the new count.
 __device__ uint32_t warp_filter_ge(unsigned long long* reg, uint32_t cnt, uint32_t T) {
@@ -916,16 +943,30 @@ struct TopkTmaSmem {
   uint32_t never;  // stays 0: the flag of the bounded waits after an abort
 };
 
+// 16 bytes of a ring slot.  A volatile load: it is performed where it stands, once, so
+// its value never comes from a re-read of the slot after the slot has been refilled.
+__device__ __forceinline__ uint4 ring_ld(const uint4* p) {
+  uint4 v;
+  asm volatile("ld.volatile.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(smem_u32(p))
+               : "memory");
+  return v;
+}
+
 // Bulk copy global -> shared of `bytes` (a multiple of 16), completing on `bar`.
-// `after` is a value loaded from the slot's previous contents: as an operand it keeps
-// the copy behind that read.
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
-                                         uint32_t after) {
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
   asm volatile(
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
           smem_u32(dst)),
-      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "r"(after)
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
+}
+
+// Orders this thread's shared-memory accesses so far before the async-proxy operations
+// (bulk copies) that follow it, in this thread or, after a barrier, in another.
+__device__ __forceinline__ void fence_proxy_async_cta() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 // The lane's vectors of warp steps s0 .. s0 + TW_GROUP - 1 of a row, read directly
@@ -970,7 +1011,8 @@ template <class C, bool WITH_LSE>
 __global__ void __launch_bounds__(C::WARPS * 32, 1)
     kd_topk_tma_kernel(const uint16_t* __restrict__ X, int64_t N, int64_t V, int64_t ld, int K,
                        int32_t* __restrict__ ids_out, float* __restrict__ vals_out, float* __restrict__ lse_out,
-                       uint32_t* err, const uint32_t* guess_in, uint32_t* guess_out) {
+                       uint32_t* err, const uint32_t* guess_in, uint32_t* guess_out,
+                       const uint16_t* __restrict__ tile_max, int64_t ld_tile_max, int ntiles) {
   extern __shared__ __align__(16) uint8_t tkt_smem_raw[];
   constexpr int GSTEPS = C::GRP;
   constexpr uint32_t GBYTES = uint32_t(C::GRP) * TW_STEP * 2;
@@ -998,7 +1040,7 @@ __global__ void __launch_bounds__(C::WARPS * 32, 1)
   int64_t prow = row;
   int pg = 0;
   uint32_t issued = 0;
-  auto issue = [&](uint32_t slot, uint32_t after) {
+  auto issue = [&](uint32_t slot) {
     if (prow < N) {
       if (lane == 0) {
         const int64_t e0 = int64_t(pg) * GSTEPS * TW_STEP;
@@ -1006,7 +1048,7 @@ __global__ void __launch_bounds__(C::WARPS * 32, 1)
         uint32_t bytes = left >= int64_t(GSTEPS) * TW_STEP ? GBYTES : uint32_t(left * 2) & ~15u;
         if (!KD_DCHECK(e0 >= 0 && e0 + bytes / 2 <= V && bytes <= GBYTES, err, 0x7401)) bytes = 0;
         mbar_arrive_expect_tx(&ts.full[slot], bytes);  // 0 bytes: the phase completes on the arrival
-        if (bytes != 0) bulk_g2s(&ts.ring[slot][0][0], X + prow * ld + e0, bytes, &ts.full[slot], after);
+        if (bytes != 0) bulk_g2s(&ts.ring[slot][0][0], X + prow * ld + e0, bytes, &ts.full[slot]);
       }
       ++issued;
       if (++pg == ngr) {
@@ -1015,7 +1057,7 @@ __global__ void __launch_bounds__(C::WARPS * 32, 1)
       }
     }
   };
-  for (int r = 0; r < C::RING; ++r) issue(uint32_t(r), 0u);
+  for (int r = 0; r < C::RING; ++r) issue(uint32_t(r));
 
   uint32_t gidx = 0;  // groups consumed
   bool ok = true;
@@ -1034,6 +1076,9 @@ __global__ void __launch_bounds__(C::WARPS * 32, 1)
     st.tv = key_to_float(0);
     float lm = -INFINITY, ls = 0.f;
 
+    // Tile start (maxima of ntiles >= K disjoint column ranges of every row given, as the
+    // teacher projection emits them): their K-th largest is reached by at least K elements,
+    // so every element of the top K has a key >= it, an exact first threshold.
     // Guessed start (every row after a warp's first, K >= 16): the threshold is a key taken
     // from the previous row's best K (below).  If at least K elements reach it, the top K
     // all do and the row is selected exactly; if not, the list ends short of K and the row
@@ -1042,8 +1087,15 @@ __global__ void __launch_bounds__(C::WARPS * 32, 1)
     // row's last).  The K-th largest of their per-lane vector maxima is reached by at least
     // K elements, so every element of the top K has a key >= it: those groups are then
     // consumed with that threshold (>=), and the rest of the row with the raised ones.
-    const bool guessed = guess != 0u;
-    if (guessed) {
+    const bool tiles = tile_max != nullptr && ntiles >= K;
+    const bool guessed = !tiles && guess != 0u;
+    if (tiles) {
+      const uint32_t T = warp_kth_largest_bf16(tile_max + row * ld_tile_max, uint32_t(ntiles), Ku, ws.hist);
+      if (T != 0) {
+        st.wth = T;
+        st.tv = key_to_float(T - 1u == 0x7FFFu ? 0x7FFEu : T - 1u);
+      }
+    } else if (guessed) {
       st.wth = guess;
       st.tv = key_to_float(guess - 1u == 0x7FFFu ? 0x7FFEu : guess - 1u);
     } else if (ngr > C::RING && K <= C::RING * C::GRP * 32) {
@@ -1056,7 +1108,7 @@ __global__ void __launch_bounds__(C::WARPS * 32, 1)
       for (int r = 0; r < C::RING; ++r) {
 #pragma unroll
         for (int k = 0; k < C::GRP; ++k) {
-          const uint4 v = ts.ring[(gidx + r) & (C::RING - 1)][k][lane];
+          const uint4 v = ring_ld(&ts.ring[(gidx + r) & (C::RING - 1)][k][lane]);
           const float m = vec_max(v);
           uint32_t key;
           if (m == m) {
@@ -1088,7 +1140,7 @@ __global__ void __launch_bounds__(C::WARPS * 32, 1)
       }
       uint4 v[GSTEPS];
 #pragma unroll
-      for (int k = 0; k < GSTEPS; ++k) v[k] = ts.ring[slot][k][lane];
+      for (int k = 0; k < GSTEPS; ++k) v[k] = ring_ld(&ts.ring[slot][k][lane]);
       const int s0 = g * GSTEPS;
       uint32_t live = (1u << GSTEPS) - 1u;
       if (g == ngr - 1) {  // the row's last group
@@ -1099,11 +1151,11 @@ __global__ void __launch_bounds__(C::WARPS * 32, 1)
             if (s0 + k == nst - 1) v[k] = load_step(xr, V, nst - 1);
         }
       }
-      uint32_t after = 0;
-#pragma unroll
-      for (int k = 0; k < GSTEPS; ++k) after ^= v[k].x;
-      __syncwarp();  // every lane has read the slot
-      issue(slot, after);
+      // The slot is refilled by the async proxy: every lane's reads of it are ordered before
+      // the refill (a proxy fence in each lane, then the warp barrier before lane 0 issues).
+      fence_proxy_async_cta();
+      __syncwarp();
+      issue(slot);
       test_group<C, WITH_LSE>(ws, st, v, s0, live, lm, ls, V32, Ku);
     }
     if (!ok) break;
@@ -1148,7 +1200,8 @@ __global__ void __launch_bounds__(C::WARPS * 32, 1)
 
 template <class C>
 cudaError_t launch_topk_tma(const uint16_t* X, int64_t N, int64_t V, int64_t ld, int K, int32_t* ids, float* vals,
-                            float* lse, uint32_t* err, cudaStream_t s, const uint32_t* guess_in, uint32_t* guess_out) {
+                            float* lse, uint32_t* err, cudaStream_t s, const uint32_t* guess_in, uint32_t* guess_out,
+                            const uint16_t* tile_max, int64_t ld_tile_max, int ntiles) {
   static bool attr = false;
   const int smem = int(C::WARPS * sizeof(TopkTmaSmem<C>));
   if (!attr) {
@@ -1164,15 +1217,16 @@ cudaError_t launch_topk_tma(const uint16_t* X, int64_t N, int64_t V, int64_t ld,
   if (grid > KD_TOPK_MAX_WARPS / C::WARPS) guess_in = guess_out = nullptr;  // more warps than guess words
   if (lse)
     kd_topk_tma_kernel<C, true><<<grid, C::WARPS * 32, smem, s>>>(X, N, V, ld, K, ids, vals, lse, err, guess_in,
-                                                                   guess_out);
+                                                                   guess_out, tile_max, ld_tile_max, ntiles);
   else
     kd_topk_tma_kernel<C, false><<<grid, C::WARPS * 32, smem, s>>>(X, N, V, ld, K, ids, vals, lse, err, guess_in,
-                                                                    guess_out);
+                                                                    guess_out, tile_max, ld_tile_max, ntiles);
   return cudaSuccess;
 }
 
 cudaError_t launch_topk(const uint16_t* X, int64_t N, int64_t V, int64_t ld, int K, int32_t* ids, float* vals,
-                        float* lse, uint32_t* err, cudaStream_t s, const uint32_t* guess_in, uint32_t* guess_out) {
+                        float* lse, uint32_t* err, cudaStream_t s, const uint32_t* guess_in, uint32_t* guess_out,
+                        const uint16_t* tile_max, int64_t ld_tile_max, int ntiles) {
   static bool attr_set = false;
   const int smem = int(sizeof(TopkSmem));
   if (!attr_set) {
@@ -1185,10 +1239,12 @@ cudaError_t launch_topk(const uint16_t* X, int64_t N, int64_t V, int64_t ld, int
   if (grid <= 0) return cudaSuccess;
   prof_before("kd_topk_cache", s);
   if (K <= TmSmallK::MAXK) {
-    cudaError_t e = launch_topk_tma<TmSmallK>(X, N, V, ld, K, ids, vals, lse, err, s, guess_in, guess_out);
+    cudaError_t e = launch_topk_tma<TmSmallK>(X, N, V, ld, K, ids, vals, lse, err, s, guess_in, guess_out, tile_max,
+                                              ld_tile_max, ntiles);
     if (e != cudaSuccess) return e;
   } else if (K <= TmLargeK::MAXK) {
-    cudaError_t e = launch_topk_tma<TmLargeK>(X, N, V, ld, K, ids, vals, lse, err, s, guess_in, guess_out);
+    cudaError_t e = launch_topk_tma<TmLargeK>(X, N, V, ld, K, ids, vals, lse, err, s, guess_in, guess_out, tile_max,
+                                              ld_tile_max, ntiles);
     if (e != cudaSuccess) return e;
   } else {
     kd_topk_kernel<<<grid, TK_THREADS, smem, s>>>(X, N, V, ld, K, ids, vals, lse, err);

@@ -132,6 +132,7 @@ def test_topk_mid_workload_sampled(kd, cuda_device):
                                ws.data_ptr(), ws.numel(), torch.cuda.current_stream().cuda_stream)
     assert st == 0
     torch.cuda.synchronize()
+    assert kd.device_error(ws) == (0, 0)
     rows = np.random.default_rng(0).choice(w.N, 48, replace=False)
     rows = np.concatenate([rows, [0, w.N - 1]])
     bits = bf16_bits(X[torch.as_tensor(rows, device=cuda_device)])
@@ -140,7 +141,8 @@ def test_topk_mid_workload_sampled(kd, cuda_device):
     assert np.array_equal(vals.cpu().numpy()[rows].view(np.uint32), rval.view(np.uint32))
     # every row: sorted descending, distinct ids
     v = vals.cpu()
-    assert bool((v[:, 1:] <= v[:, :-1]).all())
+    uns = torch.nonzero((v[:, 1:] > v[:, :-1]).any(dim=1)).flatten().tolist()
+    assert not uns, f"{len(uns)} rows not sorted, first {uns[:8]}: {v[uns[0]].tolist() if uns else ''}"
     s, _ = torch.sort(ids.cpu(), dim=1)
     assert bool((s[:, 1:] != s[:, :-1]).all())
 
@@ -158,18 +160,19 @@ def test_topk_dropped_mass(kd, cuda_device):
     assert np.all(ref >= -1e-12)
 
 
-@pytest.mark.parametrize("N,dt,chunk", [
-    (300, 64, 128),   # one row tile per chunk: single-CTA tiles
-    (300, 192, 256),  # CTA pairs, 3 k-blocks, then a 44-row single-CTA chunk
-    (700, 320, 384),  # CTA pairs over 3 row tiles (the pair's phantom tile stores nothing)
-    (600, 200, 256),  # dt not a multiple of 64: a ragged last k-block
+@pytest.mark.parametrize("N,dt,chunk,V,K", [
+    (300, 64, 128, 5000, 37),    # one row tile per chunk: single-CTA tiles
+    (300, 192, 256, 5000, 37),   # CTA pairs, 3 k-blocks, then a 44-row single-CTA chunk
+    (700, 320, 384, 5000, 37),   # CTA pairs over 3 row tiles (the pair's phantom tile stores nothing)
+    (600, 200, 256, 5000, 37),   # dt not a multiple of 64: a ragged last k-block
+    (300, 192, 256, 12000, 37),  # 47 column tiles >= K: rows start from their tile maxima (ragged last tile)
+    (520, 64, 256, 20000, 64),   # the same over 79 tiles, three chunks
 ])
-def test_teacher_topk_exact_integer_logits(kd, cuda_device, N, dt, chunk):
+def test_teacher_topk_exact_integer_logits(kd, cuda_device, N, dt, chunk, V, K):
     """Small-integer teacher hidden states and weights make every logit an integer that fp32 holds
     exactly, rounded once to bf16, so the fused projection + top-K must match the oracle's cache of
     the logits bit for bit (with many ties, broken by the lower id)."""
     g = torch.Generator().manual_seed(21 + dt)
-    V, K = 5000, 37
     Ht = torch.randint(-2, 3, (N, dt), generator=g).to(torch.bfloat16)
     Wt = torch.randint(-2, 3, (V, dt), generator=g).to(torch.bfloat16)
     ids, vals, lse = kd.teacher_topk(Ht.to(cuda_device), Wt.to(cuda_device), K, chunk=chunk, with_lse=True)
@@ -182,12 +185,12 @@ def test_teacher_topk_exact_integer_logits(kd, cuda_device, N, dt, chunk):
     assert np.max(np.abs(lse.cpu().numpy() - ref_lse)) <= 1e-5 * np.max(np.abs(ref_lse))
 
 
-@pytest.mark.parametrize("N,dt,chunk", [(260, 200, 128), (520, 256, 256)])
-def test_teacher_topk_random_is_a_valid_topk(kd, cuda_device, N, dt, chunk):
+@pytest.mark.parametrize("N,dt,chunk,V", [(260, 200, 128, 3001), (520, 256, 256, 3001), (400, 128, 256, 16411)])
+def test_teacher_topk_random_is_a_valid_topk(kd, cuda_device, N, dt, chunk, V):
     """Random teacher inputs: the kept values are the logits rounded to bf16 (within one bf16 step of the
     float64 product) and no logit left out exceeds the smallest kept one by more than that rounding."""
     g = torch.Generator().manual_seed(22)
-    V, K = 3001, 50
+    K = 50
     Ht = torch.randn((N, dt), generator=g).to(torch.bfloat16)
     Wt = (torch.randn((V, dt), generator=g) / 14).to(torch.bfloat16)
     ids, vals = kd.teacher_topk(Ht.to(cuda_device), Wt.to(cuda_device), K, chunk=chunk)
