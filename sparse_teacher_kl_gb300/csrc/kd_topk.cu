@@ -3,7 +3,8 @@
 // the first fix; [DAI] "As duas inovações" item 1; [EPO] "Los dos cambios
 // propuestos", first item).
 //
-// HBM-bound: every logit is read exactly once.  Each element becomes a 48-bit
+// HBM-bound: every logit is read once (twice for a row whose guessed starting
+// threshold, below, turned out too high).  Each element becomes a 48-bit
 // composite
 //   (order-preserving 16-bit key of the bf16 value) << 32 | (~column)
 // which is unique per element and orders by value descending, then column
@@ -435,10 +436,14 @@ __global__ void __launch_bounds__(TK_THREADS, 2)
 //  * the copy engine streams the row: each warp owns a ring of RING slots of GRP warp
 //    steps (a step is 256 elements, 16 bytes per lane); lane 0 fills a slot with one bulk
 //    copy completing on the slot's mbarrier, RING groups ahead of its use, running on
-//    into the warp's next row while the current one is finished;
-//  * quick start: when a row begins, the ring holds its first RING x GRP steps; the K-th
-//    largest of their 8-element vector maxima is reached by at least K elements, so it
-//    is a first threshold (key >= it) before any element is kept;
+//    into the warp's next row while the current one is finished; every lane fences its
+//    reads of a slot before the warp barrier after which the slot is refilled;
+//  * a first threshold (key >= it) before any element is kept, the first of these that
+//    applies: the K-th largest of per-tile row maxima a producer supplies (the teacher
+//    projection's epilogue); a guess from the warp's previous row, verified when the row
+//    ends (a row short of K entries at or above it is selected again from its start);
+//    the K-th largest of the 8-element vector maxima of the row's first RING x GRP steps,
+//    which the ring already holds when the row begins (quick start);
 //  * each lane tests its 8 values with one packed bf16 max against the threshold, GRP
 //    steps at a time with one vote; a vector that passes is queued whole in shared
 //    memory, and the warp filters BATCH queued vectors at a time (one per lane) with
