@@ -948,17 +948,6 @@ struct TopkTmaSmem {
   uint32_t never;  // stays 0: the flag of the bounded waits after an abort
 };
 
-// 16 bytes of a ring slot.  A volatile load: it is performed where it stands, once, so
-// its value never comes from a re-read of the slot after the slot has been refilled.
-__device__ __forceinline__ uint4 ring_ld(const uint4* p) {
-  uint4 v;
-  asm volatile("ld.volatile.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "r"(smem_u32(p))
-               : "memory");
-  return v;
-}
-
 // Bulk copy global -> shared of `bytes` (a multiple of 16), completing on `bar`.
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
   asm volatile(
@@ -1113,7 +1102,7 @@ __global__ void __launch_bounds__(C::WARPS * 32, 1)
       for (int r = 0; r < C::RING; ++r) {
 #pragma unroll
         for (int k = 0; k < C::GRP; ++k) {
-          const uint4 v = ring_ld(&ts.ring[(gidx + r) & (C::RING - 1)][k][lane]);
+          const uint4 v = ts.ring[(gidx + r) & (C::RING - 1)][k][lane];
           const float m = vec_max(v);
           uint32_t key;
           if (m == m) {
@@ -1145,7 +1134,7 @@ __global__ void __launch_bounds__(C::WARPS * 32, 1)
       }
       uint4 v[GSTEPS];
 #pragma unroll
-      for (int k = 0; k < GSTEPS; ++k) v[k] = ring_ld(&ts.ring[slot][k][lane]);
+      for (int k = 0; k < GSTEPS; ++k) v[k] = ts.ring[slot][k][lane];
       const int s0 = g * GSTEPS;
       uint32_t live = (1u << GSTEPS) - 1u;
       if (g == ngr - 1) {  // the row's last group
