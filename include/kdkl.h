@@ -91,11 +91,12 @@ KD_API size_t kd_topk_cache_workspace(int64_t N, int64_t V, int K);
  * by ascending id and the cut at K keeps the lowest ids; -0.0 equals +0.0.
  * Values are the bf16 inputs widened exactly.  NaN inputs are ordered by their
  * sign bit like any other bit pattern (positive NaN above +inf).
- * Performance note: rows are streamed by warps, each over several rows; a warp
- * starts each row after its first from a threshold guessed from the row before
- * and checks it when the row ends.  Rows that resemble their predecessors (as the
- * rows of one model's logits do) gain the most; a row where the guess was too high
- * is read a second time.  The result never depends on the guesses.
+ * Performance note: rows are streamed by warps, each over several rows.  With
+ * KD_TOPK_GUESS=1 in the environment a warp starts each row after its first from a
+ * threshold guessed from the row before and checks it when the row ends: faster
+ * when consecutive rows have the same scale, slower when their scales differ by a
+ * few percent, since a row whose guess was too high is read a second time.  The
+ * result never depends on the guesses.
  */
 KD_API int kd_topk_cache(const void* logits_bf16, int64_t N, int64_t V, int64_t ld, int K,
                   int32_t* ids_out, float* vals_out, float* lse_out,

@@ -23,6 +23,7 @@
 // logits, so that the probability mass the cache drops, 1 - sum_k e^(t_k - lse),
 // can be reported per position ([ART] paragraph on the top-K limitation).
 #include <stdint.h>
+#include <stdlib.h>
 
 #include "kd_device.cuh"
 #include "kd_internal.h"
@@ -1005,7 +1006,7 @@ template <class C, bool WITH_LSE>
 __global__ void __launch_bounds__(C::WARPS * 32, 1)
     kd_topk_tma_kernel(const uint16_t* __restrict__ X, int64_t N, int64_t V, int64_t ld, int K,
                        int32_t* __restrict__ ids_out, float* __restrict__ vals_out, float* __restrict__ lse_out,
-                       uint32_t* err, const uint32_t* guess_in, uint32_t* guess_out,
+                       uint32_t* err, int guesses, const uint32_t* guess_in, uint32_t* guess_out,
                        const uint16_t* __restrict__ tile_max, int64_t ld_tile_max, int ntiles) {
   extern __shared__ __align__(16) uint8_t tkt_smem_raw[];
   constexpr int GSTEPS = C::GRP;
@@ -1057,7 +1058,8 @@ __global__ void __launch_bounds__(C::WARPS * 32, 1)
   bool ok = true;
   // Guessed threshold for the warp's next row (0: none) and the margin factor behind it.
   const int64_t gw = int64_t(blockIdx.x) * C::WARPS + (threadIdx.x >> 5);  // this warp's guess word
-  uint32_t guess = (guess_in && gw < KD_TOPK_MAX_WARPS && K >= 16) ? guess_in[gw] : 0u;
+  const bool may_guess = guesses != 0 && K >= 16;
+  uint32_t guess = (may_guess && guess_in && gw < KD_TOPK_MAX_WARPS) ? guess_in[gw] : 0u;
   float margin = TW_GUESS_MARGIN;
   for (; row < N; row += nwarps) {
     const uint16_t* xr = X + row * ld;
@@ -1073,8 +1075,8 @@ __global__ void __launch_bounds__(C::WARPS * 32, 1)
     // Tile start (maxima of ntiles >= K disjoint column ranges of every row given, as the
     // teacher projection emits them): their K-th largest is reached by at least K elements,
     // so every element of the top K has a key >= it, an exact first threshold.
-    // Guessed start (every row after a warp's first, K >= 16): the threshold is a key taken
-    // from the previous row's best K (below).  If at least K elements reach it, the top K
+    // Guessed start (when enabled: every row after a warp's first, K >= 16): the threshold
+    // is a key taken from the previous row's best K (below).  If at least K elements reach it, the top K
     // all do and the row is selected exactly; if not, the list ends short of K and the row
     // is selected again from its start with no threshold.
     // Quick start (otherwise): the ring holds this row's first RING groups (none of them the
@@ -1160,7 +1162,7 @@ __global__ void __launch_bounds__(C::WARPS * 32, 1)
       st = warp_reselect<C>(ws, xr, V, nst, V32, Ku);
       margin *= 4.f;  // a wider margin for the rows after a miss
     }
-    if (K >= 16) {
+    if (may_guess) {
       // Next guess: the K-th best value lowered by margin x (its distance to the (K/2)-th).
       // For tails like the normal's or the logistic's the top order statistics are spaced
       // about logarithmically in rank, so margin m lands near rank 2^m K of a row like this.
@@ -1192,6 +1194,21 @@ __global__ void __launch_bounds__(C::WARPS * 32, 1)
   if (guess_out && gw < KD_TOPK_MAX_WARPS && lane == 0) guess_out[gw] = guess;
 }
 
+// Guessed starting thresholds are speculative: a row whose guess was too high is read a
+// second time by its warp alone, at the end of that warp's work, so a few misses decide
+// the launch's duration.  They pay off only when consecutive rows have about the same
+// scale (0.52 against 0.65 ms on 8192 rows of N(0, 2) over 151936 columns, K = 100) and
+// cost when it varies (0.77 ms with the rows' scales 5 % apart): off unless
+// KD_TOPK_GUESS=1 is set in the environment.
+static int topk_guesses() {
+  static int on = -1;
+  if (on < 0) {
+    const char* v = getenv("KD_TOPK_GUESS");
+    on = (v && v[0] == '1') ? 1 : 0;
+  }
+  return on;
+}
+
 template <class C>
 cudaError_t launch_topk_tma(const uint16_t* X, int64_t N, int64_t V, int64_t ld, int K, int32_t* ids, float* vals,
                             float* lse, uint32_t* err, cudaStream_t s, const uint32_t* guess_in, uint32_t* guess_out,
@@ -1209,12 +1226,13 @@ cudaError_t launch_topk_tma(const uint16_t* X, int64_t N, int64_t V, int64_t ld,
   int grid = gemm_max_grid();  // one block of C::WARPS row-streaming warps per SM
   if (int64_t(grid) * C::WARPS > N) grid = int((N + C::WARPS - 1) / C::WARPS);
   if (grid > KD_TOPK_MAX_WARPS / C::WARPS) guess_in = guess_out = nullptr;  // more warps than guess words
+  const int guesses = topk_guesses();
   if (lse)
-    kd_topk_tma_kernel<C, true><<<grid, C::WARPS * 32, smem, s>>>(X, N, V, ld, K, ids, vals, lse, err, guess_in,
-                                                                   guess_out, tile_max, ld_tile_max, ntiles);
+    kd_topk_tma_kernel<C, true><<<grid, C::WARPS * 32, smem, s>>>(X, N, V, ld, K, ids, vals, lse, err, guesses,
+                                                                   guess_in, guess_out, tile_max, ld_tile_max, ntiles);
   else
-    kd_topk_tma_kernel<C, false><<<grid, C::WARPS * 32, smem, s>>>(X, N, V, ld, K, ids, vals, lse, err, guess_in,
-                                                                    guess_out, tile_max, ld_tile_max, ntiles);
+    kd_topk_tma_kernel<C, false><<<grid, C::WARPS * 32, smem, s>>>(X, N, V, ld, K, ids, vals, lse, err, guesses,
+                                                                    guess_in, guess_out, tile_max, ld_tile_max, ntiles);
   return cudaSuccess;
 }
 

@@ -4,8 +4,8 @@ and report one out of range through the workspace error word instead of using it
 Runs, in a child process that loads the checked library, the cases that stress those
 indices most: top-K rows where every element becomes a candidate (ascending values),
 rows of one value (ties everywhere), both warp-per-row buffer sizes and the block kernel
-for K > 256, warps of several rows whose guessed thresholds miss, the fused teacher
-projection, and a fused fwd + bwd.  Every result must
+for K > 256, warps of several rows with guessed row thresholds (switched on here with
+KD_TOPK_GUESS=1) that miss, the fused teacher projection, and a fused fwd + bwd.  Every result must
 match the oracle and every error word must stay clean.
 """
 import os
@@ -98,7 +98,7 @@ print("checked build ok")
 def test_checked_build_parity_and_clean_error_word(cuda_device):
     from sparse_teacher_kl_gb300.build import build_library
     build_library(debug=True)
-    env = dict(os.environ, KD_DEBUG="1")
+    env = dict(os.environ, KD_DEBUG="1", KD_TOPK_GUESS="1")  # guessed row thresholds on, misses included
     r = subprocess.run([sys.executable, "-c", CHILD], cwd=ROOT, env=env, capture_output=True, text=True,
                        timeout=900)
     assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-3000:]
