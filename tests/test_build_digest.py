@@ -22,7 +22,7 @@ def test_source_digest_follows_code_not_comments(tmp_path, monkeypatch):
     src.write_text("__global__ void k(int* p) { *p = 1; }\n")
     monkeypatch.setattr(build, "CSRC", str(tmp_path))
     d0 = build.source_digest(["k.cu"])
-    src.write_text("// a note\n__global__ void k(int* p) {\n  *p = 1;  /* store */\n}\n")
+    src.write_text("// a note\n\n    __global__ void k(int* p) { *p = 1; }  /* store */\n")
     assert build.source_digest(["k.cu"]) == d0
     src.write_text("__global__ void k(int* p) { *p = 2; }\n")
     assert build.source_digest(["k.cu"]) != d0
