@@ -216,7 +216,8 @@ KD_API int kd_chunked_kl_bwd(const void* H_bf16, const void* W_bf16,
  * the library instead of a workspace:
  *   - every GPU that loads the library holds that array until the process exits;
  *   - the array's device address is looked up on the first call made with a
- *     given device current, so make that first call before any stream capture;
+ *     given device current, so make that first call before any stream capture
+ *     (it is looked up again after a device reset gives the device a new context);
  *   - it returns KD_ERR_WORKSPACE, before any launch, when the problem needs more
  *     than the array holds, i.e. when kd_fused_kl_workspace(N, d, V, K, chunk)
  *     exceeds KD_STATIC_SCRATCH_BYTES;
@@ -225,7 +226,8 @@ KD_API int kd_chunked_kl_bwd(const void* H_bf16, const void* W_bf16,
  *     so calls whose GPU work overlaps (other streams or host threads) race and
  *     must be serialised by the caller;
  *   - device-side conditions (a teacher id out of range) are recorded in the
- *     shared array and are not reported by this variant.
+ *     shared array's error word: kd_get_device_error(NULL, stream, &detail)
+ *     reads and clears it.
  * Argument errors that kd_fused_kl_fwd detects are returned as there; the
  * scratch set-up and the clearing of its control block may already have been
  * enqueued when an alignment or shape check fails.
@@ -238,7 +240,8 @@ KD_API int kd_fused_kl_fwd_static(const void* H_bf16, const void* W_bf16,
 
 /*
  * Reads (synchronising `stream`) and clears the device error word of a
- * workspace used by the calls above.  Returns KD_OK, KD_ERR_TIMEOUT or
+ * workspace used by the calls above; ws == NULL names the scratch array of
+ * kd_fused_kl_fwd_static on the current device.  Returns KD_OK, KD_ERR_TIMEOUT or
  * KD_ERR_DEVICE; *detail_out (may be NULL) receives a call-specific detail
  * (for a bad teacher id: the first offending row).  A library built with
  * KD_DEBUG (libkdkl_debug.so) also checks the indices its kernels compute and

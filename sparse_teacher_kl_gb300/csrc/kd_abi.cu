@@ -10,6 +10,7 @@
 #include <mutex>
 #include <vector>
 
+#include "kd_host_state.h"
 #include "kd_internal.h"
 
 namespace kd {
@@ -106,17 +107,23 @@ bool make_tmap_2d_f32(CUtensorMap* map, const void* base, uint64_t inner, uint64
 
 // ---------------------------------------------------------- device check ---
 
-static int g_dev_ok = -1;  // -1 unknown, 0 no, 1 yes
+static PerDevice<int> g_dev_ok;  // per device: 1 = sm_103, 0 = another architecture
 
+// The current device is an sm_103 GPU (the kernels are built for sm_103a only).
 static kd_status check_device() {
-  if (g_dev_ok < 0) {
-    int dev = 0, major = 0, minor = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return KD_ERR_CUDA;
-    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
-    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
-    g_dev_ok = (major == 10 && minor == 3) ? 1 : 0;
-  }
-  return g_dev_ok ? KD_OK : KD_ERR_UNSUPPORTED;
+  int dev = 0, ok = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return KD_ERR_CUDA;
+  const int rc = g_dev_ok.get(dev, &ok, [](int d, int* v) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, d) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, d) != cudaSuccess)
+      return 1;
+    *v = (major == 10 && minor == 3) ? 1 : 0;
+    return 0;
+  });
+  if (rc < 0) return KD_ERR_UNSUPPORTED;  // an ordinal beyond the per-device tables
+  if (rc > 0) return KD_ERR_CUDA;
+  return ok ? KD_OK : KD_ERR_UNSUPPORTED;
 }
 
 // -------------------------------------------------------------- layout ---
@@ -155,43 +162,14 @@ static KlLayout kl_layout(int64_t N, int64_t d, int64_t V, int K, int64_t chunk)
   return L;
 }
 
-// CTAs per cluster sharing the B operand (see GemmProblem::cluster) for a launch with
-// m_tiles row tiles.  The loss epilogues need an even m_tiles (no phantom tile
+// CTA pairs (GemmProblem::cta_pair, clusters of two) for every launch with at least two
+// row tiles (measured on the gpt-oss shape: 342k against 295k tokens/s for single-CTA
+// tiles).  The loss epilogues also need an even number of row tiles (no phantom tile
 // writing past the chunk); the gradient products check their rows themselves.
-// KD_GEMM_CLUSTER=1, 2 or 4 in the environment forces one size (for measurements).
-static int pick_cluster(int epi, int m_tiles) {
-  static int env = -1;
-  if (env < 0) {
-    const char* v = getenv("KD_GEMM_CLUSTER");
-    env = (v && (v[0] == '1' || v[0] == '2' || v[0] == '4')) ? (v[0] - '0') : 0;
-  }
-  const bool loss_epi = (epi == EPI_LSE || epi == EPI_DZ || epi == EPI_LSE_Z);
-  // measured on the gpt-oss shape: quads help the two gradient products (MN-major
-  // operands, fp32 output), pairs suit the loss epilogues
-  int c = env ? env : (loss_epi ? 2 : 4);
-  while (c > 1 && (m_tiles < c || (loss_epi && (m_tiles % c) != 0))) c >>= 1;
-  return c;
-}
-
-// CTA-pair tensor-core mode (GemmProblem::cta_pair), used for every launch with at
-// least two row tiles (measured on the gpt-oss shape: 342k vs 295k tokens/s for the
-// single-CTA tiles with shared B).  KD_GEMM_PAIR=0 turns it off (for measurements).
-static bool pair_mode() {
-  static int env = -1;
-  if (env < 0) {
-    const char* v = getenv("KD_GEMM_PAIR");
-    env = (v && v[0] == '0') ? 0 : 1;
-  }
-  return env == 1;
-}
-
 static void set_cluster(GemmProblem& p) {
-  p.cluster = pick_cluster(p.epi, p.m_tiles);
-  p.cta_pair = 0;
-  if (p.cluster >= 2 && pair_mode()) {
-    p.cluster = 2;
-    p.cta_pair = 1;
-  }
+  const bool loss_epi = (p.epi == EPI_LSE || p.epi == EPI_DZ || p.epi == EPI_LSE_Z);
+  p.cta_pair = (p.m_tiles >= 2 && !(loss_epi && p.m_tiles % 2 != 0)) ? 1 : 0;
+  p.cluster = p.cta_pair ? 2 : 1;
 }
 
 // Number of K splits for a product of `tiles` output tiles with `k_blocks` steps of
@@ -326,8 +304,9 @@ int kd_teacher_topk(const void* Ht_bf16, const void* Wt_bf16, int64_t N, int64_t
   uint16_t* tmax = reinterpret_cast<uint16_t*>(guesses + KD_TOPK_MAX_WARPS);
   const uint16_t* Ht = static_cast<const uint16_t*>(Ht_bf16);
   const int grid_max = gemm_max_grid();
-  alignas(64) CUtensorMap tw[3], th, tw2, th2;
-  for (int i = 0; i < 3; ++i)
+  // Wt boxes: BN rows for single CTAs, BN / 2 for a CTA pair's halves
+  alignas(64) CUtensorMap tw[2], th, tw2, th2;
+  for (int i = 0; i < 2; ++i)
     if (!make_tmap_2d_bf16(&tw[i], Wt_bf16, uint64_t(dt), uint64_t(V), uint64_t(dt) * 2, BK, BN >> i))
       return KD_ERR_CUDA;
   const bool dt64 = dt % 64 == 0;  // two k-blocks per box for CTA pairs
@@ -356,9 +335,8 @@ int kd_teacher_topk(const void* Ht_bf16, const void* Wt_bf16, int64_t N, int64_t
     p.m_fast = 1;  // Wt (larger than L2) read once per chunk, the chunk of Ht kept in L2
     alignas(64) CUtensorMap tz;
     if (!make_tmap_2d_bf16(&tz, zbuf, uint64_t(V), uint64_t(n), uint64_t(ldz) * 2, 64, 32)) return KD_ERR_CUDA;
-    const int ci = p.cluster == 4 ? 2 : (p.cluster == 2 ? 1 : 0);
     p.a_k3d = p.b_k3d = p.cta_pair && dt64;
-    cudaError_t e = launch_gemm(p, p.a_k3d ? th2 : th, p.b_k3d ? tw2 : tw[ci], tz, grid_max, s);
+    cudaError_t e = launch_gemm(p, p.a_k3d ? th2 : th, p.b_k3d ? tw2 : tw[p.cta_pair], tz, grid_max, s);
     if (e != cudaSuccess) return KD_ERR_CUDA;
     // exact top-K (and row logsumexp) of those bf16 logits
     // each warp's threshold guess carries from one chunk's rows into the next chunk's
@@ -406,9 +384,7 @@ static int fwd_impl(const void* H_bf16, const void* W_bf16, const int32_t* t_ids
   if (!make_tmap_2d_bf16(&tw, W_bf16, uint64_t(d), uint64_t(V), uint64_t(d) * 2, BK, BN)) return KD_ERR_CUDA;
   if (!make_tmap_2d_bf16(&tw_half, W_bf16, uint64_t(d), uint64_t(V), uint64_t(d) * 2, BK, BN / 2))
     return KD_ERR_CUDA;
-  alignas(64) CUtensorMap tw_quarter, tw2, th2;
-  if (!make_tmap_2d_bf16(&tw_quarter, W_bf16, uint64_t(d), uint64_t(V), uint64_t(d) * 2, BK, BN / 4))
-    return KD_ERR_CUDA;
+  alignas(64) CUtensorMap tw2, th2;
   const bool d64 = d % 64 == 0;  // two k-blocks per box for CTA pairs
   if (d64 && !make_tmap_mn2_bf16(&tw2, W_bf16, uint64_t(d), uint64_t(V), uint64_t(d) * 2, BN / 2)) return KD_ERR_CUDA;
   if (z_store) {
@@ -442,7 +418,7 @@ static int fwd_impl(const void* H_bf16, const void* W_bf16, const int32_t* t_ids
     p.partials = partials; p.rows = n; p.err = &ctrl->err;
     p.a_k3d = p.b_k3d = p.cta_pair && d64;
     e = launch_gemm(p, p.a_k3d ? th2 : th,
-                    p.b_k3d ? tw2 : (p.cluster == 4 ? tw_quarter : (p.cluster == 2 ? tw_half : tw)), z_store ? tz : tw,
+                    p.b_k3d ? tw2 : (p.cta_pair ? tw_half : tw), z_store ? tz : tw,
                     grid_max, s);
     if (e != cudaSuccess) return KD_ERR_CUDA;
     e = launch_lse_combine(partials, L.n_groups, n, negent, inv_tau, lse_out + c0, kl + c0, s);
@@ -487,9 +463,6 @@ static int bwd_impl(const void* H_bf16, const void* W_bf16, const int32_t* t_ids
   const bool d64 = d % 64 == 0;  // 3-D two-block views of W and H need whole 64-column blocks
   if (!make_tmap_2d_bf16(&tw_k, W_bf16, uint64_t(d), uint64_t(V), uint64_t(d) * 2, BK, BN)) return KD_ERR_CUDA;
   if (!make_tmap_2d_bf16(&tw_k_half, W_bf16, uint64_t(d), uint64_t(V), uint64_t(d) * 2, BK, BN / 2))
-    return KD_ERR_CUDA;
-  alignas(64) CUtensorMap tw_k_quarter;
-  if (!make_tmap_2d_bf16(&tw_k_quarter, W_bf16, uint64_t(d), uint64_t(V), uint64_t(d) * 2, BK, BN / 4))
     return KD_ERR_CUDA;
   if (!make_tmap_2d_f32(&tgw, grad_W, uint64_t(d), uint64_t(V), uint64_t(d) * 4, 32, 32)) return KD_ERR_CUDA;
   if (!make_tmap_2d_bf16(&tw_mn, W_bf16, uint64_t(d), uint64_t(V), uint64_t(d) * 2, 64, BK)) return KD_ERR_CUDA;
@@ -545,7 +518,7 @@ static int bwd_impl(const void* H_bf16, const void* W_bf16, const int32_t* t_ids
     p.dz = dz; p.ldz = L.ldz; p.rows = n; p.err = &ctrl->err;
     p.a_k3d = p.b_k3d = p.cta_pair && d64;
     e = launch_gemm(p, p.a_k3d ? th_k2 : th_k,
-                    p.b_k3d ? tw_k2 : (p.cluster == 4 ? tw_k_quarter : (p.cluster == 2 ? tw_k_half : tw_k)), tdz_st,
+                    p.b_k3d ? tw_k2 : (p.cta_pair ? tw_k_half : tw_k), tdz_st,
                     grid_max, s);
     if (e != cudaSuccess) return KD_ERR_CUDA;
     }
@@ -640,7 +613,12 @@ int kd_chunked_kl_bwd(const void* H_bf16, const void* W_bf16, const int32_t* t_i
 }
 
 int kd_get_device_error(void* ws, void* stream, int64_t* detail_out) {
-  if (!ws || !aligned(ws, 256)) return KD_ERR_WORKSPACE;
+  if (ws == nullptr) {
+    // the scratch array of the allocation-free forward on the current device
+    kd_status st = static_scratch_address(&ws);
+    if (st != KD_OK) return st;
+  }
+  if (!aligned(ws, 256)) return KD_ERR_WORKSPACE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaStreamSynchronize(s) != cudaSuccess) return KD_ERR_CUDA;
   uint32_t w[2] = {0, 0};
@@ -678,7 +656,6 @@ int kd_gemm_bf16(const void* A, const void* B, float* C, int64_t M, int64_t N, i
   p.epi = accumulate ? EPI_ACCUM : EPI_STORE;
   p.m_tiles = int((M + BM - 1) / BM);
   set_cluster(p);
-  const int cluster = p.cluster;
   bool ok;
   if (p.cta_pair) {
     // kk 64-deep k-blocks per ring stage; each operand in one box where whole 64-column
@@ -700,7 +677,7 @@ int kd_gemm_bf16(const void* A, const void* B, float* C, int64_t M, int64_t N, i
     ok = a_mn ? make_tmap_2d_bf16(&ta, A, uint64_t(M), uint64_t(K), uint64_t(M) * 2, 64, BK)
               : make_tmap_2d_bf16(&ta, A, uint64_t(K), uint64_t(M), uint64_t(K) * 2, BK, BM);
     ok = ok && (b_mn ? make_tmap_2d_bf16(&tb, B, uint64_t(N), uint64_t(K), uint64_t(N) * 2, 64, BK)
-                     : make_tmap_2d_bf16(&tb, B, uint64_t(K), uint64_t(N), uint64_t(K) * 2, BK, BN / cluster));
+                     : make_tmap_2d_bf16(&tb, B, uint64_t(K), uint64_t(N), uint64_t(K) * 2, BK, BN));
   }
   ok = ok && make_tmap_2d_f32(&tc, C, uint64_t(N), uint64_t(M), uint64_t(N) * 4, 32, 32);
   if (!ok) return KD_ERR_CUDA;

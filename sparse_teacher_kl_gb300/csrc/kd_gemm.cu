@@ -2,10 +2,13 @@
 // fifth-generation tensor cores (tcgen05.mma, fp32 accumulators in tensor
 // memory), fed by TMA, with the loss arithmetic fused into the epilogue.
 //
-// One CTA per SM.  Warp 0 issues TMA loads into a 4-stage shared-memory ring,
-// warp 1 owns tensor memory and issues the MMAs (one thread), warps 2..5 drain
-// finished 128 x 256 accumulators from tensor memory while the next tile is
-// being multiplied into the other half of it (512 columns, double-buffered).
+// One CTA per SM.  Warp 0 issues TMA loads into a shared-memory ring, warp 1
+// owns tensor memory and issues the MMAs (one thread), warps 2..5 drain finished
+// accumulators (128 rows x 256 columns per CTA) from tensor memory while the next
+// tile is being multiplied into the other half of it (512 columns, double-buffered).
+// A product with at least two row tiles runs as CTA pairs (clusters of two): each
+// pair computes a 256 x 256 tile with tcgen05 cta_group::2 MMAs, every CTA loading
+// its own half of both operands with plain (non-multicast) TMA copies.
 //
 // Epilogues (the loss steps of the fused chunked KL, [ART] paragraph on the
 // second fix; [DAI] "As duas inovações" item 2):
@@ -22,6 +25,7 @@
 #include <stdio.h>
 
 #include "kd_device.cuh"
+#include "kd_host_state.h"
 #include "kd_internal.h"
 
 namespace kd {
@@ -114,17 +118,15 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 
   const uint32_t warp = threadIdx.x >> 5;
   const uint32_t lane = lane_id();
-  const uint32_t crank = p.cluster > 1 ? cluster_ctarank() : 0u;
-  const uint16_t cmask = uint16_t((1u << p.cluster) - 1u);
+  const uint32_t crank = CG == 2 ? cluster_ctarank() : 0u;
   const int u_first = int(blockIdx.x) / p.cluster;
   const int u_step = int(gridDim.x) / p.cluster;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < G::kStages; ++s) {
       mbar_init(&tail->full[s], 1);
-      // released by every CTA whose data lands in this stage (B multicast), or once by
-      // the pair's single MMA thread
-      mbar_init(&tail->empty[s], CG == 2 ? 1u : uint32_t(p.cluster));
+      // released once by the MMA thread (for a pair: the first CTA's, on both CTAs)
+      mbar_init(&tail->empty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tail->tfull[a], 1);
@@ -145,7 +147,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (p.cluster > 1) cluster_sync();  // the peer's barriers exist before any multicast reaches them
+  if (CG == 2) cluster_sync();  // the peer's barriers exist before any commit or copy reaches them
   tc_fence_after();
   const uint32_t tmem_base = tail->tmem_base;
 
@@ -230,21 +232,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
               for (int j = 0; j < BM / 64; ++j)
                 tma_load_2d(sa + j * 8192, &tmap_a, &tail->full[s], m_blk * BM + j * 64, kb * BK);
             }
-            if (p.cluster > 1) {
-              // this CTA's half of B, multicast to both CTAs of the pair
-              // this CTA's 1/cluster share of B, multicast to every CTA of the cluster
-              if (p.b_mn == 0) {
-                const int rows = BN / p.cluster;
-                tma_load_2d_mc(sb + crank * (G::kB / p.cluster), &tmap_b, &tail->full[s], kb * BK,
-                               nb * BN + int(crank) * rows, cmask);
-              } else {
-                const int per = (BN / 64) / p.cluster;  // 64-column boxes per CTA
-                for (int j = 0; j < per; ++j) {
-                  const int jj = int(crank) * per + j;
-                  tma_load_2d_mc(sb + jj * 8192, &tmap_b, &tail->full[s], nb * BN + jj * 64, kb * BK, cmask);
-                }
-              }
-            } else if (p.b_mn == 0) {
+            if (p.b_mn == 0) {
               tma_load_2d(sb, &tmap_b, &tail->full[s], kb * BK, nb * BN);
             } else {
 #pragma unroll
@@ -311,7 +299,6 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
               else umma_bf16(d_tmem, ad, bd, idesc, (kb != kb_lo || k != 0) ? 1u : 0u);
             }
             if (CG == 2) umma_commit_pair_mc(&tail->empty[s], 0x3);
-            else if (p.cluster > 1) umma_commit_mc(&tail->empty[s], cmask);
             else umma_commit(&tail->empty[s]);
           }
           if (ok) {
@@ -609,66 +596,85 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (p.cluster > 1) cluster_sync();  // no multicast or remote arrival can still target this CTA
+  if (CG == 2) cluster_sync();  // no commit or remote arrival of the peer can still target this CTA
   tc_fence_after();
   if (warp == 1) {
     if (CG == 2) tmem_dealloc_pair(tmem_base, TMEM_COLS); else tmem_dealloc(tmem_base, TMEM_COLS);
   }
 }
 
-static int g_num_sms = 0;
+static PerDevice<int> g_num_sms;
 
 int gemm_max_grid() {
-  if (g_num_sms == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
-    if (g_num_sms <= 0) g_num_sms = 1;
-  }
-  return g_num_sms;
+  int dev = 0, n = 1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  g_num_sms.get(dev, &n, [](int d, int* v) {
+    if (cudaDeviceGetAttribute(v, cudaDevAttrMultiProcessorCount, d) != cudaSuccess) return 1;
+    if (*v <= 0) *v = 1;
+    return 0;
+  });
+  return n;
 }
 
+// One launch of the engine.  CG = 1: `grid` single CTAs (at most one per unit).  CG = 2:
+// clusters of two CTAs, as many pairs as can be resident at once (at most one per unit).
+// The kernel's shared-memory attribute and the resident pair count are set up once per
+// device (each template instance has its own).
 template <int EPI, int CG, int KKB = 1>
 static cudaError_t launch_one(const GemmProblem& p, const CUtensorMap& ta, const CUtensorMap& tb,
                               const CUtensorMap& tc, int grid, cudaStream_t s) {
-  static bool attr_set = false;
-  static int max_pairs = 0;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kd_gemm_kernel<EPI, CG, KKB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  static PerDevice<int> max_pairs;  // CG = 2: resident clusters; CG = 1: 1 once set up
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  int resident = 1;
+  const int rc = max_pairs.get(dev, &resident, [](int, int* v) {
+    cudaError_t r = cudaFuncSetAttribute(kd_gemm_kernel<EPI, CG, KKB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          int(Geo<CG, KKB>::kSmem));
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+    if (r != cudaSuccess) return int(r);
+    *v = 1;
+    if (CG == 2) {
+      cudaLaunchConfig_t q = {};
+      cudaLaunchAttribute qa[1];
+      qa[0].id = cudaLaunchAttributeClusterDimension;
+      qa[0].val.clusterDim.x = 2;
+      qa[0].val.clusterDim.y = 1;
+      qa[0].val.clusterDim.z = 1;
+      q.attrs = qa;
+      q.numAttrs = 1;
+      q.blockDim = dim3(GEMM_THREADS, 1, 1);
+      q.dynamicSmemBytes = Geo<CG, KKB>::kSmem;
+      q.gridDim = dim3(unsigned((gemm_max_grid() / 2) * 2), 1, 1);
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, kd_gemm_kernel<EPI, CG, KKB>, &q) == cudaSuccess && n >= 1) *v = n;
+    }
+    return 0;
+  });
+  if (rc != 0) return rc > 0 ? cudaError_t(rc) : cudaErrorInvalidDevice;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   cfg.blockDim = dim3(GEMM_THREADS, 1, 1);
   cfg.dynamicSmemBytes = Geo<CG, KKB>::kSmem;
   cfg.stream = s;
-  if (p.cluster > 1) {
+  if (CG == 2) {
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = unsigned(p.cluster);
+    attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (max_pairs == 0) {
-      // persistent grid: as many pairs as can be resident at once
-      cfg.gridDim = dim3(unsigned((gemm_max_grid() / p.cluster) * p.cluster), 1, 1);
-      int n = 0;
-      if (cudaOccupancyMaxActiveClusters(&n, kd_gemm_kernel<EPI, CG, KKB>, &cfg) != cudaSuccess || n < 1) n = 1;
-      max_pairs = n;
-    }
-    int pairs = grid / p.cluster;
-    if (pairs > max_pairs) pairs = max_pairs;
+    int pairs = grid / 2;
+    if (pairs > resident) pairs = resident;
     if (pairs > p.n_units) pairs = p.n_units;
     if (pairs < 1) pairs = 1;
-    cfg.gridDim = dim3(unsigned(pairs * p.cluster), 1, 1);
+    cfg.gridDim = dim3(unsigned(pairs * 2), 1, 1);
   } else {
+    if (grid > p.n_units) grid = p.n_units;
     cfg.gridDim = dim3(unsigned(grid), 1, 1);
     cfg.attrs = nullptr;
     cfg.numAttrs = 0;
   }
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kd_gemm_kernel<EPI, CG, KKB>, ta, tb, tc, p);
+  e = cudaLaunchKernelEx(&cfg, kd_gemm_kernel<EPI, CG, KKB>, ta, tb, tc, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -686,12 +692,11 @@ static const char* gemm_name(int epi, int a_mn, int b_mn) {
 cudaError_t launch_gemm(const GemmProblem& p, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
                         int grid, cudaStream_t s) {
   if (p.n_units <= 0) return cudaSuccess;
-  if (p.cluster != 1 && p.cluster != 2 && p.cluster != 4) return cudaErrorInvalidValue;
-  if (p.cluster == 1 && grid > p.n_units) grid = p.n_units;
+  // CTA pairs run as clusters of two; everything else as single CTAs
+  if (p.cluster != (p.cta_pair ? 2 : 1)) return cudaErrorInvalidValue;
   prof_before(gemm_name(p.epi, p.a_mn, p.b_mn), s);
   cudaError_t e;
   if (p.cta_pair) {
-    if (p.cluster != 2) return cudaErrorInvalidValue;
     const bool two = pair_kblocks(p.a_mn, p.b_mn) == 2;
     switch (p.epi) {
       // the loss sweeps read H and W K-major: always two k-blocks per stage

@@ -7,6 +7,7 @@
 #include <stdint.h>
 
 #include "../../include/kdkl.h"
+#include "kd_host_state.h"
 
 namespace kd {
 
@@ -82,13 +83,12 @@ struct GemmProblem {
   // one box of depth 2 from a 3-D view (64, rows, K / 64); 0: one box per k-block.
   int a_k3d, b_k3d;
   int z_row0;                 // EPI_LSE_Z: row of the stored logits that chunk row 0 maps to
-  // cluster = 2 or 4: the CTAs of a cluster take consecutive m tiles of the same n tile
-  // and share the B operand: each loads 1/cluster of it (K-major B map box 64 x 256/cluster)
-  // multicast to all of them.  n_units then counts clusters' units.  cluster = 1: every
-  // CTA loads its own operands.
+  // cluster: CTAs per cluster, 2 for CTA pairs (cta_pair = 1), else 1.  The CTAs of a
+  // pair take consecutive m tiles of the same n tile; n_units counts pairs' units.
   int cluster;
-  // cta_pair = 1 (requires cluster = 2): each pair computes one 256 x 256 tile with
-  // tcgen05 cta_group::2 MMAs (A split by rows, B by columns between the two CTAs).
+  // cta_pair = 1 (cluster = 2): each pair computes one 256 x 256 tile with tcgen05
+  // cta_group::2 MMAs (A split by rows, B by columns between the two CTAs, each CTA
+  // loading its own halves; K-major B map box 64 x 128).
   int cta_pair;
   // EPI_STORE / EPI_ACCUM
   void* C;
@@ -138,6 +138,20 @@ bool make_tmap_mn2_bf16(CUtensorMap* map, const void* base, uint64_t cols, uint6
 bool make_tmap_2d_f32(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
                       uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer);
 
+// Raise a kernel's dynamic shared-memory limit to `bytes` once per device (safe from
+// several host threads; `done` is the kernel's own per-device record).
+inline cudaError_t smem_attr_once(PerDevice<int>& done, const void* func, int bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  int v = 0;
+  const int rc = done.get(dev, &v, [&](int, int* out) {
+    *out = 1;
+    return int(cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes));
+  });
+  return rc == 0 ? cudaSuccess : (rc > 0 ? cudaError_t(rc) : cudaErrorInvalidDevice);
+}
+
 // Launchers (return a cudaError_t).
 // tc: output map for the epilogues that write through TMA (EPI_ACCUM: fp32 C,
 // box 32 x 32; EPI_DZ: bf16 dZ, box 64 x 32; both 128-byte swizzle); ignored
@@ -176,6 +190,10 @@ cudaError_t launch_split_reduce(const float* parts, int splits, int64_t split_st
                                 int out_bf16, cudaStream_t s);
 
 constexpr int KD_MAX_SPLITS = 8;
+
+// Device address of the library's own scratch array (kd_fused_kl_fwd_static) on the
+// current device, looked up once per device and context.
+kd_status static_scratch_address(void** out);
 
 // Profiling hooks (kd_abi.cu): bracket a launch with events when enabled.
 void prof_before(const char* name, cudaStream_t s);

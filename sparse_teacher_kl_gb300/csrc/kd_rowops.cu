@@ -115,13 +115,10 @@ cudaError_t launch_teacher_prologue(const int32_t* ids, const float* tlog, int r
   int KP = 32;
   while (KP < K) KP <<= 1;
   const size_t smem = size_t(PRO_WARPS) * KP * sizeof(unsigned long long);
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kd_teacher_prologue_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         int(PRO_WARPS * 1024 * sizeof(unsigned long long)));
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static PerDevice<int> attr;
+  cudaError_t e = smem_attr_once(attr, reinterpret_cast<const void*>(kd_teacher_prologue_kernel),
+                                 int(PRO_WARPS * 1024 * sizeof(unsigned long long)));
+  if (e != cudaSuccess) return e;
   const int grid = (rows + PRO_WARPS - 1) / PRO_WARPS;
   prof_before("kd_teacher_prologue", s);
   kd_teacher_prologue_kernel<<<grid, PRO_WARPS * 32, smem, s>>>(ids, tlog, rows, K, KP, V, inv_tau, ids_sorted,

@@ -1213,16 +1213,12 @@ template <class C>
 cudaError_t launch_topk_tma(const uint16_t* X, int64_t N, int64_t V, int64_t ld, int K, int32_t* ids, float* vals,
                             float* lse, uint32_t* err, cudaStream_t s, const uint32_t* guess_in, uint32_t* guess_out,
                             const uint16_t* tile_max, int64_t ld_tile_max, int ntiles) {
-  static bool attr = false;
+  static PerDevice<int> attr_plain, attr_lse;
   const int smem = int(C::WARPS * sizeof(TopkTmaSmem<C>));
-  if (!attr) {
-    cudaError_t e =
-        cudaFuncSetAttribute(kd_topk_tma_kernel<C, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(kd_topk_tma_kernel<C, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  cudaError_t e = smem_attr_once(attr_plain, reinterpret_cast<const void*>(kd_topk_tma_kernel<C, false>), smem);
+  if (e == cudaSuccess)
+    e = smem_attr_once(attr_lse, reinterpret_cast<const void*>(kd_topk_tma_kernel<C, true>), smem);
+  if (e != cudaSuccess) return e;
   int grid = gemm_max_grid();  // one block of C::WARPS row-streaming warps per SM
   if (int64_t(grid) * C::WARPS > N) grid = int((N + C::WARPS - 1) / C::WARPS);
   if (grid > KD_TOPK_MAX_WARPS / C::WARPS) guess_in = guess_out = nullptr;  // more warps than guess words
@@ -1239,13 +1235,10 @@ cudaError_t launch_topk_tma(const uint16_t* X, int64_t N, int64_t V, int64_t ld,
 cudaError_t launch_topk(const uint16_t* X, int64_t N, int64_t V, int64_t ld, int K, int32_t* ids, float* vals,
                         float* lse, uint32_t* err, cudaStream_t s, const uint32_t* guess_in, uint32_t* guess_out,
                         const uint16_t* tile_max, int64_t ld_tile_max, int ntiles) {
-  static bool attr_set = false;
+  static PerDevice<int> attr;
   const int smem = int(sizeof(TopkSmem));
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kd_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  cudaError_t ea = smem_attr_once(attr, reinterpret_cast<const void*>(kd_topk_kernel), smem);
+  if (ea != cudaSuccess) return ea;
   int grid = 2 * gemm_max_grid();
   if (int64_t(grid) > N) grid = int(N);
   if (grid <= 0) return cudaSuccess;

@@ -84,3 +84,58 @@ def test_static_scratch_rejects_problems_beyond_its_size(kd, cuda_device):
     torch.cuda.synchronize()
     assert st == kd._abi.KD_ERR_WORKSPACE
     assert torch.isnan(loss).all()          # nothing was launched
+
+
+def test_static_scratch_call_allocates_no_device_memory(kd, cuda_device):
+    """After a first call (which looks up the array's address), further calls change
+    neither the device's free memory nor torch's allocator: nothing is allocated."""
+    dev = cuda_device
+    H, W, ids, tlog, mask = _inputs(13, 512, 256, 4096, 16, dev, True)
+    N, d = H.shape
+    V, K = W.shape[0], ids.shape[1]
+    loss = torch.empty((1,), device=dev)
+    lse = torch.empty((N,), device=dev)
+    stream = torch.cuda.current_stream().cuda_stream
+
+    def call():
+        return kd._abi.kd_fused_kl_fwd_static(H.data_ptr(), W.data_ptr(), ids.data_ptr(), tlog.data_ptr(),
+                                              mask.data_ptr(), N, d, V, K, 128, 1.0, loss.data_ptr(),
+                                              lse.data_ptr(), None, stream)
+
+    assert call() == 0
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info(dev)
+    alloc0 = torch.cuda.memory_allocated(dev)
+    for _ in range(3):
+        assert call() == 0
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info(dev)
+    assert free1 == free0
+    assert torch.cuda.memory_allocated(dev) == alloc0
+    assert torch.isfinite(loss).all()
+
+
+def test_static_scratch_error_word_is_readable(kd, cuda_device):
+    """A device-side condition of the static variant (a teacher id out of range) lands in
+    the array's error word, which kd_get_device_error reads and clears given NULL."""
+    import ctypes
+    dev = cuda_device
+    H, W, ids, tlog, _ = _inputs(14, 256, 128, 2048, 16, dev, False)
+    ids = ids.clone()
+    ids[201, 5] = W.shape[0]    # out of range: recorded, never used as an address
+    st, loss, _, _ = _call_static(kd, H, W, ids, tlog, None, 128)
+    assert st == 0
+    stream = torch.cuda.current_stream().cuda_stream
+    detail = ctypes.c_int64(-1)
+    assert kd._abi.kd_get_device_error(None, stream, ctypes.byref(detail)) == kd._abi.KD_ERR_DEVICE
+    assert detail.value == 201
+    assert kd._abi.kd_get_device_error(None, stream, ctypes.byref(detail)) == 0   # reading clears it
+    # the next call starts from a clean control block and matches the workspace forward
+    H2, W2, ids2, tlog2, mask2 = _inputs(15, 256, 128, 2048, 16, dev, True)
+    st, loss_s, lse_s, kl_s = _call_static(kd, H2, W2, ids2, tlog2, mask2, 128)
+    assert st == 0
+    loss_r, lse_r, kl_r = _call_regular(kd, H2, W2, ids2, tlog2, mask2, 128)
+    torch.cuda.synchronize()
+    assert abs(loss_s.item() - loss_r.item()) <= LOSS_RTOL * abs(loss_r.item())
+    assert _close(lse_s, lse_r, ROW_TOL)
+    assert kd._abi.kd_get_device_error(None, stream, ctypes.byref(detail)) == 0
