@@ -9,7 +9,11 @@ per position (the most probable tokens) are kept, together with their token ids.
 Readings: the cache holds the raw logits (not log-probabilities), widened
 exactly from bf16 to fp32; it is ordered by value, highest first; equal values
 are ordered by ascending token id, and the cut at K keeps the lowest ids;
--0.0 and +0.0 are equal.
+-0.0 and +0.0 are equal.  The pages never mention NaN; a NaN logit takes its
+place in the IEEE 754 totalOrder predicate (the ordering the standard defines
+for every bit pattern): positive NaNs above +inf, negative NaNs below -inf,
+and among NaNs of one sign the larger payload further from zero.  The only
+departure from totalOrder is the one above: the two zeros are equal.
 """
 from __future__ import annotations
 
@@ -18,10 +22,32 @@ import numpy as np
 from .kl import bf16_to_f64
 
 
+def rank_keys(bits_row: np.ndarray):
+    """(class, within) of each bf16 element: an element ranks above another when its
+    pair is larger.  class 2 = positive NaN, 1 = a number (infinities included),
+    0 = negative NaN; within a number's class its value (-0.0 == +0.0); within a NaN
+    class the payload (the 7 mantissa bits), negated for negative NaNs, which
+    totalOrder orders further below -inf the larger their payload."""
+    b = np.asarray(bits_row).astype(np.int64)
+    is_nan = ((b & 0x7F80) == 0x7F80) & ((b & 0x007F) != 0)
+    negative = (b & 0x8000) != 0
+    cls = np.where(is_nan, np.where(negative, 0, 2), 1)
+    payload = (b & 0x007F).astype(np.float64)
+    with np.errstate(invalid="ignore"):
+        value = bf16_to_f64(b.astype(np.uint16))
+    within = np.where(is_nan, np.where(negative, -payload, payload), value)
+    return cls, within
+
+
+def widen_bits(bits: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns to fp32 with every bit kept (NaN payloads included)."""
+    return (np.asarray(bits).astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
 def topk_cache(bits: np.ndarray, K: int):
     """Per row of a bf16 [N, V] logits array (raw uint16 bits): ids int32 [N, K], logits fp32 [N, K].
 
-    A stable lexicographic sort on (-value, id) per row, then the first K.
+    A stable lexicographic sort on (rank descending, id ascending) per row, then the first K.
     """
     bits = np.asarray(bits)
     assert bits.dtype == np.uint16 and bits.ndim == 2
@@ -32,10 +58,10 @@ def topk_cache(bits: np.ndarray, K: int):
     vals = np.empty((N, K), dtype=np.float32)
     col = np.arange(V)
     for r in range(N):
-        v = bf16_to_f64(bits[r])
-        order = np.lexsort((col, -v))[:K]          # primary key: -value; secondary: id
+        cls, within = rank_keys(bits[r])
+        order = np.lexsort((col, -within, -cls))[:K]   # keys: -class, then -within, then id
         ids[r] = order
-        vals[r] = v[order].astype(np.float32)
+        vals[r] = widen_bits(bits[r, order])
     return ids, vals
 
 

@@ -141,6 +141,97 @@ def test_topk_small_workload(kd, cuda_device):
     _check(kd, X, w.K, cuda_device)
 
 
+def _oracle_rows_parallel(bits, K, block=256):
+    """oracle.topk_cache and oracle.teacher_logsumexp over every row of a large host array, in
+    row blocks on a pool of spawned workers (the oracle is a per-row sort; spawned, not
+    forked, because this process already holds a CUDA context)."""
+    import multiprocessing as mp
+    import os
+    from functools import partial
+    N = bits.shape[0]
+    blocks = [bits[i:i + block] for i in range(0, N, block)]
+    workers = max(1, min(len(os.sched_getaffinity(0)), 32))
+    with mp.get_context("spawn").Pool(workers) as pool:
+        tk = pool.map(partial(oracle.topk_cache, K=K), blocks)
+        lse = pool.map(oracle.teacher_logsumexp, blocks)
+    return (np.concatenate([t[0] for t in tk]), np.concatenate([t[1] for t in tk]), np.concatenate(lse))
+
+
+def test_topk_mid_workload_every_row(kd, cuda_device):
+    """The 8192 x 151936 dense teacher logits N(0, 2), K = 100: three launches (one with the row
+    logsumexp), every row of each compared with the oracle: ids and value bits exact, logsumexp
+    within 1e-5 of its magnitude.  Three launches so that a fault that strikes about once per
+    launch (a race between a ring refill and a read, say) cannot pass unseen."""
+    w = WORKLOADS["mid"]
+    dev = cuda_device
+    X = make_dense_teacher_logits(w.N, w.V, seed=w.seed, device=dev)
+    ws = kd.workspace(kd._abi.kd_topk_cache_workspace(w.N, w.V, w.K), dev)
+    outs = []
+    lse = torch.empty((w.N,), dtype=torch.float32, device=dev)
+    for run in range(3):
+        ids = torch.empty((w.N, w.K), dtype=torch.int32, device=dev)
+        vals = torch.empty((w.N, w.K), dtype=torch.float32, device=dev)
+        st = kd._abi.kd_topk_cache(X.data_ptr(), w.N, w.V, w.V, w.K, ids.data_ptr(), vals.data_ptr(),
+                                   lse.data_ptr() if run == 1 else None, ws.data_ptr(), ws.numel(),
+                                   torch.cuda.current_stream().cuda_stream)
+        assert st == 0
+        outs.append((ids, vals))
+    torch.cuda.synchronize()
+    assert kd.device_error(ws) == (0, 0)
+    bits = bf16_bits(X)
+    del X
+    rid, rval, rlse = _oracle_rows_parallel(bits, w.K)
+    for run, (ids, vals) in enumerate(outs):
+        gid, gval = ids.cpu().numpy(), vals.cpu().numpy()
+        bad = np.flatnonzero(np.any(gid != rid, axis=1) | np.any(gval.view(np.uint32) != rval.view(np.uint32), axis=1))
+        assert bad.size == 0, f"launch {run}: {bad.size} rows differ, first {bad[:8].tolist()}"
+    glse = lse.cpu().numpy().astype(np.float64)
+    assert np.max(np.abs(glse - rlse)) <= 1e-5 * np.max(np.abs(rlse))
+
+
+def test_topk_nan_rows(kd, cuda_device):
+    """Rows holding NaNs of both signs and several payloads among ordinary values and
+    infinities, ordered as the IEEE 754 totalOrder with the two zeros equal: positive NaNs
+    above +inf, negative NaNs below -inf."""
+    g = torch.Generator().manual_seed(31)
+    N, V = 40, 6000
+    X = torch.randn((N, V), generator=g).to(torch.bfloat16)
+    b = X.view(torch.int16)
+    pos_nan = [0x7FC0, 0x7F81, 0x7FFF, 0x7FA5]
+    neg_nan = [0xFFC0 - 0x10000, 0xFF81 - 0x10000, 0xFFFF - 0x10000]
+    for r in range(N):
+        cols = torch.randperm(V, generator=g)[: 3 + (r % 9) * 17]
+        for j, c in enumerate(cols.tolist()):
+            if r % 5 == 4:
+                b[r, c] = neg_nan[j % 3]                      # only negative NaNs in this row
+            else:
+                b[r, c] = (pos_nan + neg_nan)[j % 7]
+        if r % 3 == 0:
+            b[r, (r * 37) % V] = 0x7F80                        # +inf
+            b[r, (r * 53) % V] = 0xFF80 - 0x10000              # -inf
+    b[N - 1, :] = 0x7FC0                                       # a row of one NaN pattern: lowest ids
+    for K in (1, 100, 300):
+        _check_ids_and_bits(kd, X, K, cuda_device)
+
+
+def _check_ids_and_bits(kd, X_host, K, dev):
+    """As _check for rows whose logsumexp is not a number: ids and value bits only."""
+    N, V = X_host.shape
+    Xd = X_host.to(dev)
+    ids = torch.empty((N, K), dtype=torch.int32, device=dev)
+    vals = torch.empty((N, K), dtype=torch.float32, device=dev)
+    ws = kd.workspace(kd._abi.kd_topk_cache_workspace(N, V, K), dev)
+    st = kd._abi.kd_topk_cache(Xd.data_ptr(), N, V, V, K, ids.data_ptr(), vals.data_ptr(), None, ws.data_ptr(),
+                               ws.numel(), torch.cuda.current_stream().cuda_stream)
+    assert st == 0
+    torch.cuda.synchronize()
+    assert kd.device_error(ws) == (0, 0)
+    rid, rval = oracle.topk_cache(bf16_bits(X_host), K)
+    gid, gval = ids.cpu().numpy(), vals.cpu().numpy()
+    assert np.array_equal(gid, rid), f"K={K}: ids differ in rows {np.flatnonzero(np.any(gid != rid, axis=1))[:8]}"
+    assert np.array_equal(gval.view(np.uint32), rval.view(np.uint32)), f"K={K}: value bits differ"
+
+
 def test_topk_mid_workload_sampled(kd, cuda_device):
     """The 8192 x 151936 dense teacher logits N(0, 2); the oracle checks a sample of rows."""
     w = WORKLOADS["mid"]

@@ -109,13 +109,36 @@ def test_kl_mutant_is_caught(name, old, new):
         assert not all_kl_pins(mutant), f"no pin caught mutant: {name}"
 
 
-def test_topk_tie_mutant_is_caught():
-    old, new = "np.lexsort((col, -v))", "np.lexsort((-col, -v))"
-    assert TOPK_SRC.count(old) == 1
+def _topk_mutant(old, new):
+    assert TOPK_SRC.count(old) == 1, f"mutation anchor not unique: {old}"
     kl_mod = _load(KL_SRC, "oracle_kl_for_topk_mutant")
     src = TOPK_SRC.replace(old, new).replace("from .kl import bf16_to_f64", "")
     mut = _load(src, "oracle_topk_mutant")
     mut.bf16_to_f64 = kl_mod.bf16_to_f64
+    return mut, kl_mod
+
+
+# Slips in the NaN reading: NaN ranked by its numeric comparison (last, the behaviour of a
+# plain sort on values), the payload order of negative NaNs not reversed, and values
+# re-rounded through float64 (a signalling NaN comes back quieted).
+TOPK_NAN_MUTANTS = [
+    ("nan_class_dropped", "np.lexsort((col, -within, -cls))", "np.lexsort((col, -within, 0 * cls))"),
+    ("negative_payload_not_reversed", "np.where(negative, -payload, payload)", "payload"),
+    ("values_through_float64", "vals[r] = widen_bits(bits[r, order])",
+     "vals[r] = bf16_to_f64(bits[r, order]).astype(np.float32)"),
+]
+
+
+@pytest.mark.parametrize("name,old,new", TOPK_NAN_MUTANTS, ids=[m[0] for m in TOPK_NAN_MUTANTS])
+def test_topk_nan_mutant_is_caught(name, old, new):
+    from test_oracle_pins import nan_order_pin
+    mut, _ = _topk_mutant(old, new)
+    with np.errstate(all="ignore"):
+        assert not nan_order_pin(mut.topk_cache), f"no pin caught mutant: {name}"
+
+
+def test_topk_tie_mutant_is_caught():
+    mut, kl_mod = _topk_mutant("np.lexsort((col, -within, -cls))", "np.lexsort((-col, -within, -cls))")
     rng = np.random.default_rng(0)
     import torch
     x = np.round(rng.standard_normal((4, 64)) * 2) / 2

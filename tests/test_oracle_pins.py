@@ -233,6 +233,38 @@ def test_topk_bruteforce_with_ties():
     assert list(ids[0]) == list(range(7))                     # all equal: lowest ids
 
 
+# NaN reading (the pages never mention NaN): IEEE 754 totalOrder with the two zeros
+# equal.  The expected order below is written out by hand from the standard's
+# description (+NaN above +inf, larger payload further out; -NaN below -inf, larger
+# payload further down), not computed.
+NAN_ROW_BITS = [0x3F80,   # 0: 1.0
+                0x7FC0,   # 1: +NaN, payload 0x40
+                0xFF80,   # 2: -inf
+                0xFFC0,   # 3: -NaN, payload 0x40
+                0x7F80,   # 4: +inf
+                0x0000,   # 5: +0
+                0x8000,   # 6: -0 (equal to +0: the lower id first)
+                0x7F81,   # 7: +NaN, payload 0x01
+                0xC000,   # 8: -2.0
+                0xFF81]   # 9: -NaN, payload 0x01
+NAN_ROW_ORDER = [1, 7, 4, 0, 5, 6, 8, 2, 9, 3]
+
+
+def nan_order_pin(topk_fn) -> bool:
+    bits = np.array([NAN_ROW_BITS], dtype=np.uint16)
+    ok = True
+    for K in (1, 4, 10):
+        ids, vals = topk_fn(bits, K)
+        ok &= list(ids[0]) == NAN_ROW_ORDER[:K]
+        # values are the input bits widened, payloads kept
+        ok &= list(vals[0].view(np.uint32) >> 16) == [NAN_ROW_BITS[i] for i in NAN_ROW_ORDER[:K]]
+    return bool(ok)
+
+
+def test_topk_nan_order_by_hand():
+    assert nan_order_pin(topk_cache)
+
+
 def test_bf16_widening_is_exact():
     x = np.array([1.0, -2.5, 3.140625, 65280.0, 1e-38, -0.0], dtype=np.float32)
     bits = _bf16_bits_of(x)
