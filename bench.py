@@ -129,7 +129,7 @@ def bench_topk(kd, dev, stream, peaks, steps):
     for name, lp in (("ids+vals", None), ("ids+vals+lse", lse)):
         def run():
             st = kd._abi.kd_topk_cache(X.data_ptr(), N, V, V, K, ids.data_ptr(), vals.data_ptr(),
-                                       None if lp is None else lp.data_ptr(), ws.data_ptr(), ws.numel(),
+                                       None if lp is None else lp.data_ptr(), None, ws.data_ptr(), ws.numel(),
                                        stream.cuda_stream)
             assert st == 0
         for _ in range(3):
@@ -145,8 +145,11 @@ def bench_topk(kd, dev, stream, peaks, steps):
         ms = a.elapsed_time(b) / steps
         byts = N * V * 2 + N * K * 8 + (N * 4 if lp is not None else 0)
         gbs = byts / (ms * 1e-3) / 1e9
+        # rows selected a second time after a speculative start (control block word 2), per launch
+        resel = int(ws[8:12].view(torch.int32).item()) / (steps + 3)
+        ws[8:12].zero_()
         out[name] = {"ms": ms, "achieved_gbs": gbs, "peak_gbs": peaks["hbm"], "frac": gbs / peaks["hbm"],
-                     "bytes_per_launch": byts}
+                     "bytes_per_launch": byts, "reselected_rows_per_launch": resel}
     out["roofline"] = {"bound": "hbm", "achieved": out["ids+vals"]["achieved_gbs"], "peak": peaks["hbm"],
                        "unit": "GB/s", "frac": out["ids+vals"]["frac"], "traffic": ncu_traffic("kd_topk_cache", "mid"),
                        "peak_source": f"{peaks['source']} copy bandwidth"}
@@ -171,7 +174,7 @@ def bench_teacher_topk(kd, dev, stream, peaks, steps):
 
     def run():
         st = kd._abi.kd_teacher_topk(Ht.data_ptr(), Wt.data_ptr(), N, dt, V, K, c, ids.data_ptr(), vals.data_ptr(),
-                                     None, ws.data_ptr(), ws.numel(), stream.cuda_stream)
+                                     None, None, ws.data_ptr(), ws.numel(), stream.cuda_stream)
         assert st == 0
     for _ in range(2):
         run()

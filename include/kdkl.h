@@ -73,7 +73,9 @@ KD_API int kd_version(void);
  * token ids, are kept and reused.
  * ------------------------------------------------------------------------ */
 
-/* Workspace bytes kd_topk_cache needs (>= 256; it holds the error word). */
+/* Workspace bytes kd_topk_cache needs (>= 256; it holds the control block: the error
+ * word read by kd_get_device_error, and as its third uint32 (byte offset 8) a count, which
+ * the caller may read and reset, of rows selected a second time, see below). */
 KD_API size_t kd_topk_cache_workspace(int64_t N, int64_t V, int K);
 
 /*
@@ -84,22 +86,27 @@ KD_API size_t kd_topk_cache_workspace(int64_t N, int64_t V, int K);
  *   K           : 1 <= K <= min(V, KD_MAX_K).
  *   ids_out     : [N, K] int32, written.   vals_out: [N, K] fp32, written.
  *   lse_out     : [N] fp32 or NULL.  If given, also the full-row logsumexp of the
- *                 logits, so that the probability mass the cache drops,
- *                 1 - sum_k exp(vals_k - lse), can be reported ([ART] paragraph on
- *                 the top-K limitation: the cache loses the teacher's tail).
+ *                 logits (fp32 running max and sum of exponentials).
+ *   dropped_out : [N] fp32 or NULL.  If given, the teacher probability the cache
+ *                 drops per row, 1 - sum_k exp(vals_k - lse) (the softmax of the
+ *                 full row outside its K kept logits, [ART] paragraph on the top-K
+ *                 limitation: the cache loses the teacher's tail), computed in the
+ *                 same pass (fp32, compensated sum; NaN where lse is not finite).
  * Each output row is ordered by value, highest first; equal values are ordered
  * by ascending id and the cut at K keeps the lowest ids; -0.0 equals +0.0.
- * Values are the bf16 inputs widened exactly.  NaN inputs are ordered by their
- * sign bit like any other bit pattern (positive NaN above +inf).
- * Performance note: rows are streamed by warps, each over several rows.  With
- * KD_TOPK_GUESS=1 in the environment a warp starts each row after its first from a
- * threshold guessed from the row before and checks it when the row ends: faster
- * when consecutive rows have the same scale, slower when their scales differ by a
- * few percent, since a row whose guess was too high is read a second time.  The
- * result never depends on the guesses.
+ * Values are the bf16 inputs widened exactly.  NaN inputs take their place in
+ * the IEEE 754 totalOrder (positive NaNs above +inf, negative NaNs below -inf,
+ * a larger payload further out); apart from the zeros, that is the order.
+ * Performance note: each row is streamed once by one warp.  Its selection starts
+ * from a threshold taken from the row's first 4096 values, extrapolated into its
+ * upper tail (invariant to the row's offset and scale); when fewer than K values
+ * reach it (rows whose first 4096 values are far above the rest, for instance),
+ * the row is read and selected a second time from an exact bound, the count in
+ * the control block's third word goes up, and that warp stops extrapolating for
+ * the rest of the call.  The result never depends on the start.
  */
 KD_API int kd_topk_cache(const void* logits_bf16, int64_t N, int64_t V, int64_t ld, int K,
-                  int32_t* ids_out, float* vals_out, float* lse_out,
+                  int32_t* ids_out, float* vals_out, float* lse_out, float* dropped_out,
                   void* ws, size_t ws_bytes, void* stream);
 
 /*
@@ -109,13 +116,14 @@ KD_API int kd_topk_cache(const void* logits_bf16, int64_t N, int64_t V, int64_t 
  * (fp32 accumulation, rounded once to bf16 as a bf16 teacher would emit them) into a
  * [chunk, V] workspace buffer and reduced to their top K right away, so the dense
  * [N, V] teacher logits never exist.  Outputs as kd_topk_cache (ids, vals, optional
- * row logsumexp).  dt % 8 == 0; chunk a multiple of 128.  The workspace also holds
- * 16 KB of per-warp selection thresholds carried from one chunk's rows to the next's
- * (a start guess, verified per row: results never depend on it).
+ * row logsumexp and dropped mass).  dt % 8 == 0; chunk a multiple of 128.  The
+ * workspace holds the [chunk, V] bf16 logits and, per row and 256-column tile, the
+ * tile's largest logit, which the projection's epilogue emits: with at least K
+ * tiles, their K-th largest is an exact start for the row's selection.
  */
 KD_API size_t kd_teacher_topk_workspace(int64_t N, int64_t dt, int64_t V, int K, int64_t chunk);
 KD_API int kd_teacher_topk(const void* Ht_bf16, const void* Wt_bf16, int64_t N, int64_t dt, int64_t V, int K,
-                           int64_t chunk, int32_t* ids_out, float* vals_out, float* lse_out,
+                           int64_t chunk, int32_t* ids_out, float* vals_out, float* lse_out, float* dropped_out,
                            void* ws, size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------------------------------ *

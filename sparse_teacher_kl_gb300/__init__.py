@@ -21,7 +21,6 @@ from ._abi import KDError, KD_MAX_K
 __all__ = [
     "topk_cache",
     "teacher_topk",
-    "dropped_mass",
     "fused_kl",
     "fused_kl_forward",
     "fused_kl_backward",
@@ -63,49 +62,46 @@ def _require_cuda(*ts):
             raise ValueError("all tensors must be contiguous")
 
 
-def topk_cache(logits: torch.Tensor, K: int, ws: Optional[torch.Tensor] = None, with_lse: bool = False):
-    """Top-K teacher cache of a dense bf16 [N, V] logits tensor: (ids int32 [N, K], vals fp32 [N, K]),
-    plus the full-row logsumexp [N] when ``with_lse`` (see :func:`dropped_mass`)."""
+def topk_cache(logits: torch.Tensor, K: int, ws: Optional[torch.Tensor] = None, with_lse: bool = False,
+               with_dropped: bool = False):
+    """Top-K teacher cache of a dense bf16 [N, V] logits tensor: (ids int32 [N, K], vals fp32 [N, K]), then,
+    when asked, the full-row logsumexp [N] (``with_lse``) and the teacher probability outside the K kept
+    logits [N] (``with_dropped``), both computed by the kernel in the same pass."""
     _require_cuda(logits)
     if logits.dtype != torch.bfloat16 or logits.dim() != 2:
         raise ValueError("logits must be a 2-D bf16 tensor")
     N, V = logits.shape
-    ids = torch.empty((N, K), dtype=torch.int32, device=logits.device)
-    vals = torch.empty((N, K), dtype=torch.float32, device=logits.device)
-    need = _abi.kd_topk_cache_workspace(N, V, K)
+    dev = logits.device
+    ids = torch.empty((N, K), dtype=torch.int32, device=dev)
+    vals = torch.empty((N, K), dtype=torch.float32, device=dev)
     if ws is None:
-        ws = workspace(need, logits.device)
-    lse = torch.empty((N,), dtype=torch.float32, device=logits.device) if with_lse else None
-    st = _abi.kd_topk_cache(_ptr(logits), N, V, logits.stride(0), K, _ptr(ids), _ptr(vals), _ptr(lse), _ptr(ws),
-                            ws.numel(), _stream(logits.device))
+        ws = workspace(_abi.kd_topk_cache_workspace(N, V, K), dev)
+    lse = torch.empty((N,), dtype=torch.float32, device=dev) if with_lse else None
+    dropped = torch.empty((N,), dtype=torch.float32, device=dev) if with_dropped else None
+    st = _abi.kd_topk_cache(_ptr(logits), N, V, logits.stride(0), K, _ptr(ids), _ptr(vals), _ptr(lse), _ptr(dropped),
+                            _ptr(ws), ws.numel(), _stream(dev))
     _abi.check(st, "kd_topk_cache")
-    return (ids, vals, lse) if with_lse else (ids, vals)
+    return (ids, vals) + ((lse,) if with_lse else ()) + ((dropped,) if with_dropped else ())
 
 
 def teacher_topk(Ht: torch.Tensor, Wt: torch.Tensor, K: int, chunk: int = 1024, with_lse: bool = False,
-                 ws: Optional[torch.Tensor] = None):
+                 with_dropped: bool = False, ws: Optional[torch.Tensor] = None):
     """Top-K cache straight from teacher hidden states Ht [N, dt] and LM-head Wt [V, dt] (bf16): the
-    teacher logits exist only one chunk at a time (see kd_teacher_topk)."""
+    teacher logits exist only one chunk at a time (see kd_teacher_topk).  Returns as topk_cache."""
     _require_cuda(Ht, Wt)
     N, dt = Ht.shape
     V = Wt.shape[0]
-    ids = torch.empty((N, K), dtype=torch.int32, device=Ht.device)
-    vals = torch.empty((N, K), dtype=torch.float32, device=Ht.device)
-    lse = torch.empty((N,), dtype=torch.float32, device=Ht.device) if with_lse else None
+    dev = Ht.device
+    ids = torch.empty((N, K), dtype=torch.int32, device=dev)
+    vals = torch.empty((N, K), dtype=torch.float32, device=dev)
+    lse = torch.empty((N,), dtype=torch.float32, device=dev) if with_lse else None
+    dropped = torch.empty((N,), dtype=torch.float32, device=dev) if with_dropped else None
     if ws is None:
-        ws = workspace(_abi.kd_teacher_topk_workspace(N, dt, V, K, chunk), Ht.device)
-    st = _abi.kd_teacher_topk(_ptr(Ht), _ptr(Wt), N, dt, V, K, chunk, _ptr(ids), _ptr(vals), _ptr(lse), _ptr(ws),
-                              ws.numel(), _stream(Ht.device))
+        ws = workspace(_abi.kd_teacher_topk_workspace(N, dt, V, K, chunk), dev)
+    st = _abi.kd_teacher_topk(_ptr(Ht), _ptr(Wt), N, dt, V, K, chunk, _ptr(ids), _ptr(vals), _ptr(lse), _ptr(dropped),
+                              _ptr(ws), ws.numel(), _stream(dev))
     _abi.check(st, "kd_teacher_topk")
-    return (ids, vals, lse) if with_lse else (ids, vals)
-
-
-def dropped_mass(vals: torch.Tensor, lse: torch.Tensor, tau: float = 1.0) -> torch.Tensor:
-    """Teacher probability outside the cached top-K per position, 1 - sum_k softmax(t)_k over the full
-    vocabulary (at tau = 1: 1 - sum_k exp(vals_k - lse)).  A diagnostic on the host side of the cache."""
-    if tau != 1.0:
-        raise ValueError("the cached logsumexp is taken at temperature 1")
-    return 1.0 - torch.exp(vals - lse[:, None]).sum(dim=1)
+    return (ids, vals) + ((lse,) if with_lse else ()) + ((dropped,) if with_dropped else ())
 
 
 def fused_kl_forward(H, W, ids, tlog, mask=None, chunk=4096, tau=1.0, ws=None, kl_out=None):

@@ -36,11 +36,11 @@ _SIGNATURES = {
     "kd_status_string": (ctypes.c_char_p, [_c_int]),
     "kd_version": (_c_int, []),
     "kd_topk_cache_workspace": (_c_size, [_c_i64, _c_i64, _c_int]),
-    "kd_topk_cache": (_c_int, [_c_ptr, _c_i64, _c_i64, _c_i64, _c_int, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_size,
-                               _c_ptr]),
+    "kd_topk_cache": (_c_int, [_c_ptr, _c_i64, _c_i64, _c_i64, _c_int, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr,
+                               _c_size, _c_ptr]),
     "kd_teacher_topk_workspace": (_c_size, [_c_i64, _c_i64, _c_i64, _c_int, _c_i64]),
     "kd_teacher_topk": (_c_int, [_c_ptr, _c_ptr, _c_i64, _c_i64, _c_i64, _c_int, _c_i64, _c_ptr, _c_ptr, _c_ptr, _c_ptr,
-                                 _c_size, _c_ptr]),
+                                 _c_ptr, _c_size, _c_ptr]),
     "kd_fused_kl_workspace": (_c_size, [_c_i64, _c_i64, _c_i64, _c_int, _c_i64]),
     "kd_fused_kl_fwd": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_i64, _c_i64, _c_i64, _c_int, _c_i64,
                                  _c_float, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_size, _c_ptr]),

@@ -236,24 +236,25 @@ const char* kd_status_string(int status) {
 int kd_version(void) { return 100; }
 
 size_t kd_topk_cache_workspace(int64_t N, int64_t V, int K) {
-  (void)N; (void)V; (void)K;
-  return sizeof(Ctrl);
+  (void)V;
+  if (N < 1 || K < 1) return sizeof(Ctrl);
+  return sizeof(Ctrl) + align_up(topk_scratch_bytes(N, K), 256);
 }
 
 int kd_topk_cache(const void* logits_bf16, int64_t N, int64_t V, int64_t ld, int K, int32_t* ids_out,
-                  float* vals_out, float* lse_out, void* ws, size_t ws_bytes, void* stream) {
+                  float* vals_out, float* lse_out, float* dropped_out, void* ws, size_t ws_bytes, void* stream) {
   if (N < 1 || V < 1 || K < 1 || K > KD_MAX_K || int64_t(K) > V || ld < V) return KD_ERR_INVALID_ARG;
   if (V > 0x7fffffffLL || ld % 8 != 0) return KD_ERR_INVALID_ARG;
   if (!logits_bf16 || !ids_out || !vals_out) return KD_ERR_INVALID_ARG;
   if (!aligned(logits_bf16, 16) || !aligned(ids_out, 4) || !aligned(vals_out, 4)) return KD_ERR_INVALID_ARG;
-  if (lse_out && !aligned(lse_out, 4)) return KD_ERR_INVALID_ARG;
+  if ((lse_out && !aligned(lse_out, 4)) || (dropped_out && !aligned(dropped_out, 4))) return KD_ERR_INVALID_ARG;
   if (!ws || !aligned(ws, 256) || ws_bytes < kd_topk_cache_workspace(N, V, K)) return KD_ERR_WORKSPACE;
   kd_status st = check_device();
   if (st != KD_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   Ctrl* ctrl = static_cast<Ctrl*>(ws);
   return map_cuda(launch_topk(static_cast<const uint16_t*>(logits_bf16), N, V, ld, K, ids_out, vals_out, lse_out,
-                              &ctrl->err, s));
+                              dropped_out, &ctrl->err, static_cast<uint8_t*>(ws) + sizeof(Ctrl), s));
 }
 
 size_t kd_fused_kl_workspace(int64_t N, int64_t d, int64_t V, int K, int64_t chunk) {
@@ -261,32 +262,34 @@ size_t kd_fused_kl_workspace(int64_t N, int64_t d, int64_t V, int K, int64_t chu
   return kl_layout(N, d, V, K, chunk).total;
 }
 
-static size_t teacher_topk_ws(int64_t N, int64_t V, int64_t chunk) {
+// Teacher workspace: control block | the chunk's bf16 logits [rows_pad, ldz] | per-tile row
+// maxima [rows_pad, ldt] | the top-K scratch of one chunk.
+static size_t teacher_topk_ws(int64_t N, int64_t V, int K, int64_t chunk) {
   const int64_t c = chunk < N ? chunk : N;
   const int64_t rows_pad = (c + BM - 1) / BM * BM;
   const int64_t ldz = (V + 7) / 8 * 8;
   const int64_t ldt = ((V + BN - 1) / BN + 7) / 8 * 8;  // per-tile row maxima of the logits
-  return sizeof(Ctrl) + align_up(size_t(rows_pad) * size_t(ldz) * 2, 256) + size_t(KD_TOPK_MAX_WARPS) * 4 +
-         align_up(size_t(rows_pad) * size_t(ldt) * 2, 256);
+  return sizeof(Ctrl) + align_up(size_t(rows_pad) * size_t(ldz) * 2, 256) +
+         align_up(size_t(rows_pad) * size_t(ldt) * 2, 256) + align_up(topk_scratch_bytes(c, K), 256);
 }
 
 size_t kd_teacher_topk_workspace(int64_t N, int64_t dt, int64_t V, int K, int64_t chunk) {
   if (N < 1 || dt < 1 || V < 1 || K < 1 || chunk < 1) return 0;
-  return teacher_topk_ws(N, V, chunk);
+  return teacher_topk_ws(N, V, K, chunk);
 }
 
 int kd_teacher_topk(const void* Ht_bf16, const void* Wt_bf16, int64_t N, int64_t dt, int64_t V, int K,
-                    int64_t chunk, int32_t* ids_out, float* vals_out, float* lse_out, void* ws, size_t ws_bytes,
-                    void* stream) {
+                    int64_t chunk, int32_t* ids_out, float* vals_out, float* lse_out, float* dropped_out, void* ws,
+                    size_t ws_bytes, void* stream) {
   if (N < 1 || dt < 8 || dt % 8 != 0 || V < 1 || K < 1 || K > KD_MAX_K || int64_t(K) > V) return KD_ERR_INVALID_ARG;
   if (chunk < BM || chunk % BM != 0 || V > 0x7fffffffLL || N > 0x7fffffffLL || dt > 0x7fffffffLL)
     return KD_ERR_INVALID_ARG;
   if (!Ht_bf16 || !Wt_bf16 || !ids_out || !vals_out) return KD_ERR_INVALID_ARG;
   if (!aligned(Ht_bf16, 16) || !aligned(Wt_bf16, 16) || !aligned(ids_out, 4) || !aligned(vals_out, 4))
     return KD_ERR_INVALID_ARG;
-  if (lse_out && !aligned(lse_out, 4)) return KD_ERR_INVALID_ARG;
+  if ((lse_out && !aligned(lse_out, 4)) || (dropped_out && !aligned(dropped_out, 4))) return KD_ERR_INVALID_ARG;
   if (!ws || !aligned(ws, 256)) return KD_ERR_WORKSPACE;
-  if (ws_bytes < teacher_topk_ws(N, V, chunk)) return KD_ERR_WORKSPACE;
+  if (ws_bytes < teacher_topk_ws(N, V, K, chunk)) return KD_ERR_WORKSPACE;
   kd_status st = check_device();
   if (st != KD_OK) return st;
 
@@ -295,13 +298,14 @@ int kd_teacher_topk(const void* Ht_bf16, const void* Wt_bf16, int64_t N, int64_t
   Ctrl* ctrl = reinterpret_cast<Ctrl*>(w8);
   uint16_t* zbuf = reinterpret_cast<uint16_t*>(w8 + sizeof(Ctrl));
   const int64_t ldz = (V + 7) / 8 * 8;
-  uint32_t* guesses = reinterpret_cast<uint32_t*>(
-      w8 + sizeof(Ctrl) + align_up(size_t((((chunk < N ? chunk : N) + BM - 1) / BM) * BM) * size_t(ldz) * 2, 256));
   // each chunk row's maximum over every BN-column tile of its logits, from the projection's
   // epilogue: their K-th largest starts the row's top-K selection
   const int ntiles = int((V + BN - 1) / BN);
   const int64_t ldt = (int64_t(ntiles) + 7) / 8 * 8;
-  uint16_t* tmax = reinterpret_cast<uint16_t*>(guesses + KD_TOPK_MAX_WARPS);
+  const int64_t crows = chunk < N ? chunk : N;
+  const size_t rows_pad = size_t((crows + BM - 1) / BM * BM);
+  uint16_t* tmax = reinterpret_cast<uint16_t*>(w8 + sizeof(Ctrl) + align_up(rows_pad * size_t(ldz) * 2, 256));
+  void* tk_scratch = reinterpret_cast<uint8_t*>(tmax) + align_up(rows_pad * size_t(ldt) * 2, 256);
   const uint16_t* Ht = static_cast<const uint16_t*>(Ht_bf16);
   const int grid_max = gemm_max_grid();
   // Wt boxes: BN rows for single CTAs, BN / 2 for a CTA pair's halves
@@ -338,10 +342,9 @@ int kd_teacher_topk(const void* Ht_bf16, const void* Wt_bf16, int64_t N, int64_t
     p.a_k3d = p.b_k3d = p.cta_pair && dt64;
     cudaError_t e = launch_gemm(p, p.a_k3d ? th2 : th, p.b_k3d ? tw2 : tw[p.cta_pair], tz, grid_max, s);
     if (e != cudaSuccess) return KD_ERR_CUDA;
-    // exact top-K (and row logsumexp) of those bf16 logits
-    // each warp's threshold guess carries from one chunk's rows into the next chunk's
+    // exact top-K (and row logsumexp, dropped mass) of those bf16 logits
     e = launch_topk(zbuf, n, V, ldz, K, ids_out + c0 * K, vals_out + c0 * K, lse_out ? lse_out + c0 : nullptr,
-                    &ctrl->err, s, c0 == 0 ? nullptr : guesses, guesses, tmax, ldt, ntiles);
+                    dropped_out ? dropped_out + c0 : nullptr, &ctrl->err, tk_scratch, s, tmax, ldt, ntiles);
     if (e != cudaSuccess) return KD_ERR_CUDA;
   }
   return KD_OK;

@@ -26,7 +26,8 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 struct Ctrl {
   uint32_t err;        // KD_DEVERR_*
   uint32_t err_detail;
-  uint32_t pad0[2];
+  uint32_t topk_reselected;  // top-K: rows selected a second time after a speculative start
+  uint32_t pad0;
   int32_t n_valid;     // number of valid positions of the current call
   uint32_t pad1[59];
 };
@@ -160,17 +161,17 @@ cudaError_t launch_gemm(const GemmProblem& p, const CUtensorMap& ta, const CUten
                         int grid, cudaStream_t s);
 int gemm_max_grid();
 
-// Row-streaming warps of one top-K launch are at most this many (one block per SM); a
-// guess array (guess_in / guess_out, KD_TOPK_MAX_WARPS words) carries each warp's next-row
-// threshold guess from one launch into the next over rows of the same source (NULL: none).
-constexpr int KD_TOPK_MAX_WARPS = 4096;
-// tile_max (NULL: none): per row, the maxima of ntiles disjoint column ranges of the row
-// (bf16 bits, [N, ld_tile_max]); with ntiles >= K their K-th largest is a lower bound of
-// the row's K-th largest value and starts the row's selection.
+// Top-K of every row of X [N, ld] bf16 (columns [0, V)): ids and values [N, K], optionally
+// the row logsumexp lse [N] and the dropped teacher mass dropped [N] (NULL: not wanted).
+// err: the workspace control block's error word (its third word counts rows that a
+// speculative start made select twice).  scratch: topk_scratch_bytes(N, K) bytes, 256-byte
+// aligned.  tile_max (NULL: none): per row, the maxima of ntiles disjoint column ranges of
+// the row (bf16 bits, [N, ld_tile_max]); with ntiles >= K their K-th largest is a lower
+// bound of the row's K-th largest value and starts the row.
+size_t topk_scratch_bytes(int64_t N, int K);
 cudaError_t launch_topk(const uint16_t* X, int64_t N, int64_t V, int64_t ld, int K, int32_t* ids,
-                        float* vals, float* lse, uint32_t* err, cudaStream_t s, const uint32_t* guess_in = nullptr,
-                        uint32_t* guess_out = nullptr, const uint16_t* tile_max = nullptr,
-                        int64_t ld_tile_max = 0, int ntiles = 0);
+                        float* vals, float* lse, float* dropped, uint32_t* err, void* scratch, cudaStream_t s,
+                        const uint16_t* tile_max = nullptr, int64_t ld_tile_max = 0, int ntiles = 0);
 
 cudaError_t launch_count_valid(const uint8_t* mask, int64_t N, int32_t* n_valid, cudaStream_t s);
 cudaError_t launch_teacher_prologue(const int32_t* ids, const float* tlog, int rows, int K, int64_t V,

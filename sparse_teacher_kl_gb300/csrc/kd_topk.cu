@@ -46,6 +46,7 @@ struct TopkSmem {
   uint32_t hist[256];
   float red_m[TK_THREADS / 32];
   float red_s[TK_THREADS / 32];
+  float lse_row;  // the row's logsumexp, for the dropped mass
   uint32_t count;
   uint32_t sel_bin;
   uint32_t sel_need;
@@ -225,11 +226,12 @@ __device__ __forceinline__ uint4 load_seg(const uint16_t* xr, int64_t V, int seg
 __global__ void __launch_bounds__(TK_THREADS, 2)
     kd_topk_kernel(const uint16_t* __restrict__ X, int64_t N, int64_t V, int64_t ld, int K,
                    int32_t* __restrict__ ids_out, float* __restrict__ vals_out, float* __restrict__ lse_out,
-                   uint32_t* err) {
+                   float* __restrict__ dropped_out, uint32_t* err) {
   extern __shared__ __align__(16) uint8_t tk_smem_raw[];
   TopkSmem& sm = *reinterpret_cast<TopkSmem*>(tk_smem_raw);
   if (threadIdx.x == 0) sm.err = err;  // read after the first barrier below
   const int nseg = int((V + TK_SEG - 1) / TK_SEG);
+  const bool want_lse = lse_out != nullptr || dropped_out != nullptr;
 
   for (int64_t row = blockIdx.x; row < N; row += gridDim.x) {
     const uint16_t* xr = X + row * ld;
@@ -266,7 +268,7 @@ __global__ void __launch_bounds__(TK_THREADS, 2)
         kb[e] = (i0b + e < V) ? bf16_key(wb[e >> 1] >> (16 * (e & 1))) : 0u;
         tmax = max(tmax, max(ka[e], kb[e]));
       }
-      if (lse_out != nullptr) {
+      if (want_lse) {
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const uint32_t* w = h ? wb : wa;
@@ -332,7 +334,7 @@ __global__ void __launch_bounds__(TK_THREADS, 2)
 #pragma unroll
           for (int e = 0; e < TK_VEC; ++e)
             xf[e] = __uint_as_float((e & 1) ? (w[e >> 1] & 0xFFFF0000u) : (w[e >> 1] << 16));
-          if (lse_out != nullptr) {
+          if (want_lse) {
             float vm = -INFINITY;
             float x2[TK_VEC];
 #pragma unroll
@@ -382,7 +384,7 @@ __global__ void __launch_bounds__(TK_THREADS, 2)
       }
     }
 
-    if (lse_out != nullptr) {
+    if (want_lse) {
       // merge the threads' (max, sum) pairs: warp shuffles, then warp 0 over the warps
       for (int o = 16; o > 0; o >>= 1) {
         const float om = __shfl_xor_sync(0xffffffffu, lm, o);
@@ -407,7 +409,8 @@ __global__ void __launch_bounds__(TK_THREADS, 2)
             M = nm;
           }
         }
-        lse_out[row] = (M + log2f(S)) * 0.69314718055994531f;
+        sm.lse_row = (M + log2f(S)) * 0.69314718055994531f;
+        if (lse_out) lse_out[row] = sm.lse_row;
       }
     }
 
@@ -422,71 +425,115 @@ __global__ void __launch_bounds__(TK_THREADS, 2)
       count = sm.count;
     }
     sort_desc(sm, count);
+    float part = 0.f;  // this thread's share of sum_k exp(v_k - lse) (at most two terms)
     for (int j = threadIdx.x; j < K; j += TK_THREADS) {
       const uint32_t col = ~uint32_t(sm.buf[j]);
       ids_out[row * K + j] = int32_t(col);
-      if (KD_DCHECK(int64_t(col) < V, sm.err, 0x7002)) vals_out[row * K + j] = __uint_as_float(uint32_t(xr[col]) << 16);
+      if (KD_DCHECK(int64_t(col) < V, sm.err, 0x7002)) {
+        const float v = __uint_as_float(uint32_t(xr[col]) << 16);
+        vals_out[row * K + j] = v;
+        if (dropped_out) part += expf(v - sm.lse_row);
+      }
+    }
+    if (dropped_out) {
+      // the teacher probability outside the K kept logits: 1 - sum over the block
+      for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+      __syncthreads();
+      if ((threadIdx.x & 31) == 0) sm.red_s[threadIdx.x >> 5] = part;
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        float tot = 0.f;
+        for (int i = 0; i < TK_THREADS / 32; ++i) tot += sm.red_s[i];
+        dropped_out[row] = 1.f - tot;
+      }
     }
     __syncthreads();
   }
 }
 
 // ---------------------------------------------------------------------------
-// Warp-per-row path for K <= TW_MAXK (the pages' top-100 cache).  The same selection,
-// run by one warp per row so that no block barrier is ever taken:
-//  * the copy engine streams the row: each warp owns a ring of RING slots of GRP warp
+// Warp-per-row path for K <= TW_MAXK (the pages' top-100 cache): two kernels.
+//
+// kd_topk_stream_kernel, one warp per row, no block barrier; it reads every logit once:
+//  * the copy engine streams the row: each warp owns a ring of RING slots of TW_GROUP warp
 //    steps (a step is 256 elements, 16 bytes per lane); lane 0 fills a slot with one bulk
-//    copy completing on the slot's mbarrier, RING groups ahead of its use, running on
-//    into the warp's next row while the current one is finished; every lane fences its
-//    reads of a slot before the warp barrier after which the slot is refilled;
-//  * a first threshold (key >= it) before any element is kept, the first of these that
-//    applies: the K-th largest of per-tile row maxima a producer supplies (the teacher
-//    projection's epilogue); a guess from the warp's previous row, verified when the row
-//    ends (a row short of K entries at or above it is selected again from its start);
-//    the K-th largest of the 8-element vector maxima of the row's first RING x GRP steps,
-//    which the ring already holds when the row begins (quick start);
-//  * each lane tests its 8 values with one packed bf16 max against the threshold, GRP
-//    steps at a time with one vote; a vector that passes is queued whole in shared
-//    memory, and the warp filters BATCH queued vectors at a time (one per lane) with
-//    exact comparisons;
-//  * the warp keeps the row's best K so far as a sorted list and merges each drained
-//    batch into it (a bitonic sort across the lanes and a rank merge); once it holds K
-//    entries its last key is the threshold, exact after every drain: one warp sees the
-//    whole row, so the threshold is as tight as the prefix allows, and the list is the
-//    answer when the row ends.
-// Elements past V read as -inf and are dropped by their column.
+//    copy completing on the slot's mbarrier, RING groups ahead of its use, running on into
+//    the warp's next row while the current one is finished; every lane fences its reads
+//    of a slot before the warp barrier after which the slot is refilled;
+//  * a first threshold before any element is kept: the K-th largest of per-tile row
+//    maxima a producer supplies (the teacher projection's epilogue; exact), else from the
+//    ring's first RING groups, which it holds when the row begins: the K-th largest of
+//    their 512 vector maxima (T0; at least K elements reach it: exact), raised by a
+//    speculative step (below) when that helps;
+//  * the pre-test: per step, each lane's 8 values reduced by three packed bf16 maxima
+//    and compared with the threshold by one packed unordered compare (a NaN passes);
+//  * a vector that passes is queued in the lane's own shared-memory queue by predicated
+//    stores (no warp vote per vector); when a lane's queue is nearly full the warp drains
+//    every queue: one slot at a time, each lane tests its vector's elements exactly and
+//    the warp appends the ones that pass to a candidate buffer; the threshold is then
+//    raised to the K-th largest key of the buffer, and the buffer is filtered to what
+//    reaches it when it runs short of room;
+//  * when the row ends: the K-th largest key T of the buffer, and the candidates that
+//    reach it (K of them, or a few more on ties) handed to a per-row slot of the
+//    workspace; the warp goes on with its next row.
+// kd_topk_emit_kernel, one warp per row: sorts the row's handed-over candidates in
+// registers (a bitonic network across the lanes) and writes the first K: ids, values (the
+// candidates carry their bf16 bits) and, when asked, the dropped teacher mass.
+//
+// The K-th largest key of a set of keys is found by bisection over the 16-bit key space
+// (17 steps of a per-lane count and a warp sum), in registers.
+//
+// Speculative start.  Among the 512 vector maxima of the row's first 4096 elements, the
+// K-th largest T0 and the (K/4)-th largest T1 locate and scale the row's upper tail; the
+// start T0 + c (T1 - T0) is invariant to the row's offset and scale.  A simulation of
+// rows of normal, logistic, Gumbel and uniform values (offset and scale varying per row)
+// put the row's K-th value above T0 + c (T1 - T0) in 99.5 % of rows or more for c up to
+// 1.1 (uniform) and 1.8 (the others); c = TW_SPEC_C puts the start near rank 5 K of a
+// normal row.  At least K elements must reach the start for the selection to be exact:
+// a row where fewer do (its buffer ends short of K) is selected again from its start with
+// T0, and that warp makes no further speculative starts in the launch.  The control
+// block's third word counts such rows.
 
 constexpr int TW_MAXK = 256;
-constexpr int TW_STEP = 32 * TK_VEC;         // elements per warp step
-constexpr int TW_GROUP = 4;                  // steps tested together (one vote)
-constexpr int TW_QUEUE = 64;                 // queued vectors per warp (ring)
+constexpr int TW_STEP = 32 * TK_VEC;   // elements per warp step
+constexpr int TW_GROUP = 4;            // steps per ring slot, tested together
+constexpr int TW_HAND = 256;           // candidates handed over per row, at most
 constexpr float TW_LOG2E = 1.4426950408889634f;
-// Margin of a guessed threshold below the previous row's K-th value, in units of that
-// row's spacing between its (K/2)-th and K-th values (about rank 2.8 K for normal rows).
-constexpr float TW_GUESS_MARGIN = 1.5f;
+constexpr float TW_SPEC_C = 1.3f;      // speculative start: T0 + c (T1 - T0)
+constexpr int TW_SPEC_MIN_K = 16;      // smaller K: too few vector maxima above T1 to place it
 
-// A configuration: CAP candidate entries per warp, WARPS rows in flight per block (one
-// block per SM), BATCH queued vectors filtered per drain (at most 8 * BATCH new
-// entries), MAXK the largest K it serves.  The top list (<= MAXK) and one drain's
-// entries fit in the buffer, and its bitonic sort pads to a power of two within it.
-template <int CAP_, int WARPS_, int BATCH_, int MAXK_>
+// A configuration: CAP candidate entries per warp, WARPS rows in flight per block (one block
+// per SM), QL queued vectors per lane, MAXK the largest K it serves, RING ring slots.  A
+// queue slot adds at most 256 elements, and a filtered buffer over CAP - 256 entries (ties)
+// is cut to its best K; both fit, and the bitonic sort pads to a power of two within CAP.
+template <int CAP_, int WARPS_, int QL_, int MAXK_, int RING_>
 struct TwCfg {
   static constexpr int CAP = CAP_;
   static constexpr int WARPS = WARPS_;
-  static constexpr int BATCH = BATCH_;
+  static constexpr int QL = QL_;
   static constexpr int MAXK = MAXK_;
-  static_assert((CAP & (CAP - 1)) == 0, "the bitonic sort pads to a power of two within the buffer");
-  static_assert(MAXK + 8 * BATCH <= CAP && MAXK <= TW_MAXK && MAXK % 32 == 0, "a drain fits after the list");
-  static_assert(BATCH <= 32 && BATCH + 32 <= TW_QUEUE, "one vector per lane; the queue holds a batch and a step");
+  static constexpr int RING = RING_;
+  static_assert(CAP == 512, "the bisection selects hold the buffer as 16 keys per lane");
+  static_assert(CAP >= MAXK + TW_STEP, "a slot's elements fit after a cut list");
+  static_assert(MAXK <= TW_MAXK && MAXK <= TW_HAND && MAXK <= RING * TW_GROUP * 32, "limits of K");
+  static_assert(QL >= 2 * TW_GROUP, "a group's vectors fit in a lane's queue after the drain check");
+  static_assert(RING == 4, "the quick start holds 16 vector maxima per lane");
 };
+using TmSmallK = TwCfg<512, 12, 8, 128, 4>;    // K <= 128
+using TmLargeK = TwCfg<512, 12, 8, 256, 4>;    // K <= 256
 
-template <int CAP>
-struct TopkWarpSmem {
-  unsigned long long buf[CAP];
-  uint4 qv[TW_QUEUE];
-  uint32_t qcol[TW_QUEUE];
-  uint32_t hist[256];
-  uint32_t* err;  // the workspace error word (checked builds report bad indices there)
+template <class C>
+struct TwSmem {                             // one warp's part of the block's shared memory
+  uint4 ring[C::RING][TW_GROUP][32];        // bulk-copy ring: slot, step, lane
+  uint4 qv[C::QL][32];                      // per-lane queues: slot j of lane l at [j][l]
+  uint32_t qcol[C::QL][32];                 // first column of each queued vector
+  unsigned long long buf[C::CAP];           // candidates (cand_make)
+  uint32_t hist[256];                       // byte histograms (K-th of the tile maxima)
+  uint64_t full[C::RING];
+  uint32_t abort;                           // set by a timed-out wait
+  uint32_t never;                           // stays 0: the flag of the bounded waits after an abort
+  uint32_t* err;                            // the workspace error word (checked builds report there)
+  uint32_t pad[2];
 };
 
 __device__ __forceinline__ void warp_find_bin(const uint32_t* h, uint32_t target, uint32_t& bin, uint32_t& need,
@@ -526,35 +573,6 @@ __device__ __forceinline__ void warp_find_bin(const uint32_t* h, uint32_t target
   above = __shfl_sync(0xffffffffu, ab, owner);
 }
 
-// Warp: K-th largest key among reg[0, cnt) (cnt >= K) and how many keys reach it.
-__device__ uint32_t warp_kth_largest(const unsigned long long* reg, uint32_t cnt, uint32_t K, uint32_t* h,
-                                     uint32_t& count_ge) {
-  const uint32_t lane = lane_id();
-  for (uint32_t i = lane; i < 256; i += 32) h[i] = 0;
-  __syncwarp();
-  for (uint32_t base = 0; base < cnt; base += 32) {
-    const uint32_t i = base + lane;
-    hist_add_warp(h, i < cnt, i < cnt ? comp_key(reg[i]) >> 8 : 0u);
-  }
-  __syncwarp();
-  uint32_t b1, need, above1;
-  warp_find_bin(h, K, b1, need, above1);
-  __syncwarp();
-  for (uint32_t i = lane; i < 256; i += 32) h[i] = 0;
-  __syncwarp();
-  for (uint32_t base = 0; base < cnt; base += 32) {
-    const uint32_t i = base + lane;
-    const uint32_t k = i < cnt ? comp_key(reg[i]) : 0u;
-    hist_add_warp(h, i < cnt && (k >> 8) == b1, k & 255u);
-  }
-  __syncwarp();
-  uint32_t b2, need2, above2;
-  warp_find_bin(h, need, b2, need2, above2);
-  count_ge = above1 + above2 + h[b2];
-  __syncwarp();
-  return (b1 << 8) | b2;
-}
-
 // Warp: K-th largest key among the bf16 values src[0, cnt) in global memory (cnt >= K).
 __device__ uint32_t warp_kth_largest_bf16(const uint16_t* src, uint32_t cnt, uint32_t K, uint32_t* h) {
   const uint32_t lane = lane_id();
@@ -580,32 +598,6 @@ __device__ uint32_t warp_kth_largest_bf16(const uint16_t* src, uint32_t cnt, uin
   warp_find_bin(h, need, b2, need2, above2);
   __syncwarp();
   return (b1 << 8) | b2;
-}
-
-// Warp: keep the entries of reg[0, cnt) with key >= T, in place (each round of 256 is
-// read before any survivor of it is written); returns the new count.
-__device__ uint32_t warp_filter_ge(unsigned long long* reg, uint32_t cnt, uint32_t T) {
-  const uint32_t lane = lane_id();
-  uint32_t out = 0;
-  for (uint32_t base = 0; base < cnt; base += 256) {
-    unsigned long long held[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const uint32_t i = base + lane + 32u * j;
-      held[j] = i < cnt ? reg[i] : 0ull;
-    }
-    __syncwarp();
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const uint32_t i = base + lane + 32u * j;
-      const bool take = i < cnt && comp_key(held[j]) >= T;
-      const uint32_t bal = __ballot_sync(0xffffffffu, take);
-      if (take) reg[out + __popc(bal & ((1u << lane) - 1u))] = held[j];
-      out += __popc(bal);
-    }
-    __syncwarp();
-  }
-  return out;
 }
 
 // Warp: sort reg[0, cnt) descending (bitonic, padded with 0 up to a power of two).
@@ -673,180 +665,6 @@ __device__ __forceinline__ uint32_t key_floor(float x) {
   return bf16_key(b);
 }
 
-// Per-warp selection state (warp-uniform).
-struct WarpSel {
-  uint32_t cnt;   // entries in buf
-  uint32_t qh;    // queue head (ring index of the oldest queued vector)
-  uint32_t nq;    // queued vectors
-  uint32_t wth;   // threshold key
-  bool ge;        // until the list holds K entries: key >= wth is a candidate (wth = 0: every element)
-  float tv;       // pre-test bound: a vector can hold a candidate only if its maximum is > tv
-};
-
-// Warp: merge the T (<= 32) candidates buf[nt, nt + T) into the top list buf[0, nt)
-// (composites, sorted descending, nt <= K <= 32 * SLOTS), keeping the K best, in place.
-// The candidates come from later columns than every list entry and lie in column order,
-// so ranks need only 32-bit keys: a list entry outranks a candidate of equal key, and of
-// two equal candidates the earlier one wins.  The candidates are sorted across the lanes
-// by (key, -index) as one 32-bit word (bitonic, empty lanes last); every element's new
-// place is its index plus the number of elements of the other list above it (binary
-// searches over 32-bit keys); nothing is written until everything is read.  `keys`
-// (>= 32 words) holds the sorted candidate keys.  Returns min(nt + T, K).
-template <int SLOTS>
-__device__ uint32_t warp_merge_top(unsigned long long* buf, uint32_t* keys, uint32_t nt, uint32_t T, uint32_t K) {
-  const uint32_t lane = lane_id();
-  const uint32_t* key_hi = reinterpret_cast<const uint32_t*>(buf) + 1;  // high word of buf[i] at [2 i]
-  uint32_t s = lane < T ? (key_hi[2 * (nt + lane)] << 16) | (0xFFFFu - lane) : 0u;
-#pragma unroll
-  for (uint32_t k = 2; k <= 32; k <<= 1) {
-#pragma unroll
-    for (uint32_t j = k >> 1; j > 0; j >>= 1) {
-      const uint32_t o = __shfl_xor_sync(0xffffffffu, s, j);
-      const bool desc = (lane & k) == 0;
-      const bool low = (lane & j) == 0;
-      s = (low == desc) ? max(s, o) : min(s, o);
-    }
-  }
-  // sorted candidate `lane`: its key, its composite, its place
-  const uint32_t ck = s >> 16;
-  const unsigned long long c = lane < T ? buf[nt + (0xFFFFu - (s & 0xFFFFu))] : 0ull;
-  uint32_t lo = 0, hi = nt;  // list entries with key >= ck
-  while (lo < hi) {
-    const uint32_t mid = (lo + hi) >> 1;
-    if (key_hi[2 * mid] >= ck) lo = mid + 1; else hi = mid;
-  }
-  const uint32_t cpos = lane + lo;
-  keys[lane] = ck;
-  __syncwarp();
-  unsigned long long tv[SLOTS];
-  uint32_t tpos[SLOTS];
-#pragma unroll
-  for (int m = 0; m < SLOTS; ++m) {
-    const uint32_t j = lane + 32u * m;
-    tv[m] = 0ull;
-    tpos[m] = K;
-    if (j < nt) {
-      tv[m] = buf[j];
-      const uint32_t tk = uint32_t(tv[m] >> 32);
-      uint32_t a = 0, b = T;  // candidates with a key above tk
-      while (a < b) {
-        const uint32_t mid = (a + b) >> 1;
-        if (keys[mid] > tk) a = mid + 1; else b = mid;
-      }
-      tpos[m] = j + a;
-    }
-  }
-  __syncwarp();
-  if (lane < T && cpos < K) buf[cpos] = c;
-#pragma unroll
-  for (int m = 0; m < SLOTS; ++m)
-    if (tpos[m] < K) buf[tpos[m]] = tv[m];
-  __syncwarp();
-  return nt + T < K ? nt + T : K;
-}
-
-// Warp: filter the nb (<= BATCH) oldest queued vectors, one per lane, and merge what
-// passes into the top list.  For values other than NaN, key(x) > wth exactly when
-// x > value(wth) (-0 and +0 have one key), and the same for >=, so the test is a float
-// compare; a vector holding a NaN, or a threshold key that is a NaN pattern, takes the
-// key path.  Once the list holds K entries its last key is the threshold (later
-// elements need a larger key: an equal key comes with a larger column).  Out of line:
-// it runs once per BATCH queued vectors, and one copy of it keeps the streaming loop
-// small in the instruction cache.
-template <class C>
-__device__ __noinline__ WarpSel warp_drain(TopkWarpSmem<C::CAP>& ws, WarpSel st, uint32_t nb, uint32_t V32,
-                                           uint32_t K) {
-  const uint32_t lane = lane_id();
-  uint32_t take = 0, col0 = 0;
-  unsigned long long lo = 0, hi = 0;
-  if (lane < nb) {
-    const uint32_t q = (st.qh + lane) & (TW_QUEUE - 1);
-    const uint4 v = ws.qv[q];
-    col0 = ws.qcol[q];
-    lo = (static_cast<unsigned long long>(v.y) << 32) | v.x;
-    hi = (static_cast<unsigned long long>(v.w) << 32) | v.z;
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    const float t = key_to_float(st.wth);
-    if (st.ge && st.wth == 0) {
-      take = 0xFFu;  // every element
-    } else if (vec_max(v) == vec_max(v) && t == t) {
-#pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        const float a = __uint_as_float(w[h] << 16), b = __uint_as_float(w[h] & 0xFFFF0000u);
-        if (st.ge ? a >= t : a > t) take |= 1u << (2 * h);
-        if (st.ge ? b >= t : b > t) take |= 2u << (2 * h);
-      }
-    } else {
-#pragma unroll
-      for (int e = 0; e < TK_VEC; ++e) {
-        const uint32_t key = bf16_key(w[e >> 1] >> (16 * (e & 1)));
-        if (st.ge ? key >= st.wth : key > st.wth) take |= 1u << e;
-      }
-    }
-    if (col0 + TK_VEC > V32) take &= (V32 > col0 ? (1u << (V32 - col0)) - 1u : 0u);
-  }
-  // exclusive prefix of the per-lane counts (<= 8: four bits) and the warp total
-  const uint32_t c = __popc(take);
-  const uint32_t lt = (1u << lane) - 1u;
-  uint32_t pre = 0, tot = 0;
-#pragma unroll
-  for (int b = 0; b < 4; ++b) {
-    const uint32_t bb = __ballot_sync(0xffffffffu, (c >> b) & 1u);
-    pre += uint32_t(__popc(bb & lt)) << b;
-    tot += uint32_t(__popc(bb)) << b;
-  }
-  uint32_t pos = st.cnt + pre;  // after the top list
-  while (take) {
-    const uint32_t e = __ffs(take) - 1;
-    take &= take - 1;
-    const uint32_t bits = uint32_t(((e & 4) ? hi : lo) >> (16 * (e & 3))) & 0xFFFFu;
-    if (KD_DCHECK(pos < uint32_t(C::CAP), ws.err, 0x7101))
-      ws.buf[pos] = (static_cast<unsigned long long>(bf16_key(bits)) << 32) | uint32_t(~(col0 + e));
-    ++pos;
-  }
-  st.qh = (st.qh + nb) & (TW_QUEUE - 1);
-  st.nq -= nb;
-  __syncwarp();
-  if (tot == 0) return st;
-  if (!KD_DCHECK(st.cnt + tot <= uint32_t(C::CAP), ws.err, 0x7102)) return st;
-  if (tot <= 32) {
-    st.cnt = warp_merge_top<C::MAXK / 32>(ws.buf, ws.hist, st.cnt, tot, K);
-  } else {  // a large batch: select and sort the whole list
-    uint32_t cnt = st.cnt + tot;
-    if (cnt > K) {
-      uint32_t cge = 0;
-      const uint32_t T = warp_kth_largest(ws.buf, cnt, K, ws.hist, cge);
-      if (cge < cnt) cnt = warp_filter_ge(ws.buf, cnt, T);
-    }
-    warp_sort_desc(ws.buf, cnt);
-    st.cnt = cnt < K ? cnt : K;
-  }
-  if (st.cnt >= K) {
-    st.wth = comp_key(ws.buf[K - 1]);
-    st.ge = false;
-    st.tv = key_to_float(st.wth);
-  }
-  return st;
-}
-
-// Warp: the top list (sorted; K entries whenever V >= K) to the row's outputs; values
-// are read back from the row (exact bits, -0 kept).
-__device__ __noinline__ void warp_finish(const unsigned long long* top, uint32_t cnt, uint32_t K, const uint16_t* xr,
-                                         uint32_t V32, uint32_t* err, int32_t* ids_row, float* vals_row) {
-  (void)V32;
-  (void)err;
-  for (uint32_t j = lane_id(); j < K; j += 32) {
-    if (j < cnt) {
-      const uint32_t col = ~uint32_t(top[j]);
-      ids_row[j] = int32_t(col);
-      if (KD_DCHECK(col < V32, err, 0x7301)) vals_row[j] = __uint_as_float(uint32_t(xr[col]) << 16);
-    } else {
-      ids_row[j] = -1;
-      vals_row[j] = -INFINITY;
-    }
-  }
-}
-
 // Sum over the 8 values x of v of 2^(x log2 e - b), b = lm log2 e: each word's pair of
 // values goes through one packed f32x2 multiply-add and one packed add.
 __device__ __forceinline__ float lse_terms(const uint4& v, float b) {
@@ -871,83 +689,6 @@ __device__ __forceinline__ float lse_terms(const uint4& v, float b) {
   asm("mov.b64 {%0, %1}, %2;" : "=r"(a0), "=r"(a1) : "l"(acc));
   return __uint_as_float(a0) + __uint_as_float(a1);
 }
-
-// One group of TW_GROUP steps of a lane, vectors v[0 ..]: the packed pre-test of each
-// against the warp's threshold (st.tv is NaN while every element is a candidate), one
-// vote for the group, and, when a vector passed, its queueing and a drain every BATCH
-// queued.  s0 = the group's first step; `live` = the group's steps that exist.
-template <class C, bool WITH_LSE>
-__device__ __forceinline__ void test_group(TopkWarpSmem<C::CAP>& ws, WarpSel& st, const uint4* v, int s0,
-                                           uint32_t live, float& lm, float& ls, uint32_t V32, uint32_t K) {
-  const uint32_t lane = lane_id();
-  float vm[TW_GROUP];
-  uint32_t pass = 0;
-#pragma unroll
-  for (int k = 0; k < TW_GROUP; ++k) {
-    vm[k] = vec_max(v[k]);
-    if (((live >> k) & 1u) && !(vm[k] <= st.tv)) pass |= 1u << k;
-  }
-  if (WITH_LSE) {
-    float gm = -INFINITY;
-#pragma unroll
-    for (int k = 0; k < TW_GROUP; ++k)
-      if ((live >> k) & 1u) gm = fmaxf(gm, vm[k]);
-    if (gm > lm) {
-      ls *= ex2_approx((lm - gm) * TW_LOG2E);
-      lm = gm;
-    }
-    if (lm != -INFINITY) {
-      const float b = lm * TW_LOG2E;
-#pragma unroll
-      for (int k = 0; k < TW_GROUP; ++k)
-        if ((live >> k) & 1u) ls += lse_terms(v[k], b);
-    }
-  }
-  if (__any_sync(0xffffffffu, pass != 0)) {
-#pragma unroll
-    for (int k = 0; k < TW_GROUP; ++k) {
-      const bool p = (pass >> k) & 1u;
-      const uint32_t bal = __ballot_sync(0xffffffffu, p);
-      if (bal != 0) {
-        if (p) {
-          const uint32_t q = (st.qh + st.nq + __popc(bal & ((1u << lane) - 1u))) & (TW_QUEUE - 1);
-          ws.qv[q] = v[k];
-          ws.qcol[q] = uint32_t(s0 + k) * TW_STEP + lane * TK_VEC;
-        }
-        st.nq += __popc(bal);  // < BATCH + 32 <= TW_QUEUE
-        if (st.nq >= uint32_t(C::BATCH)) {
-          __syncwarp();
-          do {
-            st = warp_drain<C>(ws, st, C::BATCH, V32, K);
-          } while (st.nq >= uint32_t(C::BATCH));
-        }
-      }
-    }
-  }
-}
-
-// Ring feeding: (RING - 1) x GRP x 512 bytes per warp stay in flight whatever the
-// register schedule.  A row's last group copies whole 16-byte vectors only; the one lane
-// whose vector straddles the end of the row (and the lanes past it) read theirs directly.
-
-template <int CAP_, int WARPS_, int BATCH_, int MAXK_, int RING_, int GRP_>
-struct TmaCfg : TwCfg<CAP_, WARPS_, BATCH_, MAXK_> {
-  static constexpr int RING = RING_;
-  static constexpr int GRP = GRP_;
-  static_assert(GRP == TW_GROUP, "a slot is one tested group");
-  static_assert((RING & (RING - 1)) == 0, "slots wrap with a mask");
-};
-using TmSmallK = TmaCfg<512, 15, 24, 128, 4, 4>;   // K <= 128
-using TmLargeK = TmaCfg<1024, 12, 32, 256, 4, 4>;  // K <= 256
-
-template <class C>
-struct TopkTmaSmem {
-  uint4 ring[C::RING][C::GRP][32];
-  TopkWarpSmem<C::CAP> sel;
-  uint64_t full[C::RING];
-  uint32_t abort;  // set by a timed-out wait
-  uint32_t never;  // stays 0: the flag of the bounded waits after an abort
-};
 
 // Bulk copy global -> shared of `bytes` (a multiple of 16), completing on `bar`.
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
@@ -974,57 +715,359 @@ __device__ __forceinline__ void load_group(uint4* v, const uint16_t* xr, int64_t
   }
 }
 
-// Warp: the whole selection of one row again, read directly from global memory (the next
-// group's loads in flight while a group is tested), every element a candidate until the
-// list holds K.  Out of line: it runs only after a guessed threshold turned out too high.
+// A candidate of the warp path as one 64-bit word that orders like the element's rank:
+// key (16 bits) | ~column (32) | the bf16 bits (16), so the value, -0 and NaN payloads
+// included, travels with it.
+__device__ __forceinline__ unsigned long long cand_make(uint32_t bits, uint32_t col) {
+  return (static_cast<unsigned long long>(bf16_key(bits)) << 48) | (static_cast<unsigned long long>(~col) << 16) |
+         (bits & 0xFFFFu);
+}
+__device__ __forceinline__ uint32_t cand_key(unsigned long long c) { return uint32_t(c >> 48); }
+__device__ __forceinline__ uint32_t cand_col(unsigned long long c) { return ~uint32_t(c >> 16); }
+__device__ __forceinline__ uint32_t cand_bits(unsigned long long c) { return uint32_t(c) & 0xFFFFu; }
+
+// Warp: for each of R ranks r, the largest key T_r that at least r of the warp's keys reach
+// (the r-th largest key), and how many reach it.  Each lane holds E keys, kp[i] = key + 1
+// (0: no key).  Bisection over [0, 2^16) on the warp's counts; rank must not exceed the
+// number of keys.
+template <int E, int R>
+__device__ __forceinline__ void warp_rank_keys(const uint32_t (&kp)[E], const uint32_t (&rank)[R], uint32_t (&T)[R],
+                                               uint32_t (&count_ge)[R]) {
+  uint32_t n = 0;
+#pragma unroll
+  for (int i = 0; i < E; ++i) n += kp[i] != 0u ? 1u : 0u;
+  n = __reduce_add_sync(0xffffffffu, n);
+  uint32_t lo[R], hi[R], clo[R];
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    lo[r] = 1u;          // keys + 1 >= lo: all n of them
+    hi[r] = 0x10001u;    // none
+    clo[r] = n;
+  }
+#pragma unroll 1
+  for (int it = 0; it < 17; ++it) {
+    uint32_t mid[R], c[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      mid[r] = (lo[r] + hi[r]) >> 1;
+      c[r] = 0;
+    }
+#pragma unroll
+    for (int i = 0; i < E; ++i)
+#pragma unroll
+      for (int r = 0; r < R; ++r) c[r] += kp[i] >= mid[r] ? 1u : 0u;
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      c[r] = __reduce_add_sync(0xffffffffu, c[r]);
+      if (hi[r] - lo[r] > 1u) {
+        if (c[r] >= rank[r]) {
+          lo[r] = mid[r];
+          clo[r] = c[r];
+        } else {
+          hi[r] = mid[r];
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    T[r] = lo[r] - 1u;
+    count_ge[r] = clo[r];
+  }
+}
+
+// Warp: the K-th largest key of the buffer's cnt entries (K <= cnt <= CAP = 512: 16 per lane)
+// and how many entries reach it.
+__device__ __forceinline__ uint32_t buf_rank_key(const unsigned long long* buf, uint32_t cnt, uint32_t K,
+                                                 uint32_t& count_ge) {
+  const uint32_t lane = lane_id();
+  uint32_t kp[16];
+  const uint32_t* hw = reinterpret_cast<const uint32_t*>(buf) + 1;  // high word of buf[i] at [2 i]
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const uint32_t j = lane + 32u * i;
+    kp[i] = j < cnt ? (hw[2 * j] >> 16) + 1u : 0u;
+  }
+  const uint32_t rank[1] = {K};
+  uint32_t T[1], cge[1];
+  warp_rank_keys<16, 1>(kp, rank, T, cge);
+  count_ge = cge[0];
+  return T[0];
+}
+
+// Warp: keep the entries of buf[0, cnt) whose key reaches T, in place (each round of 256 is
+// read before any survivor of it is written); returns the new count.
+__device__ uint32_t buf_filter_ge(unsigned long long* buf, uint32_t cnt, uint32_t T) {
+  const uint32_t lane = lane_id();
+  uint32_t out = 0;
+  for (uint32_t base = 0; base < cnt; base += 256) {
+    unsigned long long held[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const uint32_t i = base + lane + 32u * j;
+      held[j] = i < cnt ? buf[i] : 0ull;
+    }
+    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const uint32_t i = base + lane + 32u * j;
+      const bool take = i < cnt && cand_key(held[j]) >= T;
+      const uint32_t bal = __ballot_sync(0xffffffffu, take);
+      if (take) buf[out + __popc(bal & ((1u << lane) - 1u))] = held[j];
+      out += __popc(bal);
+    }
+    __syncwarp();
+  }
+  return out;
+}
+
+// Largest of the 8 bf16 of v, as a packed pair: each half the maximum of four (NaN if one is NaN).
+__device__ __forceinline__ uint32_t vec_max2(const uint4& v) { return bmax2(bmax2(v.x, v.y), bmax2(v.z, v.w)); }
+
+// Some half of the packed bf16 pair m is > (ge: >=) the packed threshold t2, or is NaN.
+__device__ __forceinline__ bool half_passes(uint32_t m, uint32_t t2, bool ge) {
+  uint32_t r;
+  if (ge)
+    asm("{\n\t.reg .pred p, q;\n\tsetp.geu.bf16x2 p|q, %1, %2;\n\tor.pred p, p, q;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r)
+        : "r"(m), "r"(t2));
+  else
+    asm("{\n\t.reg .pred p, q;\n\tsetp.gtu.bf16x2 p|q, %1, %2;\n\tor.pred p, p, q;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r)
+        : "r"(m), "r"(t2));
+  return r != 0;
+}
+
+// bf16 bits of the value whose key is `key`, twice (a packed threshold for half_passes).
+// Key 0 (below every element) gives a NaN pattern, which every compare passes.
+__device__ __forceinline__ uint32_t key_pair(uint32_t key) {
+  const uint32_t b = (key & 0x8000u) ? (key & 0x7FFFu) : (~key & 0xFFFFu);
+  return b | (b << 16);
+}
+
+// Per-warp selection state (warp-uniform).
+struct Sel {
+  uint32_t cnt;   // entries in buf
+  uint32_t thr;   // threshold key
+  uint32_t thr2;  // key_pair(thr)
+  bool ge;        // a candidate needs key >= thr (until K entries are known to reach a key), else key > thr
+};
+
+__device__ __forceinline__ void sel_set(Sel& st, uint32_t key, bool ge) {
+  st.thr = key;
+  st.thr2 = key_pair(key);
+  st.ge = ge;
+}
+
+// Bits e of the elements of v that pass the threshold exactly.  For values other than NaN,
+// key(x) > thr exactly when x > value(thr) (-0 and +0 have one key), and the same for >=, so
+// the test is a float compare; a vector holding a NaN, or a NaN threshold, takes the key path.
+__device__ __forceinline__ uint32_t elem_mask(const uint4& v, const Sel& st) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t take = 0;
+  uint32_t m = vec_max2(v);
+  m = bmax2(m, __byte_perm(m, 0u, 0x1032));
+  const float mx = __uint_as_float(m & 0xFFFF0000u);
+  const float t = key_to_float(st.thr);
+  if (mx == mx && t == t) {
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      const float a = __uint_as_float(w[h] << 16), b = __uint_as_float(w[h] & 0xFFFF0000u);
+      if (st.ge ? a >= t : a > t) take |= 1u << (2 * h);
+      if (st.ge ? b >= t : b > t) take |= 2u << (2 * h);
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < TK_VEC; ++e) {
+      const uint32_t key = bf16_key(w[e >> 1] >> (16 * (e & 1)));
+      if (st.ge ? key >= st.thr : key > st.thr) take |= 1u << e;
+    }
+  }
+  return take;
+}
+
+// Warp: the K-th largest key T of the buffer (cnt >= K) becomes the threshold.  With
+// `strict` (every element queued so far is in the buffer), a later element needs key > T:
+// an equal key comes with a larger column and ranks below those K.  Part-way through a
+// drain, queue slots still to come may hold elements of earlier columns than some in the
+// buffer, so an element with key T may still outrank one of those K: key >= T.  With
+// `cut`, the buffer is also filtered to the entries that reach T, and cut to its best K
+// (an element it drops has K entries above it) when ties leave less than a slot's room.
 template <class C>
-__device__ __noinline__ WarpSel warp_reselect(TopkWarpSmem<C::CAP>& ws, const uint16_t* xr, int64_t V, int nst,
-                                              uint32_t V32, uint32_t K) {
-  WarpSel st;
+__device__ __noinline__ Sel tw_raise(TwSmem<C>& ws, Sel st, uint32_t K, bool cut, bool strict) {
+  uint32_t cge = 0;
+  const uint32_t T = buf_rank_key(ws.buf, st.cnt, K, cge);
+  if (cut && cge < st.cnt) st.cnt = buf_filter_ge(ws.buf, st.cnt, T);
+  if (cut && st.cnt > uint32_t(C::CAP - TW_STEP)) {
+    warp_sort_desc(ws.buf, st.cnt);
+    st.cnt = K;
+  }
+  sel_set(st, T, !strict);
+  return st;
+}
+
+// Warp: move every lane's queued vectors (nq of them in this lane) into the candidate
+// buffer, one queue slot at a time, keeping the elements that pass the threshold exactly;
+// then raise the threshold once the buffer holds K entries.  The selection state goes in
+// and out by value (out of line, a reference would keep it in local memory).
+template <class C>
+__device__ __noinline__ Sel tw_drain(TwSmem<C>& ws, Sel st, uint32_t nq, uint32_t V32, uint32_t K) {
+  const uint32_t lane = lane_id();
+  const uint32_t slots = __reduce_max_sync(0xffffffffu, nq);
+  for (uint32_t j = 0; j < slots; ++j) {
+    if (st.cnt + TW_STEP > uint32_t(C::CAP)) st = tw_raise(ws, st, K, true, false);  // room for a slot's elements
+    uint32_t take = 0, col0 = 0;
+    unsigned long long lo = 0, hi = 0;
+    if (j < nq && KD_DCHECK(j < uint32_t(C::QL), ws.err, 0x7102)) {
+      const uint4 v = ws.qv[j][lane];
+      col0 = ws.qcol[j][lane];
+      lo = (static_cast<unsigned long long>(v.y) << 32) | v.x;
+      hi = (static_cast<unsigned long long>(v.w) << 32) | v.z;
+      take = elem_mask(v, st);
+      if (col0 + TK_VEC > V32) take &= (V32 > col0 ? (1u << (V32 - col0)) - 1u : 0u);
+    }
+    // exclusive prefix of the per-lane counts (<= 8: four bits) and the warp total
+    const uint32_t c = __popc(take);
+    const uint32_t lt = (1u << lane) - 1u;
+    uint32_t pre = 0, tot = 0;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const uint32_t bb = __ballot_sync(0xffffffffu, (c >> b) & 1u);
+      pre += uint32_t(__popc(bb & lt)) << b;
+      tot += uint32_t(__popc(bb)) << b;
+    }
+    uint32_t pos = st.cnt + pre;
+    while (take) {
+      const uint32_t e = __ffs(take) - 1;
+      take &= take - 1;
+      const uint32_t bits = uint32_t(((e & 4) ? hi : lo) >> (16 * (e & 3))) & 0xFFFFu;
+      if (KD_DCHECK(pos < uint32_t(C::CAP), ws.err, 0x7101)) ws.buf[pos] = cand_make(bits, col0 + e);
+      ++pos;
+    }
+    st.cnt += tot;
+    __syncwarp();
+  }
+  if (st.cnt >= K) st = tw_raise(ws, st, K, st.cnt > uint32_t(C::CAP / 2), true);
+  return st;
+}
+
+// One group of TW_GROUP steps of a lane, vectors v[0 ..]: the packed pre-test of each against
+// the threshold; the vectors that pass go to the lane's queue (predicated stores), and the
+// warp drains the queues when one of them has less than a group's room left.  s0 = the
+// group's first step; `live` = its steps that exist (the row's last group may have fewer).
+template <class C, bool WITH_LSE>
+__device__ __forceinline__ void tw_group(TwSmem<C>& ws, Sel& st, uint32_t& nq, const uint4* v, int s0,
+                                         uint32_t live, float& lm, float& ls, uint32_t V32, uint32_t K) {
+  const uint32_t lane = lane_id();
+  uint32_t m[TW_GROUP];
+#pragma unroll
+  for (int k = 0; k < TW_GROUP; ++k) m[k] = ((live >> k) & 1u) ? vec_max2(v[k]) : 0xFF80FF80u;  // -inf pair
+  if (WITH_LSE) {
+    uint32_t g = bmax2(bmax2(m[0], m[1]), bmax2(m[2], m[3]));
+    g = bmax2(g, __byte_perm(g, 0u, 0x1032));
+    const float gm = __uint_as_float(g & 0xFFFF0000u);
+    if (gm > lm) {
+      ls *= ex2_approx((lm - gm) * TW_LOG2E);
+      lm = gm;
+    }
+    if (lm != -INFINITY) {
+      const float b = lm * TW_LOG2E;
+#pragma unroll
+      for (int k = 0; k < TW_GROUP; ++k)
+        if ((live >> k) & 1u) ls += lse_terms(v[k], b);
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < TW_GROUP; ++k) {
+    if (half_passes(m[k], st.thr2, st.ge) && KD_DCHECK(nq < uint32_t(C::QL), ws.err, 0x7103)) {
+      ws.qv[nq][lane] = v[k];
+      ws.qcol[nq][lane] = uint32_t(s0 + k) * TW_STEP + lane * TK_VEC;
+      ++nq;
+    }
+  }
+  if (__any_sync(0xffffffffu, nq > uint32_t(C::QL - TW_GROUP))) {
+    __syncwarp();
+    st = tw_drain(ws, st, nq, V32, K);
+    nq = 0;
+  }
+}
+
+// Warp: hand the row's best candidates over (cnt >= K entries in the buffer): those whose
+// key reaches the K-th largest key (K of them, more on ties, cut to the best K when ties
+// make more than TW_HAND), written to hand[0 ..], their count to *hand_cnt.
+template <class C>
+__device__ __noinline__ void tw_hand_over(TwSmem<C>& ws, Sel st, uint32_t K, unsigned long long* hand,
+                                         uint32_t* hand_cnt) {
+  const uint32_t lane = lane_id();
+  uint32_t cge = st.cnt;
+  uint32_t T = 0;
+  if (st.cnt > K) T = buf_rank_key(ws.buf, st.cnt, K, cge);
+  if (cge > uint32_t(TW_HAND)) {  // ties at T: order the buffer and keep exactly the best K
+    warp_sort_desc(ws.buf, st.cnt);
+    for (uint32_t i = lane; i < K; i += 32) hand[i] = ws.buf[i];
+    if (lane == 0) *hand_cnt = K;
+    __syncwarp();
+    return;
+  }
+  uint32_t out = 0;
+  for (uint32_t base = 0; base < st.cnt; base += 32) {
+    const uint32_t i = base + lane;
+    const unsigned long long c = i < st.cnt ? ws.buf[i] : 0ull;
+    const bool take = i < st.cnt && cand_key(c) >= T;
+    const uint32_t bal = __ballot_sync(0xffffffffu, take);
+    const uint32_t at = out + __popc(bal & ((1u << lane) - 1u));
+    if (take && KD_DCHECK(at < uint32_t(TW_HAND), ws.err, 0x7104)) hand[at] = c;
+    out += __popc(bal);
+  }
+  if (lane == 0) *hand_cnt = out;
+  __syncwarp();
+}
+
+// Warp: the selection of one row again, read directly from global memory (the next group's
+// loads in flight while a group is tested), from the exact start T0.  Out of line: it runs
+// only after a speculative start left fewer than K elements.
+template <class C>
+__device__ __noinline__ Sel tw_reselect(TwSmem<C>& ws, const uint16_t* xr, int64_t V, int nst, uint32_t T0,
+                                        uint32_t V32, uint32_t K) {
+  Sel st;
   st.cnt = 0;
-  st.qh = 0;
-  st.nq = 0;
-  st.wth = 0;
-  st.ge = true;
-  st.tv = key_to_float(0);
-  float lm = -INFINITY, ls = 0.f;  // unused: no logsumexp here
+  sel_set(st, T0, true);
+  uint32_t nq = 0;
+  float lm = -INFINITY, ls = 0.f;  // unused: the logsumexp pass is already complete
   uint4 a[TW_GROUP], b[TW_GROUP];
   load_group(a, xr, V, 0);
   for (int s0 = 0; s0 < nst; s0 += TW_GROUP) {
     if (s0 + TW_GROUP < nst) load_group(b, xr, V, s0 + TW_GROUP);
     const uint32_t live = nst - s0 >= TW_GROUP ? (1u << TW_GROUP) - 1u : (1u << (nst - s0)) - 1u;
-    test_group<C, false>(ws, st, a, s0, live, lm, ls, V32, K);
+    tw_group<C, false>(ws, st, nq, a, s0, live, lm, ls, V32, K);
 #pragma unroll
     for (int k = 0; k < TW_GROUP; ++k) a[k] = b[k];
   }
-  __syncwarp();
-  while (st.nq > 0) st = warp_drain<C>(ws, st, min(st.nq, uint32_t(C::BATCH)), V32, K);
+  if (__any_sync(0xffffffffu, nq > 0)) st = tw_drain(ws, st, nq, V32, K);
   return st;
 }
 
 template <class C, bool WITH_LSE>
 __global__ void __launch_bounds__(C::WARPS * 32, 1)
-    kd_topk_tma_kernel(const uint16_t* __restrict__ X, int64_t N, int64_t V, int64_t ld, int K,
-                       int32_t* __restrict__ ids_out, float* __restrict__ vals_out, float* __restrict__ lse_out,
-                       uint32_t* err, int guesses, const uint32_t* guess_in, uint32_t* guess_out,
-                       const uint16_t* __restrict__ tile_max, int64_t ld_tile_max, int ntiles) {
+    kd_topk_stream_kernel(const uint16_t* __restrict__ X, int64_t N, int64_t V, int64_t ld, int K,
+                          unsigned long long* __restrict__ hand, uint32_t* __restrict__ hand_cnt,
+                          float* __restrict__ lse_out, uint32_t* err, const uint16_t* __restrict__ tile_max,
+                          int64_t ld_tile_max, int ntiles) {
   extern __shared__ __align__(16) uint8_t tkt_smem_raw[];
-  constexpr int GSTEPS = C::GRP;
-  constexpr uint32_t GBYTES = uint32_t(C::GRP) * TW_STEP * 2;
+  constexpr uint32_t GBYTES = uint32_t(TW_GROUP) * TW_STEP * 2;
   const uint32_t lane = lane_id();
-  TopkTmaSmem<C>& ts = reinterpret_cast<TopkTmaSmem<C>*>(tkt_smem_raw)[threadIdx.x >> 5];
-  TopkWarpSmem<C::CAP>& ws = ts.sel;
+  TwSmem<C>& ws = reinterpret_cast<TwSmem<C>*>(tkt_smem_raw)[threadIdx.x >> 5];
   const int64_t nwarps = int64_t(gridDim.x) * C::WARPS;
   const int nst = int((V + TW_STEP - 1) / TW_STEP);
-  const int ngr = (nst + GSTEPS - 1) / GSTEPS;  // groups per row
+  const int ngr = (nst + TW_GROUP - 1) / TW_GROUP;  // groups per row
   const uint32_t V32 = uint32_t(V), Ku = uint32_t(K);
   // this lane's vector in a row's last step is not a whole 16 bytes inside the row
   const bool tail_lane = int64_t(nst - 1) * TW_STEP + int64_t(lane) * TK_VEC + TK_VEC > V;
 
   if (lane == 0) {
-    for (int r = 0; r < C::RING; ++r) mbar_init(&ts.full[r], 1);
-    ts.abort = 0;
-    ts.never = 0;
+    for (int r = 0; r < C::RING; ++r) mbar_init(&ws.full[r], 1);
+    ws.abort = 0;
+    ws.never = 0;
     ws.err = err;
     fence_mbar_init();
   }
@@ -1038,12 +1081,12 @@ __global__ void __launch_bounds__(C::WARPS * 32, 1)
   auto issue = [&](uint32_t slot) {
     if (prow < N) {
       if (lane == 0) {
-        const int64_t e0 = int64_t(pg) * GSTEPS * TW_STEP;
+        const int64_t e0 = int64_t(pg) * TW_GROUP * TW_STEP;
         const int64_t left = V - e0;
-        uint32_t bytes = left >= int64_t(GSTEPS) * TW_STEP ? GBYTES : uint32_t(left * 2) & ~15u;
+        uint32_t bytes = left >= int64_t(TW_GROUP) * TW_STEP ? GBYTES : uint32_t(left * 2) & ~15u;
         if (!KD_DCHECK(e0 >= 0 && e0 + bytes / 2 <= V && bytes <= GBYTES, err, 0x7401)) bytes = 0;
-        mbar_arrive_expect_tx(&ts.full[slot], bytes);  // 0 bytes: the phase completes on the arrival
-        if (bytes != 0) bulk_g2s(&ts.ring[slot][0][0], X + prow * ld + e0, bytes, &ts.full[slot]);
+        mbar_arrive_expect_tx(&ws.full[slot], bytes);  // 0 bytes: the phase completes on the arrival
+        if (bytes != 0) bulk_g2s(&ws.ring[slot][0][0], X + prow * ld + e0, bytes, &ws.full[slot]);
       }
       ++issued;
       if (++pg == ngr) {
@@ -1056,94 +1099,85 @@ __global__ void __launch_bounds__(C::WARPS * 32, 1)
 
   uint32_t gidx = 0;  // groups consumed
   bool ok = true;
-  // Guessed threshold for the warp's next row (0: none) and the margin factor behind it.
-  const int64_t gw = int64_t(blockIdx.x) * C::WARPS + (threadIdx.x >> 5);  // this warp's guess word
-  const bool may_guess = guesses != 0 && K >= 16;
-  uint32_t guess = (may_guess && guess_in && gw < KD_TOPK_MAX_WARPS) ? guess_in[gw] : 0u;
-  float margin = TW_GUESS_MARGIN;
+  bool may_speculate = K >= TW_SPEC_MIN_K;
   for (; row < N; row += nwarps) {
     const uint16_t* xr = X + row * ld;
-    WarpSel st;
+    Sel st;
     st.cnt = 0;
-    st.qh = 0;
-    st.nq = 0;
-    st.wth = 0;
-    st.ge = true;
-    st.tv = key_to_float(0);
+    sel_set(st, 0u, true);  // key >= 0: every element, until a start applies
+    uint32_t nq = 0;
     float lm = -INFINITY, ls = 0.f;
+    uint32_t T0 = 0;        // exact start (0: none)
+    bool speculative = false;
 
-    // Tile start (maxima of ntiles >= K disjoint column ranges of every row given, as the
-    // teacher projection emits them): their K-th largest is reached by at least K elements,
-    // so every element of the top K has a key >= it, an exact first threshold.
-    // Guessed start (when enabled: every row after a warp's first, K >= 16): the threshold
-    // is a key taken from the previous row's best K (below).  If at least K elements reach it, the top K
-    // all do and the row is selected exactly; if not, the list ends short of K and the row
-    // is selected again from its start with no threshold.
-    // Quick start (otherwise): the ring holds this row's first RING groups (none of them the
-    // row's last).  The K-th largest of their per-lane vector maxima is reached by at least
-    // K elements, so every element of the top K has a key >= it: those groups are then
-    // consumed with that threshold (>=), and the rest of the row with the raised ones.
     const bool tiles = tile_max != nullptr && ntiles >= K;
-    const bool guessed = !tiles && guess != 0u;
     if (tiles) {
+      // The K-th largest of the row's tile maxima (ntiles >= K disjoint column ranges) is
+      // reached by at least K elements: an exact start near the row's K-th value.
       const uint32_t T = warp_kth_largest_bf16(tile_max + row * ld_tile_max, uint32_t(ntiles), Ku, ws.hist);
-      if (T != 0) {
-        st.wth = T;
-        st.tv = key_to_float(T - 1u == 0x7FFFu ? 0x7FFEu : T - 1u);
-      }
-    } else if (guessed) {
-      st.wth = guess;
-      st.tv = key_to_float(guess - 1u == 0x7FFFu ? 0x7FFEu : guess - 1u);
-    } else if (ngr > C::RING && K <= C::RING * C::GRP * 32) {
+      if (T != 0) sel_set(st, T, true);
+    } else if (ngr > C::RING) {
+      // The ring holds this row's first RING groups (none of them the row's last).
       for (int r = 0; r < C::RING && ok; ++r) {
         const uint32_t u = gidx + uint32_t(r);
-        ok = mbar_wait(&ts.full[u & (C::RING - 1)], (u / C::RING) & 1u, &ts.abort, err, 0x72u);
+        ok = mbar_wait(&ws.full[u & (C::RING - 1)], (u / C::RING) & 1u, &ws.abort, err, 0x72u);
       }
       if (!ok) break;
+      uint32_t kp[C::RING * TW_GROUP];  // the lane's vector maxima keys + 1
 #pragma unroll
       for (int r = 0; r < C::RING; ++r) {
 #pragma unroll
-        for (int k = 0; k < C::GRP; ++k) {
-          const uint4 v = ts.ring[(gidx + r) & (C::RING - 1)][k][lane];
-          const float m = vec_max(v);
+        for (int k = 0; k < TW_GROUP; ++k) {
+          const uint4 v = ws.ring[(gidx + r) & (C::RING - 1)][k][lane];
+          const float mx = vec_max(v);
           uint32_t key;
-          if (m == m) {
-            key = bf16_key(__float_as_uint(m) >> 16);
+          if (mx == mx) {
+            key = bf16_key(__float_as_uint(mx) >> 16);
           } else {  // a NaN hides the maximum: take the exact keys
             key = 0;
             const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
             for (int h = 0; h < 4; ++h) key = max(key, max(bf16_key(w[h]), bf16_key(w[h] >> 16)));
           }
-          ws.buf[(r * C::GRP + k) * 32 + lane] = static_cast<unsigned long long>(key) << 32;
+          kp[r * TW_GROUP + k] = key + 1u;
         }
       }
-      __syncwarp();
-      uint32_t cge = 0;
-      const uint32_t T0 = warp_kth_largest(ws.buf, uint32_t(C::RING * C::GRP * 32), Ku, ws.hist, cge);
-      if (T0 != 0) {
-        st.wth = T0;
-        // pre-test bound just below value(T0) (the -0/+0 key is 0x8000: step past -0)
-        st.tv = key_to_float(T0 - 1u == 0x7FFFu ? 0x7FFEu : T0 - 1u);
+      const uint32_t rank[2] = {Ku, Ku / 4 > 0 ? Ku / 4 : 1u};
+      uint32_t T[2], cge[2];
+      warp_rank_keys<C::RING * TW_GROUP, 2>(kp, rank, T, cge);
+      T0 = T[0];
+      uint32_t start = T0;
+      if (may_speculate) {
+        const uint32_t T1 = T[1];
+        const bool finite = T0 > 0x007Fu && T1 < 0xFF80u;  // both keys of finite values
+        if (finite && T1 > T0) {
+          const float v0 = key_to_float(T0), v1 = key_to_float(T1);
+          const uint32_t Ts = key_floor(fmaf(TW_SPEC_C, v1 - v0, v0));
+          if (Ts > T0) {
+            start = Ts;
+            speculative = true;
+          }
+        }
       }
+      if (start != 0) sel_set(st, start, true);
     }
 
     for (int g = 0; g < ngr; ++g, ++gidx) {
       const uint32_t slot = gidx & (C::RING - 1);
-      if (!mbar_wait(&ts.full[slot], (gidx / C::RING) & 1u, &ts.abort, err, 0x70u)) {
+      if (!mbar_wait(&ws.full[slot], (gidx / C::RING) & 1u, &ws.abort, err, 0x70u)) {
         ok = false;
         break;
       }
-      uint4 v[GSTEPS];
+      uint4 v[TW_GROUP];
 #pragma unroll
-      for (int k = 0; k < GSTEPS; ++k) v[k] = ts.ring[slot][k][lane];
-      const int s0 = g * GSTEPS;
-      uint32_t live = (1u << GSTEPS) - 1u;
+      for (int k = 0; k < TW_GROUP; ++k) v[k] = ws.ring[slot][k][lane];
+      const int s0 = g * TW_GROUP;
+      uint32_t live = (1u << TW_GROUP) - 1u;
       if (g == ngr - 1) {  // the row's last group
-        live = nst - s0 >= GSTEPS ? live : (1u << (nst - s0)) - 1u;
+        live = nst - s0 >= TW_GROUP ? live : (1u << (nst - s0)) - 1u;
         if (tail_lane) {
 #pragma unroll
-          for (int k = 0; k < GSTEPS; ++k)
+          for (int k = 0; k < TW_GROUP; ++k)
             if (s0 + k == nst - 1) v[k] = load_step(xr, V, nst - 1);
         }
       }
@@ -1152,26 +1186,16 @@ __global__ void __launch_bounds__(C::WARPS * 32, 1)
       fence_proxy_async_cta();
       __syncwarp();
       issue(slot);
-      test_group<C, WITH_LSE>(ws, st, v, s0, live, lm, ls, V32, Ku);
+      tw_group<C, WITH_LSE>(ws, st, nq, v, s0, live, lm, ls, V32, Ku);
     }
     if (!ok) break;
-    __syncwarp();
-    while (st.nq > 0) st = warp_drain<C>(ws, st, min(st.nq, uint32_t(C::BATCH)), V32, Ku);
-    if (guessed && st.cnt < Ku) {
-      // fewer than K elements reach the guess (the logsumexp of the pass is complete)
-      st = warp_reselect<C>(ws, xr, V, nst, V32, Ku);
-      margin *= 4.f;  // a wider margin for the rows after a miss
+    if (__any_sync(0xffffffffu, nq > 0)) st = tw_drain(ws, st, nq, V32, Ku);
+    if (speculative && st.cnt < Ku) {
+      // fewer than K elements reach the speculative start: select the row again from T0
+      st = tw_reselect(ws, xr, V, nst, T0, V32, Ku);
+      may_speculate = false;
+      if (lane == 0) atomicAdd(err + 2, 1u);
     }
-    if (may_guess) {
-      // Next guess: the K-th best value lowered by margin x (its distance to the (K/2)-th).
-      // For tails like the normal's or the logistic's the top order statistics are spaced
-      // about logarithmically in rank, so margin m lands near rank 2^m K of a row like this.
-      const float vk = key_to_float(comp_key(ws.buf[K - 1]));
-      const float vh = key_to_float(comp_key(ws.buf[K / 2 - 1]));
-      const float g = vk - margin * (vh - vk);
-      guess = (g > -INFINITY && g < INFINITY) ? key_floor(g) : 0u;  // none after a NaN or an infinity
-    }
-
     if (WITH_LSE) {
       for (int o = 16; o > 0; o >>= 1) {
         const float om = __shfl_xor_sync(0xffffffffu, lm, o);
@@ -1184,75 +1208,165 @@ __global__ void __launch_bounds__(C::WARPS * 32, 1)
       }
       if (lane == 0) lse_out[row] = lm + log2f(ls) * 0.69314718055994531f;
     }
-    warp_finish(ws.buf, st.cnt, Ku, xr, V32, err, ids_out + row * K, vals_out + row * K);
-    __syncwarp();
+    tw_hand_over(ws, st, Ku, hand + row * TW_HAND, hand_cnt + row);
   }
   if (!ok) {  // a wait timed out: let this warp's copies still in flight land (bounded) before leaving
     for (uint32_t u = gidx; u < issued; ++u)
-      mbar_wait(&ts.full[u & (C::RING - 1)], (u / C::RING) & 1u, &ts.never, err, 0x71u, 10000000ull);
+      mbar_wait(&ws.full[u & (C::RING - 1)], (u / C::RING) & 1u, &ws.never, err, 0x71u, 10000000ull);
   }
-  if (guess_out && gw < KD_TOPK_MAX_WARPS && lane == 0) guess_out[gw] = guess;
 }
 
-// Guessed starting thresholds are speculative: a row whose guess was too high is read a
-// second time by its warp alone, at the end of that warp's work, so a few misses decide
-// the launch's duration.  They pay off only when consecutive rows have about the same
-// scale (0.52 against 0.65 ms on 8192 rows of N(0, 2) over 151936 columns, K = 100) and
-// cost when it varies (0.77 ms with the rows' scales 5 % apart): off unless
-// KD_TOPK_GUESS=1 is set in the environment.
-static int topk_guesses() {
-  static int on = -1;
-  if (on < 0) {
-    const char* v = getenv("KD_TOPK_GUESS");
-    on = (v && v[0] == '1') ? 1 : 0;
+// Warp: sort the 32 E candidates a[] of the warp descending, in registers: a bitonic network
+// over positions p = lane E + i; a partner within the lane is swapped in place, one in
+// another lane (distance >= E) comes by shuffle.
+template <int E>
+__device__ __forceinline__ void warp_sort_regs_desc(unsigned long long (&a)[E]) {
+  const uint32_t lane = lane_id();
+#pragma unroll
+  for (int k = 2; k <= 32 * E; k <<= 1) {
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      if (j >= E) {
+        const uint32_t lm = uint32_t(j / E);
+#pragma unroll
+        for (int i = 0; i < E; ++i) {
+          const uint32_t p = lane * E + i;
+          const unsigned long long o = __shfl_xor_sync(0xffffffffu, a[i], lm);
+          const bool desc = (p & uint32_t(k)) == 0;
+          const bool lower = (p & uint32_t(j)) == 0;
+          const bool keep_max = desc == lower;
+          a[i] = keep_max ? (a[i] > o ? a[i] : o) : (a[i] < o ? a[i] : o);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < E; ++i) {
+          if ((i & j) == 0) {
+            const uint32_t p = lane * E + i;
+            const bool desc = (p & uint32_t(k)) == 0;
+            const unsigned long long x = a[i], y = a[i + j];
+            const bool swap = desc ? (x < y) : (x > y);
+            a[i] = swap ? y : x;
+            a[i + j] = swap ? x : y;
+          }
+        }
+      }
+    }
   }
-  return on;
 }
 
+// Warp: sort one row's handed-over candidates (cnt <= 32 E) and write the first K.
+template <int E>
+__device__ __forceinline__ void emit_row(const unsigned long long* hand, uint32_t cnt, uint32_t K, int32_t* ids_row,
+                                         float* vals_row, const float* lse, float* dropped) {
+  const uint32_t lane = lane_id();
+  unsigned long long a[E];
+#pragma unroll
+  for (int i = 0; i < E; ++i) {
+    const uint32_t p = lane * E + i;
+    a[i] = p < cnt ? hand[p] : 0ull;  // 0 ranks below every candidate (its ~column is never 0)
+  }
+  warp_sort_regs_desc<E>(a);
+  float s = 0.f, comp = 0.f;
+  const float l = dropped ? *lse : 0.f;
+#pragma unroll
+  for (int i = 0; i < E; ++i) {
+    const uint32_t p = lane * E + i;
+    if (p < K) {
+      const bool real = p < cnt;
+      ids_row[p] = real ? int32_t(cand_col(a[i])) : -1;
+      const float v = real ? __uint_as_float(cand_bits(a[i]) << 16) : -INFINITY;
+      vals_row[p] = v;
+      if (dropped && real) {  // compensated running sum of exp(v_k - lse)
+        const float y = expf(v - l) - comp;
+        const float t = s + y;
+        comp = (t - s) - y;
+        s = t;
+      }
+    }
+  }
+  if (dropped) {
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if (lane == 0) *dropped = 1.f - s;
+  }
+}
+
+constexpr int EMIT_WARPS = 8;
+
+__global__ void __launch_bounds__(EMIT_WARPS * 32)
+    kd_topk_emit_kernel(const unsigned long long* __restrict__ hand, const uint32_t* __restrict__ hand_cnt,
+                        int64_t N, int K, int32_t* __restrict__ ids_out, float* __restrict__ vals_out,
+                        const float* __restrict__ lse, float* __restrict__ dropped_out, uint32_t* err) {
+  const int64_t nwarps = int64_t(gridDim.x) * EMIT_WARPS;
+  for (int64_t row = int64_t(blockIdx.x) * EMIT_WARPS + (threadIdx.x >> 5); row < N; row += nwarps) {
+    uint32_t cnt = hand_cnt[row];
+    if (!KD_DCHECK(cnt <= uint32_t(TW_HAND), err, 0x7501)) cnt = TW_HAND;
+    const unsigned long long* h = hand + row * TW_HAND;
+    int32_t* ids_row = ids_out + row * K;
+    float* vals_row = vals_out + row * K;
+    float* d = dropped_out ? dropped_out + row : nullptr;
+    if (cnt <= 128u && K <= 128)
+      emit_row<4>(h, cnt, uint32_t(K), ids_row, vals_row, lse ? lse + row : nullptr, d);
+    else
+      emit_row<8>(h, cnt, uint32_t(K), ids_row, vals_row, lse ? lse + row : nullptr, d);
+  }
+}
+
+// Streaming-kernel shared memory and its per-device attribute.
 template <class C>
-cudaError_t launch_topk_tma(const uint16_t* X, int64_t N, int64_t V, int64_t ld, int K, int32_t* ids, float* vals,
-                            float* lse, uint32_t* err, cudaStream_t s, const uint32_t* guess_in, uint32_t* guess_out,
-                            const uint16_t* tile_max, int64_t ld_tile_max, int ntiles) {
+static cudaError_t launch_topk_stream(const uint16_t* X, int64_t N, int64_t V, int64_t ld, int K,
+                                      unsigned long long* hand, uint32_t* hand_cnt, float* lse, uint32_t* err,
+                                      cudaStream_t s, const uint16_t* tile_max, int64_t ld_tile_max, int ntiles) {
   static PerDevice<int> attr_plain, attr_lse;
-  const int smem = int(C::WARPS * sizeof(TopkTmaSmem<C>));
-  cudaError_t e = smem_attr_once(attr_plain, reinterpret_cast<const void*>(kd_topk_tma_kernel<C, false>), smem);
+  const int smem = int(C::WARPS * sizeof(TwSmem<C>));
+  cudaError_t e = smem_attr_once(attr_plain, reinterpret_cast<const void*>(kd_topk_stream_kernel<C, false>), smem);
   if (e == cudaSuccess)
-    e = smem_attr_once(attr_lse, reinterpret_cast<const void*>(kd_topk_tma_kernel<C, true>), smem);
+    e = smem_attr_once(attr_lse, reinterpret_cast<const void*>(kd_topk_stream_kernel<C, true>), smem);
   if (e != cudaSuccess) return e;
   int grid = gemm_max_grid();  // one block of C::WARPS row-streaming warps per SM
   if (int64_t(grid) * C::WARPS > N) grid = int((N + C::WARPS - 1) / C::WARPS);
-  if (grid > KD_TOPK_MAX_WARPS / C::WARPS) guess_in = guess_out = nullptr;  // more warps than guess words
-  const int guesses = topk_guesses();
   if (lse)
-    kd_topk_tma_kernel<C, true><<<grid, C::WARPS * 32, smem, s>>>(X, N, V, ld, K, ids, vals, lse, err, guesses,
-                                                                   guess_in, guess_out, tile_max, ld_tile_max, ntiles);
+    kd_topk_stream_kernel<C, true><<<grid, C::WARPS * 32, smem, s>>>(X, N, V, ld, K, hand, hand_cnt, lse, err,
+                                                                      tile_max, ld_tile_max, ntiles);
   else
-    kd_topk_tma_kernel<C, false><<<grid, C::WARPS * 32, smem, s>>>(X, N, V, ld, K, ids, vals, lse, err, guesses,
-                                                                    guess_in, guess_out, tile_max, ld_tile_max, ntiles);
-  return cudaSuccess;
+    kd_topk_stream_kernel<C, false><<<grid, C::WARPS * 32, smem, s>>>(X, N, V, ld, K, hand, hand_cnt, lse, err,
+                                                                       tile_max, ld_tile_max, ntiles);
+  return cudaGetLastError();
+}
+
+size_t topk_scratch_bytes(int64_t N, int K) {
+  if (K > TW_MAXK) return 0;
+  // per row: TW_HAND candidates, their count, the logsumexp (for the dropped mass)
+  return size_t(N) * TW_HAND * 8 + (size_t(N) * 4 + 255) / 256 * 256 + size_t(N) * 4;
 }
 
 cudaError_t launch_topk(const uint16_t* X, int64_t N, int64_t V, int64_t ld, int K, int32_t* ids, float* vals,
-                        float* lse, uint32_t* err, cudaStream_t s, const uint32_t* guess_in, uint32_t* guess_out,
+                        float* lse, float* dropped, uint32_t* err, void* scratch, cudaStream_t s,
                         const uint16_t* tile_max, int64_t ld_tile_max, int ntiles) {
-  static PerDevice<int> attr;
-  const int smem = int(sizeof(TopkSmem));
-  cudaError_t ea = smem_attr_once(attr, reinterpret_cast<const void*>(kd_topk_kernel), smem);
-  if (ea != cudaSuccess) return ea;
-  int grid = 2 * gemm_max_grid();
-  if (int64_t(grid) > N) grid = int(N);
-  if (grid <= 0) return cudaSuccess;
+  if (N <= 0) return cudaSuccess;
   prof_before("kd_topk_cache", s);
-  if (K <= TmSmallK::MAXK) {
-    cudaError_t e = launch_topk_tma<TmSmallK>(X, N, V, ld, K, ids, vals, lse, err, s, guess_in, guess_out, tile_max,
-                                              ld_tile_max, ntiles);
+  if (K <= TW_MAXK) {
+    uint8_t* w8 = static_cast<uint8_t*>(scratch);
+    unsigned long long* hand = reinterpret_cast<unsigned long long*>(w8);
+    uint32_t* hand_cnt = reinterpret_cast<uint32_t*>(w8 + size_t(N) * TW_HAND * 8);
+    float* lse_ws = reinterpret_cast<float*>(w8 + size_t(N) * TW_HAND * 8 + (size_t(N) * 4 + 255) / 256 * 256);
+    float* lse_rows = lse ? lse : (dropped ? lse_ws : nullptr);  // the dropped mass needs the logsumexp
+    cudaError_t e = K <= TmSmallK::MAXK
+                        ? launch_topk_stream<TmSmallK>(X, N, V, ld, K, hand, hand_cnt, lse_rows, err, s, tile_max,
+                                                       ld_tile_max, ntiles)
+                        : launch_topk_stream<TmLargeK>(X, N, V, ld, K, hand, hand_cnt, lse_rows, err, s, tile_max,
+                                                       ld_tile_max, ntiles);
     if (e != cudaSuccess) return e;
-  } else if (K <= TmLargeK::MAXK) {
-    cudaError_t e = launch_topk_tma<TmLargeK>(X, N, V, ld, K, ids, vals, lse, err, s, guess_in, guess_out, tile_max,
-                                              ld_tile_max, ntiles);
-    if (e != cudaSuccess) return e;
+    int grid = 4 * gemm_max_grid();
+    if (int64_t(grid) * EMIT_WARPS > N) grid = int((N + EMIT_WARPS - 1) / EMIT_WARPS);
+    kd_topk_emit_kernel<<<grid, EMIT_WARPS * 32, 0, s>>>(hand, hand_cnt, N, K, ids, vals, lse_rows, dropped, err);
   } else {
-    kd_topk_kernel<<<grid, TK_THREADS, smem, s>>>(X, N, V, ld, K, ids, vals, lse, err);
+    static PerDevice<int> attr;
+    const int smem = int(sizeof(TopkSmem));
+    cudaError_t ea = smem_attr_once(attr, reinterpret_cast<const void*>(kd_topk_kernel), smem);
+    if (ea != cudaSuccess) return ea;
+    int grid = 2 * gemm_max_grid();
+    if (int64_t(grid) > N) grid = int(N);
+    kd_topk_kernel<<<grid, TK_THREADS, smem, s>>>(X, N, V, ld, K, ids, vals, lse, dropped, err);
   }
   prof_after(s);
   return cudaGetLastError();

@@ -59,15 +59,16 @@ P = 1 << 20  # a fake, 256-aligned "device address"; never dereferenced on these
 def test_topk_rejects_bad_arguments(lib, args):
     a = dict(N=4, V=256, ld=256, K=8, ptr=P)
     a.update(args)
-    st = lib.kd_topk_cache(a["ptr"], a["N"], a["V"], a["ld"], a["K"], P, P, None, P, 4096, None)
+    st = lib.kd_topk_cache(a["ptr"], a["N"], a["V"], a["ld"], a["K"], P, P, None, None, P, 4096, None)
     assert st == _abi.KD_ERR_INVALID_ARG
 
 
 def test_topk_rejects_bad_workspace(lib):
-    assert lib.kd_topk_cache(P, 4, 256, 256, 8, P, P, None, None, 4096, None) == _abi.KD_ERR_WORKSPACE
-    assert lib.kd_topk_cache(P, 4, 256, 256, 8, P, P, None, P + 16, 4096, None) == _abi.KD_ERR_WORKSPACE
-    assert lib.kd_topk_cache(P, 4, 256, 256, 8, P, P, None, P, 16, None) == _abi.KD_ERR_WORKSPACE
-    assert lib.kd_topk_cache(P, 4, 256, 256, 8, P, P, P + 2, P, 4096, None) == _abi.KD_ERR_INVALID_ARG
+    assert lib.kd_topk_cache(P, 4, 256, 256, 8, P, P, None, None, None, 4096, None) == _abi.KD_ERR_WORKSPACE
+    assert lib.kd_topk_cache(P, 4, 256, 256, 8, P, P, None, None, P + 16, 4096, None) == _abi.KD_ERR_WORKSPACE
+    assert lib.kd_topk_cache(P, 4, 256, 256, 8, P, P, None, None, P, 16, None) == _abi.KD_ERR_WORKSPACE
+    assert lib.kd_topk_cache(P, 4, 256, 256, 8, P, P, P + 2, None, P, 4096, None) == _abi.KD_ERR_INVALID_ARG
+    assert lib.kd_topk_cache(P, 4, 256, 256, 8, P, P, None, P + 2, P, 4096, None) == _abi.KD_ERR_INVALID_ARG
 
 
 def _fwd(lib, **kw):

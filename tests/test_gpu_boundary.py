@@ -34,9 +34,9 @@ def test_invalid_calls_do_not_touch_outputs(kd, cuda_device):
     ws = kd.workspace(256, dev)
     s = torch.cuda.current_stream().cuda_stream
     assert kd._abi.kd_topk_cache(X.data_ptr(), 4, 256, 256, 300, ids.data_ptr(), vals.data_ptr(), None,
-                                 ws.data_ptr(), 256, s) == kd._abi.KD_ERR_INVALID_ARG
+                                 None, ws.data_ptr(), 256, s) == kd._abi.KD_ERR_INVALID_ARG
     assert kd._abi.kd_topk_cache(X.data_ptr() + 2, 4, 256, 256, 8, ids.data_ptr(), vals.data_ptr(), None,
-                                 ws.data_ptr(), 256, s) == kd._abi.KD_ERR_INVALID_ARG
+                                 None, ws.data_ptr(), 256, s) == kd._abi.KD_ERR_INVALID_ARG
     torch.cuda.synchronize()
     assert torch.all(ids == -7) and torch.all(vals == 3.0)
     with pytest.raises(kd.KDError):

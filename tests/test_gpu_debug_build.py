@@ -4,9 +4,9 @@ and report one out of range through the workspace error word instead of using it
 Runs, in a child process that loads the checked library, the cases that stress those
 indices most: top-K rows where every element becomes a candidate (ascending values),
 rows of one value (ties everywhere), both warp-per-row buffer sizes and the block kernel
-for K > 256, warps of several rows with guessed row thresholds (switched on here with
-KD_TOPK_GUESS=1) that miss, the fused teacher projection, and a fused fwd + bwd.  Every result must
-match the oracle and every error word must stay clean.
+for K > 256, warps of several rows whose speculative starts miss (their first 4096 values
+far above the rest), the fused teacher projection, and a fused fwd + bwd.  Every result
+must match the oracle and every error word must stay clean.
 """
 import os
 import subprocess
@@ -42,8 +42,9 @@ def topk_case(X, K):
     ids = torch.empty((N, K), dtype=torch.int32, device=dev)
     vals = torch.empty((N, K), dtype=torch.float32, device=dev)
     ws = kd.workspace(kd._abi.kd_topk_cache_workspace(N, V, K), dev)
-    st = kd._abi.kd_topk_cache(Xd.data_ptr(), N, V, V, K, ids.data_ptr(), vals.data_ptr(), None, ws.data_ptr(),
-                               ws.numel(), stream)
+    dropped = torch.empty((N,), dtype=torch.float32, device=dev)
+    st = kd._abi.kd_topk_cache(Xd.data_ptr(), N, V, V, K, ids.data_ptr(), vals.data_ptr(), None, dropped.data_ptr(),
+                               ws.data_ptr(), ws.numel(), stream)
     assert st == 0
     device_error(ws)
     rid, rval = oracle.topk_cache(bf16_bits(X), K)
@@ -59,11 +60,13 @@ for (N, V, K) in [(300, 20000, 100), (64, 9000, 200), (8, 40000, 1024)]:
     X[2, ::3] = -0.0
     topk_case(X.to(torch.bfloat16), K)
 
-# several rows per warp with scales jumping between rows: guessed thresholds, misses and
-# the reselection of a row from its start
-N, V = 5000, 3000  # rows 16-byte aligned (ld = V)
+# several rows per warp with scales jumping between rows, rows of few values, and rows whose
+# first 4096 values sit far above the rest: speculative starts that miss, and the selection
+# of such a row a second time from its exact bound
+N, V = 5000, 12000  # rows 16-byte aligned (ld = V)
 X = torch.randn((N, V), generator=g) * 10.0 ** (torch.rand((N, 1), generator=g) * 4 - 2)
 X[1::5] = torch.randint(-2, 3, (len(range(1, N, 5)), V), generator=g).float()
+X[0::3, :4096] += 6.0 * X[0::3].std(dim=1, keepdim=True)
 topk_case(X.to(torch.bfloat16), 100)
 
 # teacher projection + top-K with exact small-integer logits
@@ -98,7 +101,7 @@ print("checked build ok")
 def test_checked_build_parity_and_clean_error_word(cuda_device):
     from sparse_teacher_kl_gb300.build import build_library
     build_library(debug=True)
-    env = dict(os.environ, KD_DEBUG="1", KD_TOPK_GUESS="1")  # guessed row thresholds on, misses included
+    env = dict(os.environ, KD_DEBUG="1")
     r = subprocess.run([sys.executable, "-c", CHILD], cwd=ROOT, env=env, capture_output=True, text=True,
                        timeout=900)
     assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-3000:]
