@@ -519,16 +519,20 @@ struct TwCfg {
   static_assert(QL >= 2 * TW_GROUP, "a group's vectors fit in a lane's queue after the drain check");
   static_assert(RING == 4, "the quick start holds 16 vector maxima per lane");
 };
-using TmSmallK = TwCfg<512, 12, 8, 128, 4>;    // K <= 128
-using TmLargeK = TwCfg<512, 12, 8, 256, 4>;    // K <= 256
+using TmSmallK = TwCfg<512, 11, 12, 128, 4>;   // K <= 128
+using TmLargeK = TwCfg<512, 11, 12, 256, 4>;   // K <= 256
 
 template <class C>
 struct TwSmem {                             // one warp's part of the block's shared memory
   uint4 ring[C::RING][TW_GROUP][32];        // bulk-copy ring: slot, step, lane
-  uint4 qv[C::QL][32];                      // per-lane queues: slot j of lane l at [j][l]
-  uint32_t qcol[C::QL][32];                 // first column of each queued vector
+  union {
+    struct {
+      uint4 qv[C::QL][32];                  // per-lane queues: slot j of lane l at [j][l]
+      uint32_t qcol[C::QL][32];             // first column of each queued vector
+    };
+    uint32_t hist[256];                     // byte histograms (K-th of the tile maxima), used at a
+  };                                        // row's start, while the queues are empty
   unsigned long long buf[C::CAP];           // candidates (cand_make)
-  uint32_t hist[256];                       // byte histograms (K-th of the tile maxima)
   uint64_t full[C::RING];
   uint32_t abort;                           // set by a timed-out wait
   uint32_t never;                           // stays 0: the flag of the bounded waits after an abort
@@ -665,31 +669,6 @@ __device__ __forceinline__ uint32_t key_floor(float x) {
   return bf16_key(b);
 }
 
-// Sum over the 8 values x of v of 2^(x log2 e - b), b = lm log2 e: each word's pair of
-// values goes through one packed f32x2 multiply-add and one packed add.
-__device__ __forceinline__ float lse_terms(const uint4& v, float b) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-  unsigned long long l2e2, nb2, acc;
-  asm("mov.b64 %0, {%1, %1};" : "=l"(l2e2) : "r"(__float_as_uint(TW_LOG2E)));
-  asm("mov.b64 %0, {%1, %1};" : "=l"(nb2) : "r"(__float_as_uint(-b)));
-  asm("mov.b64 %0, {%1, %1};" : "=l"(acc) : "r"(0u));
-#pragma unroll
-  for (int h = 0; h < 4; ++h) {
-    unsigned long long x, t, e;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "r"(w[h] << 16), "r"(w[h] & 0xFFFF0000u));
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(t) : "l"(x), "l"(l2e2), "l"(nb2));
-    uint32_t t0, t1;
-    asm("mov.b64 {%0, %1}, %2;" : "=r"(t0), "=r"(t1) : "l"(t));
-    asm("mov.b64 %0, {%1, %2};"
-        : "=l"(e)
-        : "r"(__float_as_uint(ex2_approx(__uint_as_float(t0)))), "r"(__float_as_uint(ex2_approx(__uint_as_float(t1)))));
-    asm("add.rn.f32x2 %0, %0, %1;" : "+l"(acc) : "l"(e));
-  }
-  uint32_t a0, a1;
-  asm("mov.b64 {%0, %1}, %2;" : "=r"(a0), "=r"(a1) : "l"(acc));
-  return __uint_as_float(a0) + __uint_as_float(a1);
-}
-
 // Bulk copy global -> shared of `bytes` (a multiple of 16), completing on `bar`.
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
   asm volatile(
@@ -776,23 +755,31 @@ __device__ __forceinline__ void warp_rank_keys(const uint32_t (&kp)[E], const ui
   }
 }
 
-// Warp: the K-th largest key of the buffer's cnt entries (K <= cnt <= CAP = 512: 16 per lane)
-// and how many entries reach it.
-__device__ __forceinline__ uint32_t buf_rank_key(const unsigned long long* buf, uint32_t cnt, uint32_t K,
-                                                 uint32_t& count_ge) {
+// Warp: the K-th largest key of the buffer's cnt entries (K <= cnt <= 32 E) and how many
+// entries reach it.
+template <int E>
+__device__ __forceinline__ uint32_t buf_rank_key_e(const unsigned long long* buf, uint32_t cnt, uint32_t K,
+                                                   uint32_t& count_ge) {
   const uint32_t lane = lane_id();
-  uint32_t kp[16];
+  uint32_t kp[E];
   const uint32_t* hw = reinterpret_cast<const uint32_t*>(buf) + 1;  // high word of buf[i] at [2 i]
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
+  for (int i = 0; i < E; ++i) {
     const uint32_t j = lane + 32u * i;
     kp[i] = j < cnt ? (hw[2 * j] >> 16) + 1u : 0u;
   }
   const uint32_t rank[1] = {K};
   uint32_t T[1], cge[1];
-  warp_rank_keys<16, 1>(kp, rank, T, cge);
+  warp_rank_keys<E, 1>(kp, rank, T, cge);
   count_ge = cge[0];
   return T[0];
+}
+
+// The same for any cnt up to CAP = 512, holding 8 or 16 keys per lane: (key, count reaching it).
+__device__ __noinline__ uint2 buf_rank_key(const unsigned long long* buf, uint32_t cnt, uint32_t K) {
+  uint32_t cge = 0;
+  const uint32_t T = cnt <= 256u ? buf_rank_key_e<8>(buf, cnt, K, cge) : buf_rank_key_e<16>(buf, cnt, K, cge);
+  return make_uint2(T, cge);
 }
 
 // Warp: keep the entries of buf[0, cnt) whose key reaches T, in place (each round of 256 is
@@ -895,8 +882,8 @@ __device__ __forceinline__ uint32_t elem_mask(const uint4& v, const Sel& st) {
 // (an element it drops has K entries above it) when ties leave less than a slot's room.
 template <class C>
 __device__ __noinline__ Sel tw_raise(TwSmem<C>& ws, Sel st, uint32_t K, bool cut, bool strict) {
-  uint32_t cge = 0;
-  const uint32_t T = buf_rank_key(ws.buf, st.cnt, K, cge);
+  const uint2 tc = buf_rank_key(ws.buf, st.cnt, K);
+  const uint32_t T = tc.x, cge = tc.y;
   if (cut && cge < st.cnt) st.cnt = buf_filter_ge(ws.buf, st.cnt, T);
   if (cut && st.cnt > uint32_t(C::CAP - TW_STEP)) {
     warp_sort_desc(ws.buf, st.cnt);
@@ -951,13 +938,78 @@ __device__ __noinline__ Sel tw_drain(TwSmem<C>& ws, Sel st, uint32_t nq, uint32_
   return st;
 }
 
+// Row logsumexp, per lane: an offset lm (natural units) and, per step of a group, a packed
+// pair of partial sums of e^(x - lm) = 2^(x log2 e - lm log2 e); four independent chains.
+// The offset moves only when a group's maximum passes it by more than TW_LSE_SLACK, so that
+// every term stays below e^TW_LSE_SLACK and the rescale of the sums is rare.
+constexpr float TW_LSE_SLACK = 8.f;
+
+struct LseAcc {
+  float lm;                               // offset (-inf: nothing seen yet)
+  unsigned long long acc[TW_GROUP];       // packed f32x2 partial sums
+};
+
+__device__ __forceinline__ unsigned long long f32x2_splat(float x) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %1};" : "=l"(r) : "r"(__float_as_uint(x)));
+  return r;
+}
+
+__device__ __forceinline__ void lse_init(LseAcc& a) {
+  a.lm = -INFINITY;
+#pragma unroll
+  for (int k = 0; k < TW_GROUP; ++k) a.acc[k] = 0ull;
+}
+
+// Add the live steps' vectors of one group; gm = the group's largest value.
+__device__ __forceinline__ void lse_group(LseAcc& a, const uint4* v, uint32_t live, float gm) {
+  if (gm > a.lm + TW_LSE_SLACK) {  // also the first finite value (lm = -inf); never a NaN
+    const unsigned long long f = f32x2_splat(a.lm == -INFINITY ? 0.f : ex2_approx((a.lm - gm) * TW_LOG2E));
+#pragma unroll
+    for (int k = 0; k < TW_GROUP; ++k) asm("mul.rn.f32x2 %0, %0, %1;" : "+l"(a.acc[k]) : "l"(f));
+    a.lm = gm;
+  }
+  if (a.lm == -INFINITY) return;  // every value so far is -inf: every term is 0
+  const unsigned long long l2e2 = f32x2_splat(TW_LOG2E), nb2 = f32x2_splat(-a.lm * TW_LOG2E);
+#pragma unroll
+  for (int k = 0; k < TW_GROUP; ++k) {
+    if ((live >> k) & 1u) {
+      const uint32_t w[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        unsigned long long x, t, e;
+        asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "r"(w[h] << 16), "r"(w[h] & 0xFFFF0000u));
+        asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(t) : "l"(x), "l"(l2e2), "l"(nb2));
+        uint32_t t0, t1;
+        asm("mov.b64 {%0, %1}, %2;" : "=r"(t0), "=r"(t1) : "l"(t));
+        asm("mov.b64 %0, {%1, %2};"
+            : "=l"(e)
+            : "r"(__float_as_uint(ex2_approx(__uint_as_float(t0)))), "r"(__float_as_uint(ex2_approx(__uint_as_float(t1)))));
+        asm("add.rn.f32x2 %0, %0, %1;" : "+l"(a.acc[k]) : "l"(e));
+      }
+    }
+  }
+}
+
+// The lane's (offset, sum) pair.
+__device__ __forceinline__ float lse_sum(const LseAcc& a) {
+  float s = 0.f;
+#pragma unroll
+  for (int k = 0; k < TW_GROUP; ++k) {
+    uint32_t lo, hi;
+    asm("mov.b64 {%0, %1}, %2;" : "=r"(lo), "=r"(hi) : "l"(a.acc[k]));
+    s += __uint_as_float(lo) + __uint_as_float(hi);
+  }
+  return s;
+}
+
 // One group of TW_GROUP steps of a lane, vectors v[0 ..]: the packed pre-test of each against
 // the threshold; the vectors that pass go to the lane's queue (predicated stores), and the
 // warp drains the queues when one of them has less than a group's room left.  s0 = the
 // group's first step; `live` = its steps that exist (the row's last group may have fewer).
 template <class C, bool WITH_LSE>
 __device__ __forceinline__ void tw_group(TwSmem<C>& ws, Sel& st, uint32_t& nq, const uint4* v, int s0,
-                                         uint32_t live, float& lm, float& ls, uint32_t V32, uint32_t K) {
+                                         uint32_t live, LseAcc& la, uint32_t V32, uint32_t K) {
   const uint32_t lane = lane_id();
   uint32_t m[TW_GROUP];
 #pragma unroll
@@ -965,18 +1017,9 @@ __device__ __forceinline__ void tw_group(TwSmem<C>& ws, Sel& st, uint32_t& nq, c
   if (WITH_LSE) {
     uint32_t g = bmax2(bmax2(m[0], m[1]), bmax2(m[2], m[3]));
     g = bmax2(g, __byte_perm(g, 0u, 0x1032));
-    const float gm = __uint_as_float(g & 0xFFFF0000u);
-    if (gm > lm) {
-      ls *= ex2_approx((lm - gm) * TW_LOG2E);
-      lm = gm;
-    }
-    if (lm != -INFINITY) {
-      const float b = lm * TW_LOG2E;
-#pragma unroll
-      for (int k = 0; k < TW_GROUP; ++k)
-        if ((live >> k) & 1u) ls += lse_terms(v[k], b);
-    }
+    lse_group(la, v, live, __uint_as_float(g & 0xFFFF0000u));
   }
+  // nq <= QL - TW_GROUP when a group starts, so every slot addressed below is inside the queue
 #pragma unroll
   for (int k = 0; k < TW_GROUP; ++k) {
     if (half_passes(m[k], st.thr2, st.ge) && KD_DCHECK(nq < uint32_t(C::QL), ws.err, 0x7103)) {
@@ -1001,7 +1044,11 @@ __device__ __noinline__ void tw_hand_over(TwSmem<C>& ws, Sel st, uint32_t K, uns
   const uint32_t lane = lane_id();
   uint32_t cge = st.cnt;
   uint32_t T = 0;
-  if (st.cnt > K) T = buf_rank_key(ws.buf, st.cnt, K, cge);
+  if (st.cnt > K) {
+    const uint2 tc = buf_rank_key(ws.buf, st.cnt, K);
+    T = tc.x;
+    cge = tc.y;
+  }
   if (cge > uint32_t(TW_HAND)) {  // ties at T: order the buffer and keep exactly the best K
     warp_sort_desc(ws.buf, st.cnt);
     for (uint32_t i = lane; i < K; i += 32) hand[i] = ws.buf[i];
@@ -1033,13 +1080,14 @@ __device__ __noinline__ Sel tw_reselect(TwSmem<C>& ws, const uint16_t* xr, int64
   st.cnt = 0;
   sel_set(st, T0, true);
   uint32_t nq = 0;
-  float lm = -INFINITY, ls = 0.f;  // unused: the logsumexp pass is already complete
+  LseAcc la;  // unused: the logsumexp pass is already complete
+  lse_init(la);
   uint4 a[TW_GROUP], b[TW_GROUP];
   load_group(a, xr, V, 0);
   for (int s0 = 0; s0 < nst; s0 += TW_GROUP) {
     if (s0 + TW_GROUP < nst) load_group(b, xr, V, s0 + TW_GROUP);
     const uint32_t live = nst - s0 >= TW_GROUP ? (1u << TW_GROUP) - 1u : (1u << (nst - s0)) - 1u;
-    tw_group<C, false>(ws, st, nq, a, s0, live, lm, ls, V32, K);
+    tw_group<C, false>(ws, st, nq, a, s0, live, la, V32, K);
 #pragma unroll
     for (int k = 0; k < TW_GROUP; ++k) a[k] = b[k];
   }
@@ -1074,24 +1122,27 @@ __global__ void __launch_bounds__(C::WARPS * 32, 1)
   __syncwarp();
 
   int64_t row = int64_t(blockIdx.x) * C::WARPS + (threadIdx.x >> 5);
-  // Producer: the warp's rows one after another, group by group.
+  // Producer: the warp's rows one after another, group by group.  A row's last group copies
+  // the whole 16-byte vectors that remain (possibly none).
+  const uint32_t last_bytes = uint32_t((V - int64_t(ngr - 1) * TW_GROUP * TW_STEP) * 2) & ~15u;
   int64_t prow = row;
+  const uint16_t* psrc = X + prow * ld;  // the producer's current group
   int pg = 0;
   uint32_t issued = 0;
   auto issue = [&](uint32_t slot) {
     if (prow < N) {
       if (lane == 0) {
-        const int64_t e0 = int64_t(pg) * TW_GROUP * TW_STEP;
-        const int64_t left = V - e0;
-        uint32_t bytes = left >= int64_t(TW_GROUP) * TW_STEP ? GBYTES : uint32_t(left * 2) & ~15u;
-        if (!KD_DCHECK(e0 >= 0 && e0 + bytes / 2 <= V && bytes <= GBYTES, err, 0x7401)) bytes = 0;
+        uint32_t bytes = pg < ngr - 1 ? GBYTES : last_bytes;
+        if (!KD_DCHECK(psrc + bytes / 2 <= X + prow * ld + V, err, 0x7401)) bytes = 0;
         mbar_arrive_expect_tx(&ws.full[slot], bytes);  // 0 bytes: the phase completes on the arrival
-        if (bytes != 0) bulk_g2s(&ws.ring[slot][0][0], X + prow * ld + e0, bytes, &ws.full[slot]);
+        if (bytes != 0) bulk_g2s(&ws.ring[slot][0][0], psrc, bytes, &ws.full[slot]);
       }
       ++issued;
+      psrc += TW_GROUP * TW_STEP;
       if (++pg == ngr) {
         pg = 0;
         prow += nwarps;
+        psrc = X + prow * ld;
       }
     }
   };
@@ -1106,7 +1157,8 @@ __global__ void __launch_bounds__(C::WARPS * 32, 1)
     st.cnt = 0;
     sel_set(st, 0u, true);  // key >= 0: every element, until a start applies
     uint32_t nq = 0;
-    float lm = -INFINITY, ls = 0.f;
+    LseAcc la;
+    lse_init(la);
     uint32_t T0 = 0;        // exact start (0: none)
     bool speculative = false;
 
@@ -1186,7 +1238,7 @@ __global__ void __launch_bounds__(C::WARPS * 32, 1)
       fence_proxy_async_cta();
       __syncwarp();
       issue(slot);
-      tw_group<C, WITH_LSE>(ws, st, nq, v, s0, live, lm, ls, V32, Ku);
+      tw_group<C, WITH_LSE>(ws, st, nq, v, s0, live, la, V32, Ku);
     }
     if (!ok) break;
     if (__any_sync(0xffffffffu, nq > 0)) st = tw_drain(ws, st, nq, V32, Ku);
@@ -1197,6 +1249,7 @@ __global__ void __launch_bounds__(C::WARPS * 32, 1)
       if (lane == 0) atomicAdd(err + 2, 1u);
     }
     if (WITH_LSE) {
+      float lm = la.lm, ls = lse_sum(la);
       for (int o = 16; o > 0; o >>= 1) {
         const float om = __shfl_xor_sync(0xffffffffu, lm, o);
         const float os = __shfl_xor_sync(0xffffffffu, ls, o);
