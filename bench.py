@@ -15,6 +15,7 @@ from __future__ import annotations
 
 import argparse
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -153,7 +154,44 @@ def bench_topk(kd, dev, stream, peaks, steps):
     out["roofline"] = {"bound": "hbm", "achieved": out["ids+vals"]["achieved_gbs"], "peak": peaks["hbm"],
                        "unit": "GB/s", "frac": out["ids+vals"]["frac"], "traffic": ncu_traffic("kd_topk_cache", "mid"),
                        "peak_source": f"{peaks['source']} copy bandwidth"}
-    del X
+
+    # The same rows with each row's values scaled by 1 + s N(0, 1) (rows of different scales), and
+    # with every row's first 4096 values raised by 6 standard deviations (the start taken from a
+    # row's first values then misses: the row is selected twice and its warp stops speculating).
+    def timed(Xv):
+        def run():
+            st = kd._abi.kd_topk_cache(Xv.data_ptr(), N, V, V, K, ids.data_ptr(), vals.data_ptr(), None, None,
+                                       ws.data_ptr(), ws.numel(), stream.cuda_stream)
+            assert st == 0
+        for _ in range(3):
+            run()
+        torch.cuda.synchronize(dev)
+        ws[8:12].zero_()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(steps):
+            run()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        resel = int(ws[8:12].view(torch.int32).item()) / steps
+        ws[8:12].zero_()
+        return {"ms": a.elapsed_time(b) / steps, "reselected_rows_per_launch": resel}
+
+    Xs = torch.empty_like(X)
+    gen = torch.Generator(device=dev)
+    spread = {}
+    for sp in (0.05, 0.1, 0.2):
+        gen.manual_seed(int(sp * 1000) + 7)
+        f = 1.0 + sp * torch.randn((N, 1), generator=gen, device=dev)
+        for r0 in range(0, N, 512):
+            Xs[r0:r0 + 512] = (X[r0:r0 + 512].float() * f[r0:r0 + 512]).to(torch.bfloat16)
+        spread[str(sp)] = timed(Xs)
+    out["scale_spread"] = spread
+    Xs.copy_(X)
+    Xs[:, :4096] = (Xs[:, :4096].float() + 6.0 * math.sqrt(2.0)).to(torch.bfloat16)
+    out["prefix_high"] = timed(Xs)
+    del X, Xs
     torch.cuda.empty_cache()
     return out
 
@@ -238,6 +276,78 @@ def dense_torch_reference(H, W, ids, tlog, mask, dev):
     return out
 
 
+def config_dict(w, world: int = 1) -> dict:
+    """The workload a line measures (both arms print the same dict)."""
+    return {"workload": w.name, "B": w.B, "T": w.T, "d": w.d, "V": w.V, "K": w.K, "chunk": w.chunk, "tau": 1.0,
+            "teacher": w.teacher, "p_valid": w.p_valid,
+            "l2": f"inputs larger than L2 (W is {w.V * w.d * 2 / 1e9:.2f} GB, re-read every chunk)",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+
+
+def dense_estimate_gb(w) -> float:
+    """Device memory of the dense formulation's grids alone: bf16 logits plus five fp32 [N, V] grids."""
+    return w.N * w.V * (2 + 4 * 5) / 1e9
+
+
+def bench_fused(kd, dev, stream, w, steps, warmup, peaks, dense=True):
+    """kd_fused_kl_fwd + kd_fused_kl_bwd over every chunk of workload ``w``, per step: tokens/s, executed
+    TFLOP/s (8 d V per token) and its fraction of the sustained bf16 peak, and the device memory a step
+    needs beyond its inputs (the allocator's peak: workspace, gradients, loss and lse) next to the
+    workspace alone; with ``dense``, the plain PyTorch dense formulation's peak on the same inputs
+    (measured where it fits in memory, else an estimate of its grids)."""
+    import torch
+    from synth import make_inputs
+    torch.cuda.synchronize(dev)
+    torch.cuda.empty_cache()
+    H, W, ids, tlog, mask = make_inputs(w, dev)
+    N, d, V, K, c = w.N, w.d, w.V, w.K, w.chunk
+    inputs = torch.cuda.memory_allocated(dev)
+    torch.cuda.reset_peak_memory_stats(dev)
+    ws = kd.workspace(kd._abi.kd_fused_kl_workspace(N, d, V, K, c), dev)
+    grad_H = torch.empty((N, d), dtype=torch.bfloat16, device=dev)
+    grad_W = torch.zeros((V, d), dtype=torch.float32, device=dev)
+    g = torch.ones(1, dtype=torch.float32, device=dev)
+
+    def step():
+        loss, lse, _ = kd.fused_kl_forward(H, W, ids, tlog, mask, c, 1.0, ws=ws)
+        kd.fused_kl_backward(H, W, ids, tlog, mask, lse, g, c, 1.0, ws=ws, grad_H=grad_H, grad_W=grad_W)
+        return loss
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    peak = torch.cuda.max_memory_allocated(dev) - inputs
+    st, detail = kd.device_error(ws)
+    if st != 0:
+        raise SystemExit(f"{w.name}: device error {st} ({detail})")
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = a.elapsed_time(b) / steps
+    tflops = w.flops_executed() / (ms * 1e-3) / 1e12
+    out = {"tokens_per_s": N / (ms * 1e-3), "ms_per_step": ms, "tflops_executed": tflops,
+           "tflops_useful": w.flops_useful() / (ms * 1e-3) / 1e12,
+           "frac_of_bf16_peak": tflops / peaks["bf16_sustained"], "peak_device_gb": peak / 1e9,
+           "workspace_gb": ws.numel() / 1e9, "inputs_gb": inputs / 1e9}
+    del ws, grad_H, grad_W
+    torch.cuda.empty_cache()
+    if dense:
+        est = dense_estimate_gb(w)
+        free, _ = torch.cuda.mem_get_info(dev)
+        if est < 0.8 * free / 1e9:
+            out["dense_torch"] = dense_torch_reference(H, W, ids, tlog, mask, dev)
+        else:
+            out["dense_torch"] = {"fits": False, "estimate_gb": est,
+                                  "note": "not run: its grids alone exceed the free device memory"}
+    del H, W, ids, tlog, mask
+    torch.cuda.empty_cache()
+    return out
+
+
 def aggregate_over_ranks(ms_local: float, tokens_per_rank: int, world: int, all_reduce_max=None):
     """Whole-job step time (max over ranks) and throughput (all ranks' tokens / that time).
 
@@ -277,7 +387,7 @@ def run_reference(args, w):
         "impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "B": w.B, "T": w.T, "d": w.d, "V": w.V, "K": w.K, "chunk": w.chunk},
+        "config": config_dict(w, int(os.environ.get("WORLD_SIZE", "1"))),
         "cpu_baseline": {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": f"{rows} positions of {w.name} per step (float64 numpy, fused formulation, "
                                    f"fwd+bwd incl. full grad_W), tokens/s extrapolated per position"},
@@ -302,6 +412,7 @@ def main():
     ap.add_argument("--no-topk", action="store_true", help="skip the top-K cache measurement")
     ap.add_argument("--topk-only", action="store_true", help="only the top-K cache measurement (profiling)")
     ap.add_argument("--no-teacher", action="store_true", help="skip the teacher projection + top-K measurement")
+    ap.add_argument("--no-configs", action="store_true", help="skip the other four workloads")
     ap.add_argument("--rows", type=int, default=None, help="override B*T (profiling a reduced case)")
     ap.add_argument("--vocab", type=int, default=None, help="override V (profiling a reduced case)")
     args = ap.parse_args()
@@ -337,7 +448,10 @@ def main():
         return 0
     H, W, ids, tlog, mask = make_inputs(w, dev)
     N, d, V, K, c = w.N, w.d, w.V, w.K, w.chunk
+    inputs_alloc = torch.cuda.memory_allocated(dev)
+    torch.cuda.reset_peak_memory_stats(dev)
     ws = kd.workspace(kd._abi.kd_fused_kl_workspace(N, d, V, K, c), dev)
+    ws_gb = ws.numel() / 1e9
     grad_H = torch.empty((N, d), dtype=torch.bfloat16, device=dev)
     grad_W = torch.zeros((V, d), dtype=torch.float32, device=dev)
     g = torch.ones(1, dtype=torch.float32, device=dev)
@@ -348,12 +462,10 @@ def main():
         kd.fused_kl_backward(H, W, ids, tlog, mask, lse, g, c, 1.0, ws=ws, grad_H=grad_H, grad_W=grad_W)
         return loss
 
-    base_alloc = torch.cuda.memory_allocated(dev)
-    torch.cuda.reset_peak_memory_stats(dev)
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(dev)
-    peak_alloc = torch.cuda.max_memory_allocated(dev)
+    peak_alloc = torch.cuda.max_memory_allocated(dev) - inputs_alloc  # beyond the inputs
     st, detail = kd.device_error(ws)
     if st != 0:
         raise SystemExit(f"device error {st} ({detail}) during warm-up")
@@ -494,34 +606,68 @@ def main():
                "sample": f"{args.cpu_rows} positions of {w.name} (float64 numpy, fused formulation, fwd+bwd incl. "
                          f"full grad_W) in {dt:.1f} s, extrapolated per position"}
 
+    # ---- the other four workloads, each measured the same way (the gpt-oss one is the line's value)
+    configs = None
+    if rank == 0 and not args.no_configs:
+        del H, W, ids, tlog, mask, ws, grad_H, grad_W
+        torch.cuda.empty_cache()
+        configs = {}
+        for name in ("tiny", "small", "mid", "gptoss", "headline"):
+            if name == w.name:
+                configs[name] = {"tokens_per_s": tokens_per_s, "ms_per_step": ms, "tflops_executed": tflops_exec,
+                                 "tflops_useful": w.flops_useful() / (ms * 1e-3) / 1e12,
+                                 "frac_of_bf16_peak": tflops_exec / peak, "peak_device_gb": peak_alloc / 1e9,
+                                 "workspace_gb": ws_gb, "inputs_gb": inputs_alloc / 1e9,
+                                 "dense_torch": dense if dense is not None else
+                                 {"fits": False, "estimate_gb": dense_estimate_gb(w)}}
+            else:
+                configs[name] = bench_fused(kd, dev, stream, WORKLOADS[name], args.steps, args.warmup, peaks)
+
     if rank == 0:
+        def brief(x, keys):
+            return None if x is None else {k: x[k] for k in keys if k in x}
+        topk_brief = None if topk is None else {
+            "ms": topk["ids+vals"]["ms"], "achieved_gbs": topk["ids+vals"]["achieved_gbs"],
+            "frac_of_hbm": topk["ids+vals"]["frac"], "ms_with_lse": topk["ids+vals+lse"]["ms"],
+            "scale_spread_ms": {k: v["ms"] for k, v in topk.get("scale_spread", {}).items()},
+            "prefix_high_ms": topk.get("prefix_high", {}).get("ms")}
+        teacher_brief = brief(teacher, ("ms", "positions_per_s", "projection_tflops", "frac_of_bf16_peak"))
+        configs_brief = None if configs is None else {
+            k: dict(brief(v, ("tokens_per_s", "tflops_executed", "frac_of_bf16_peak", "peak_device_gb",
+                              "workspace_gb")),
+                    dense_torch_gb=(v["dense_torch"].get("peak_device_gb") if v["dense_torch"].get("fits")
+                                    else None),
+                    dense_torch_estimate_gb=(None if v["dense_torch"].get("fits")
+                                             else v["dense_torch"].get("estimate_gb")))
+            for k, v in configs.items()}
         line = {
             "metric": METRIC, "value": tokens_per_s, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": w.name, "B": w.B, "T": w.T, "d": d, "V": V, "K": K, "chunk": c, "tau": 1.0,
-                       "teacher": w.teacher, "p_valid": w.p_valid,
-                       "l2": f"inputs larger than L2 (W is {V * d * 2 / 1e9:.2f} GB, re-read every chunk)",
-                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "config": config_dict(w, world),
             "tflops_executed": tflops_exec,
             "tflops_useful": w.flops_useful() / (ms * 1e-3) / 1e12,
             "frac_of_bf16_peak": tflops_exec / peak,
             "peak_device_gb": peak_alloc / 1e9,
-            "workspace_gb": ws.numel() / 1e9,
-            "resident_inputs_outputs_gb": base_alloc / 1e9,
+            "workspace_gb": ws_gb,
+            "inputs_gb": inputs_alloc / 1e9,
+            "topk": topk_brief,
+            "teacher_topk_brief": teacher_brief,
+            "configs": configs_brief,
             "roofline": {"bound": "tensor", "kernel": dom_name, "achieved": achieved, "peak": peak,
                          "unit": "TFLOP/s", "frac": achieved / peak, "traffic": ncu_traffic(dom_name, w.name),
                          "peak_source": f"{peaks['source']} bf16 sustained",
                          "flops_per_launch": gemm_flops_per_chunk},
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+            "clocks": clocks.summary(),
+            "gpu_launches": launches,
             "topk_cache": topk,
             "teacher_topk": teacher,
+            "configs_detail": configs,
             "forward_chunked": fc,
             "dense_torch_reference": dense,
             "kernels": kernels,
-            "gpu_launches": launches,
-            "clocks": clocks.summary(),
-            "e2e": e2e,
-            "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -25,9 +25,9 @@ def kd(cuda_device):
     return kd
 
 
-def _peak(kd, dev, N, chunk):
+def _peak(kd, dev, N, chunk, d=D, v=V, k=K, teacher="zipf", p_valid=1.0):
     """Bytes allocated at the peak of one fwd+bwd beyond the inputs, and the workspace size."""
-    w = Workload("mem", 1, N, D, V, K, chunk, "zipf", 1.0, 4242)
+    w = Workload("mem", 1, N, d, v, k, chunk, teacher, p_valid, 4242)
     H, W, ids, tlog, mask = make_inputs(w, device=dev)
     g = torch.ones((1,), dtype=torch.float32, device=dev)
     torch.cuda.synchronize(dev)
@@ -59,3 +59,25 @@ def test_peak_grows_with_chunk_not_with_tokens(kd, cuda_device):
     grid = (16384 - 4096) * V * 4
     assert large - small <= (16384 - 4096) * (D * 2 + 64) + (4 << 20)
     assert large - small < 0.01 * grid
+
+
+def test_headline_shape_peak_grows_with_chunk_not_tokens(kd, cuda_device):
+    """The pages' headline shape (d = 2880, V = 201088, K = 100, 2 % padding): going from chunk 4096
+    to 8192 adds the workspace's growth to the peak (4096 more rows of bf16 dZ, V x 2 bytes each, plus
+    their logsumexp partials and split buffers), and four times the positions at chunk 8192 adds only
+    the O(N d) outputs, far below one N x V grid ([EPO] "Adónde se va la memoria": the dense teacher
+    tensor alone is 4 x 201,088 x 32,768 values)."""
+    hd, hv, hk = 2880, 201088, 100
+    kw = dict(d=hd, v=hv, k=hk, teacher="peaked_flat", p_valid=0.98)
+    N = 4 * 32768
+    p4, ws4 = _peak(kd, cuda_device, N, 4096, **kw)
+    p8, ws8 = _peak(kd, cuda_device, N, 8192, **kw)
+    assert ws8 - ws4 >= 4096 * hv * 2
+    assert abs((p8 - p4) - (ws8 - ws4)) <= (64 << 20)
+    # fixed chunk, a quarter of the positions: the peaks differ by the O(N d) outputs and O(N) rows
+    q8, _ = _peak(kd, cuda_device, N // 4, 8192, **kw)
+    dN = N - N // 4
+    assert p8 - q8 <= dN * (hd * 2 + 64) + (64 << 20)
+    assert p8 - q8 < 0.01 * dN * hv * 4
+    # the whole call beyond its inputs at the headline shape, next to the dense grids
+    assert p8 < 16e9 < 0.05 * N * hv * (2 + 4 * 5)
