@@ -526,12 +526,10 @@ template <class C>
 struct TwSmem {                             // one warp's part of the block's shared memory
   uint4 ring[C::RING][TW_GROUP][32];        // bulk-copy ring: slot, step, lane
   union {
-    struct {
-      uint4 qv[C::QL][32];                  // per-lane queues: slot j of lane l at [j][l]
-      uint32_t qcol[C::QL][32];             // first column of each queued vector
-    };
+    uint4 qv[C::QL][32];                    // per-lane queues: slot j of lane l at [j][l]
     uint32_t hist[256];                     // byte histograms (K-th of the tile maxima), used at a
   };                                        // row's start, while the queues are empty
+  uint32_t qcol[C::QL][32];                 // first column of each queued vector
   unsigned long long buf[C::CAP];           // candidates (cand_make)
   uint64_t full[C::RING];
   uint32_t abort;                           // set by a timed-out wait
@@ -1352,7 +1350,9 @@ __global__ void __launch_bounds__(EMIT_WARPS * 32)
   const int64_t nwarps = int64_t(gridDim.x) * EMIT_WARPS;
   for (int64_t row = int64_t(blockIdx.x) * EMIT_WARPS + (threadIdx.x >> 5); row < N; row += nwarps) {
     uint32_t cnt = hand_cnt[row];
-    if (!KD_DCHECK(cnt <= uint32_t(TW_HAND), err, 0x7501)) cnt = TW_HAND;
+    // at most TW_HAND (a row the streaming kernel never reached, after a timed-out wait it
+    // reported, holds no count: its outputs are not defined, but nothing is read past its slot)
+    if (!KD_DCHECK(cnt <= uint32_t(TW_HAND), err, 0x7501) || cnt > uint32_t(TW_HAND)) cnt = TW_HAND;
     const unsigned long long* h = hand + row * TW_HAND;
     int32_t* ids_row = ids_out + row * K;
     float* vals_row = vals_out + row * K;
