@@ -624,6 +624,8 @@ def main():
                 configs[name] = bench_fused(kd, dev, stream, WORKLOADS[name], args.steps, args.warmup, peaks)
 
     if rank == 0:
+        clk = clocks.summary()
+
         def brief(x, keys):
             return None if x is None else {k: x[k] for k in keys if k in x}
         topk_brief = None if topk is None else {
@@ -660,7 +662,11 @@ def main():
                          "flops_per_launch": gemm_flops_per_chunk},
             "e2e": e2e,
             "cpu_baseline": cpu,
-            "clocks": clocks.summary(),
+            "clocks": clk,
+            "clock_normalised": None if not clk.get("sm_mhz") else {
+                "ms_per_step_x_ghz": ms * clk["sm_mhz"] / 1000.0,
+                "tokens_per_s_per_ghz": tokens_per_s / (clk["sm_mhz"] / 1000.0),
+                "note": "the step is tensor-bound under the power cap: its rate follows the median SM clock"},
             "gpu_launches": launches,
             "topk_cache": topk,
             "teacher_topk": teacher,
