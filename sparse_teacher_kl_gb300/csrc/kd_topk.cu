@@ -3,25 +3,25 @@
 // the first fix; [DAI] "As duas inovações" item 1; [EPO] "Los dos cambios
 // propuestos", first item).
 //
-// HBM-bound: every logit is read once (twice for a row whose guessed starting
-// threshold, below, turned out too high).  Each element becomes a 48-bit
-// composite
-//   (order-preserving 16-bit key of the bf16 value) << 32 | (~column)
-// which is unique per element and orders by value descending, then column
-// ascending; the top-K are the K largest composites, so the result is exact with
-// any number of ties.  A threshold key T is valid once at least K elements seen so
-// far reach it: later elements then need key > T (an equal key comes with a larger
-// column and ranks below those K).  Two kernels:
-//  * K <= 256 (the pages' top-100): one warp per row, no block barrier (the
-//    warp-per-row section below);
+// HBM-bound: every logit is read once (twice for a row whose speculative start,
+// below, turned out too high).  Every element's rank is a unique composite of the
+// order-preserving 16-bit key of its bf16 value and its column, which orders by
+// value descending, then column ascending; the top K are the K largest composites,
+// so the result is exact with any number of ties.  A threshold key T is valid once
+// at least K elements seen so far reach it: later elements then need key > T (an
+// equal key comes with a larger column and ranks below those K).  Kernels:
+//  * K <= 256 (the pages' top-100): a streaming kernel, one warp per row and no
+//    block barrier, that hands each row's best candidates to the workspace, and an
+//    emit kernel that sorts them and writes the outputs (the warp-per-row section
+//    below);
 //  * 256 < K <= 1024: one CTA per row (grid-strided): the row streams through in
 //    segments of 4096 elements into a shared candidate buffer; when it passes half
 //    full, the K-th largest key in it is found with two byte histograms and only
 //    what reaches it is kept; the survivors are sorted once at the end.
 //
 // Optionally the same pass also takes the full-row logsumexp of the teacher
-// logits, so that the probability mass the cache drops, 1 - sum_k e^(t_k - lse),
-// can be reported per position ([ART] paragraph on the top-K limitation).
+// logits and the probability mass the cache drops, 1 - sum_k e^(t_k - lse), per
+// position ([ART] paragraph on the top-K limitation).
 #include <stdint.h>
 #include <stdlib.h>
 
@@ -517,7 +517,7 @@ struct TwCfg {
   static_assert(CAP >= MAXK + TW_STEP, "a slot's elements fit after a cut list");
   static_assert(MAXK <= TW_MAXK && MAXK <= TW_HAND && MAXK <= RING * TW_GROUP * 32, "limits of K");
   static_assert(QL >= 2 * TW_GROUP, "a group's vectors fit in a lane's queue after the drain check");
-  static_assert(RING == 4, "the quick start holds 16 vector maxima per lane");
+  static_assert(RING == 4, "the start from the ring holds 16 vector maxima per lane");
 };
 using TmSmallK = TwCfg<512, 11, 12, 128, 4>;   // K <= 128
 using TmLargeK = TwCfg<512, 11, 12, 256, 4>;   // K <= 256
