@@ -517,7 +517,7 @@ struct TwCfg {
   static_assert(CAP >= MAXK + TW_STEP, "a slot's elements fit after a cut list");
   static_assert(MAXK <= TW_MAXK && MAXK <= TW_HAND && MAXK <= RING * TW_GROUP * 32, "limits of K");
   static_assert(QL >= 2 * TW_GROUP, "a group's vectors fit in a lane's queue after the drain check");
-  static_assert(RING == 4, "the start from the ring holds 16 vector maxima per lane");
+  static_assert(RING == 4, "the quick start holds 16 vector maxima per lane");
 };
 using TmSmallK = TwCfg<512, 11, 12, 128, 4>;   // K <= 128
 using TmLargeK = TwCfg<512, 11, 12, 256, 4>;   // K <= 256
