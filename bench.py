@@ -677,6 +677,7 @@ def main():
         }
         print(json.dumps(line), flush=True)
     if world > 1:
+        dist.barrier()  # the other ranks wait while rank 0 measures the extra legs, then all leave together
         dist.destroy_process_group()
     return 0
 
