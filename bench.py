@@ -634,28 +634,33 @@ def main():
             "scale_spread_ms": {k: v["ms"] for k, v in topk.get("scale_spread", {}).items()},
             "prefix_high_ms": topk.get("prefix_high", {}).get("ms")}
         teacher_brief = brief(teacher, ("ms", "positions_per_s", "projection_tflops", "frac_of_bf16_peak"))
-        configs_brief = None if configs is None else {
-            k: dict(brief(v, ("tokens_per_s", "tflops_executed", "frac_of_bf16_peak", "peak_device_gb",
-                              "workspace_gb")),
-                    dense_torch_gb=(v["dense_torch"].get("peak_device_gb") if v["dense_torch"].get("fits")
-                                    else None),
-                    dense_torch_estimate_gb=(None if v["dense_torch"].get("fits")
-                                             else v["dense_torch"].get("estimate_gb")))
-            for k, v in configs.items()}
+        def config_brief(v):
+            dt = v["dense_torch"]
+            out = {"tokens_per_s": v["tokens_per_s"], "tflops": v["tflops_executed"],
+                   "frac_of_bf16_peak": v["frac_of_bf16_peak"], "peak_gb": v["peak_device_gb"],
+                   "workspace_gb": v["workspace_gb"]}
+            if dt.get("fits"):
+                out["dense_torch_gb"] = dt["peak_device_gb"]
+            else:
+                out["dense_torch_estimate_gb"] = dt.get("estimate_gb")
+            return out
+
+        configs_brief = None if configs is None else {k: config_brief(v) for k, v in configs.items()}
+        def r4(x):
+            """Numbers of the closing summaries to four significant digits."""
+            if isinstance(x, float):
+                return float(f"{x:.4g}")
+            if isinstance(x, dict):
+                return {k: r4(v) for k, v in x.items()}
+            return x
+
+        # Contract keys first, details next; the short summaries close the line, where a reader
+        # keeping only the end of the output still finds them.
         line = {
             "metric": METRIC, "value": tokens_per_s, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": config_dict(w, world),
-            "tflops_executed": tflops_exec,
-            "tflops_useful": w.flops_useful() / (ms * 1e-3) / 1e12,
-            "frac_of_bf16_peak": tflops_exec / peak,
-            "peak_device_gb": peak_alloc / 1e9,
-            "workspace_gb": ws_gb,
-            "inputs_gb": inputs_alloc / 1e9,
-            "topk": topk_brief,
-            "teacher_topk_brief": teacher_brief,
-            "configs": configs_brief,
             "roofline": {"bound": "tensor", "kernel": dom_name, "achieved": achieved, "peak": peak,
                          "unit": "TFLOP/s", "frac": achieved / peak, "traffic": ncu_traffic(dom_name, w.name),
                          "peak_source": f"{peaks['source']} bf16 sustained",
@@ -663,17 +668,25 @@ def main():
             "e2e": e2e,
             "cpu_baseline": cpu,
             "clocks": clk,
-            "clock_normalised": None if not clk.get("sm_mhz") else {
-                "ms_per_step_x_ghz": ms * clk["sm_mhz"] / 1000.0,
-                "tokens_per_s_per_ghz": tokens_per_s / (clk["sm_mhz"] / 1000.0),
-                "note": "the step is tensor-bound under the power cap: its rate follows the median SM clock"},
             "gpu_launches": launches,
+            "kernels": kernels,
+            "dense_torch_reference": dense,
+            "forward_chunked": fc,
             "topk_cache": topk,
             "teacher_topk": teacher,
             "configs_detail": configs,
-            "forward_chunked": fc,
-            "dense_torch_reference": dense,
-            "kernels": kernels,
+            "tflops_executed": tflops_exec,
+            "tflops_useful": w.flops_useful() / (ms * 1e-3) / 1e12,
+            "frac_of_bf16_peak": tflops_exec / peak,
+            "peak_device_gb": peak_alloc / 1e9,
+            "workspace_gb": ws_gb,
+            "inputs_gb": inputs_alloc / 1e9,
+            "clock_normalised": None if not clk.get("sm_mhz") else {
+                "ms_per_step_x_ghz": ms * clk["sm_mhz"] / 1000.0,
+                "tokens_per_s_per_ghz": tokens_per_s / (clk["sm_mhz"] / 1000.0)},
+            "configs": r4(configs_brief),
+            "teacher_topk_brief": r4(teacher_brief),
+            "topk": r4(topk_brief),
         }
         print(json.dumps(line), flush=True)
     if world > 1:
