@@ -462,9 +462,9 @@ __global__ void __launch_bounds__(TK_THREADS, 2)
 //    of a slot before the warp barrier after which the slot is refilled;
 //  * a first threshold before any element is kept: the K-th largest of per-tile row
 //    maxima a producer supplies (the teacher projection's epilogue; exact), else from the
-//    ring's first RING groups, which it holds when the row begins: the K-th largest of
-//    their 512 vector maxima (T0; at least K elements reach it: exact), raised by a
-//    speculative step (below) when that helps;
+//    row's first TW_QS groups (4096 elements), which the ring holds when the row begins:
+//    the K-th largest of their 512 vector maxima (T0; at least K elements reach it: exact),
+//    raised by a speculative step (below) when that helps;
 //  * the pre-test: per step, each lane's 8 values reduced by three packed bf16 maxima
 //    and compared with the threshold by one packed unordered compare (a NaN passes);
 //  * a vector that passes is queued in the lane's own shared-memory queue by predicated
@@ -480,8 +480,8 @@ __global__ void __launch_bounds__(TK_THREADS, 2)
 // registers (a bitonic network across the lanes) and writes the first K: ids, values (the
 // candidates carry their bf16 bits) and, when asked, the dropped teacher mass.
 //
-// The K-th largest key of a set of keys is found by bisection over the 16-bit key space
-// (17 steps of a per-lane count and a warp sum), in registers.
+// The K-th largest key of a set of keys is found by bisection between the smallest and the
+// largest key present (steps of a per-lane count and a warp sum), in registers.
 //
 // Speculative start.  Among the 512 vector maxima of the row's first 4096 elements, the
 // K-th largest T0 and the (K/4)-th largest T1 locate and scale the row's upper tail; the
@@ -501,6 +501,7 @@ constexpr int TW_HAND = 256;           // candidates handed over per row, at mos
 constexpr float TW_LOG2E = 1.4426950408889634f;
 constexpr float TW_SPEC_C = 1.3f;      // speculative start: T0 + c (T1 - T0)
 constexpr int TW_SPEC_MIN_K = 16;      // smaller K: too few vector maxima above T1 to place it
+constexpr int TW_QS = 4;               // groups whose vector maxima place the start: 4096 elements
 
 // A configuration: CAP candidate entries per warp, WARPS rows in flight per block (one block
 // per SM), QL queued vectors per lane, MAXK the largest K it serves, RING ring slots.  A
@@ -517,7 +518,7 @@ struct TwCfg {
   static_assert(CAP >= MAXK + TW_STEP, "a slot's elements fit after a cut list");
   static_assert(MAXK <= TW_MAXK && MAXK <= TW_HAND && MAXK <= RING * TW_GROUP * 32, "limits of K");
   static_assert(QL >= 2 * TW_GROUP, "a group's vectors fit in a lane's queue after the drain check");
-  static_assert(RING == 4, "the quick start holds 16 vector maxima per lane");
+  static_assert(RING >= TW_QS, "the ring holds the groups of the quick start");
 };
 using TmSmallK = TwCfg<512, 11, 12, 128, 4>;   // K <= 128
 using TmLargeK = TwCfg<512, 11, 12, 256, 4>;   // K <= 256
@@ -705,24 +706,40 @@ __device__ __forceinline__ uint32_t cand_bits(unsigned long long c) { return uin
 
 // Warp: for each of R ranks r, the largest key T_r that at least r of the warp's keys reach
 // (the r-th largest key), and how many reach it.  Each lane holds E keys, kp[i] = key + 1
-// (0: no key).  Bisection over [0, 2^16) on the warp's counts; rank must not exceed the
-// number of keys.
+// (0: no key).  Bisection on the warp's counts over [smallest key, largest key + 1), the
+// keys present: count(>= lo) >= r > count(>= hi) holds from the start, and each step halves
+// the bracket until it is one key wide (a handful of steps for keys that lie close, 16 for
+// keys spread over the whole 16-bit range); rank must not exceed the number of keys.
 template <int E, int R>
 __device__ __forceinline__ void warp_rank_keys(const uint32_t (&kp)[E], const uint32_t (&rank)[R], uint32_t (&T)[R],
                                                uint32_t (&count_ge)[R]) {
-  uint32_t n = 0;
+  uint32_t n = 0, kmin = 0xFFFFFFFFu, kmax = 0u;
 #pragma unroll
-  for (int i = 0; i < E; ++i) n += kp[i] != 0u ? 1u : 0u;
+  for (int i = 0; i < E; ++i) {
+    n += kp[i] != 0u ? 1u : 0u;
+    kmin = min(kmin, kp[i] != 0u ? kp[i] : 0xFFFFFFFFu);
+    kmax = max(kmax, kp[i]);
+  }
   n = __reduce_add_sync(0xffffffffu, n);
+  kmin = __reduce_min_sync(0xffffffffu, kmin);
+  kmax = __reduce_max_sync(0xffffffffu, kmax);
+  if (n == 0u) {  // no keys (not a caller's case): T = 0, nothing reaches it
+    kmin = 1u;
+    kmax = 1u;
+  }
   uint32_t lo[R], hi[R], clo[R];
 #pragma unroll
   for (int r = 0; r < R; ++r) {
-    lo[r] = 1u;          // keys + 1 >= lo: all n of them
-    hi[r] = 0x10001u;    // none
+    lo[r] = kmin;        // keys + 1 >= lo: all n of them
+    hi[r] = kmax + 1u;   // none
     clo[r] = n;
   }
 #pragma unroll 1
-  for (int it = 0; it < 17; ++it) {
+  for (;;) {
+    bool open = false;
+#pragma unroll
+    for (int r = 0; r < R; ++r) open |= hi[r] - lo[r] > 1u;
+    if (!open) break;  // lo and hi come from warp sums: the exit is warp-uniform
     uint32_t mid[R], c[R];
 #pragma unroll
     for (int r = 0; r < R; ++r) {
@@ -892,11 +909,11 @@ __device__ __noinline__ Sel tw_raise(TwSmem<C>& ws, Sel st, uint32_t K, bool cut
 }
 
 // Warp: move every lane's queued vectors (nq of them in this lane) into the candidate
-// buffer, one queue slot at a time, keeping the elements that pass the threshold exactly;
-// then raise the threshold once the buffer holds K entries.  The selection state goes in
-// and out by value (out of line, a reference would keep it in local memory).
+// buffer one queue slot at a time, keeping the elements that pass the threshold exactly and
+// raising the threshold before a slot that might not fit.  The selection state goes in and
+// out by value (out of line, a reference would keep it in local memory).
 template <class C>
-__device__ __noinline__ Sel tw_drain(TwSmem<C>& ws, Sel st, uint32_t nq, uint32_t V32, uint32_t K) {
+__device__ __noinline__ Sel tw_drain_slots(TwSmem<C>& ws, Sel st, uint32_t nq, uint32_t V32, uint32_t K) {
   const uint32_t lane = lane_id();
   const uint32_t slots = __reduce_max_sync(0xffffffffu, nq);
   for (uint32_t j = 0; j < slots; ++j) {
@@ -928,6 +945,80 @@ __device__ __noinline__ Sel tw_drain(TwSmem<C>& ws, Sel st, uint32_t nq, uint32_
       const uint32_t bits = uint32_t(((e & 4) ? hi : lo) >> (16 * (e & 3))) & 0xFFFFu;
       if (KD_DCHECK(pos < uint32_t(C::CAP), ws.err, 0x7101)) ws.buf[pos] = cand_make(bits, col0 + e);
       ++pos;
+    }
+    st.cnt += tot;
+    __syncwarp();
+  }
+  return st;
+}
+
+// The lane's queued vectors tested exactly against the threshold: for each of its nq slots
+// the bits of the elements that pass (elements past the row's end never do), eight bits per
+// slot, slots 0-7 in mw[0] and 8-15 in mw[1]; returns how many pass.
+template <class C>
+__device__ __forceinline__ uint32_t queue_masks(const TwSmem<C>& ws, const Sel& st, uint32_t nq, uint32_t V32,
+                                                unsigned long long (&mw)[2]) {
+  static_assert(C::QL <= 16, "two 64-bit words of slot masks");
+  const uint32_t lane = lane_id();
+  uint32_t n = 0;
+  mw[0] = 0ull;
+  mw[1] = 0ull;
+#pragma unroll 1
+  for (uint32_t j = 0; j < nq; ++j) {
+    const uint4 v = ws.qv[j][lane];
+    const uint32_t col0 = ws.qcol[j][lane];
+    uint32_t take = elem_mask(v, st);
+    if (col0 + TK_VEC > V32) take &= (V32 > col0 ? (1u << (V32 - col0)) - 1u : 0u);
+    const unsigned long long t = static_cast<unsigned long long>(take) << (8 * (j & 7u));
+    if (j < 8u) mw[0] |= t; else mw[1] |= t;
+    n += uint32_t(__popc(take));
+  }
+  return n;
+}
+
+// Warp: move every lane's queued vectors into the candidate buffer, keeping the elements that
+// pass the threshold exactly, then raise the threshold once the buffer holds K entries.
+// Every lane tests all its vectors first (no warp operation between them), one prefix sum
+// over the lanes' counts places them, and each lane writes its own.  When they do not all
+// fit, the threshold is raised on the buffer first (the queued elements lie in later columns
+// than every buffered one; key >= T is kept, which is always safe) and they are tested again;
+// if they still do not fit, they go one queue slot at a time.
+template <class C>
+__device__ __noinline__ Sel tw_drain(TwSmem<C>& ws, Sel st, uint32_t nq, uint32_t V32, uint32_t K) {
+  static_assert(8 * C::QL < 128, "a lane's passing count fits the seven-bit prefix sum");
+  const uint32_t lane = lane_id();
+  unsigned long long mw[2];
+  uint32_t n = queue_masks<C>(ws, st, nq, V32, mw);
+  uint32_t tot = __reduce_add_sync(0xffffffffu, n);
+  if (st.cnt + tot > uint32_t(C::CAP) && st.cnt >= K) {
+    st = tw_raise(ws, st, K, true, false);
+    n = queue_masks<C>(ws, st, nq, V32, mw);
+    tot = __reduce_add_sync(0xffffffffu, n);
+  }
+  if (st.cnt + tot > uint32_t(C::CAP)) {
+    st = tw_drain_slots(ws, st, nq, V32, K);
+  } else {
+    const uint32_t lt = (1u << lane) - 1u;
+    uint32_t pre = 0;
+#pragma unroll
+    for (int b = 0; b < 7; ++b) pre += uint32_t(__popc(__ballot_sync(0xffffffffu, (n >> b) & 1u) & lt)) << b;
+    uint32_t pos = st.cnt + pre;
+#pragma unroll 1
+    for (uint32_t j = 0; j < nq; ++j) {
+      uint32_t take = uint32_t((j < 8u ? mw[0] : mw[1]) >> (8 * (j & 7u))) & 0xFFu;
+      if (take) {
+        const uint4 v = ws.qv[j][lane];
+        const uint32_t col0 = ws.qcol[j][lane];
+        const unsigned long long lo = (static_cast<unsigned long long>(v.y) << 32) | v.x;
+        const unsigned long long hi = (static_cast<unsigned long long>(v.w) << 32) | v.z;
+        do {
+          const uint32_t e = __ffs(take) - 1;
+          take &= take - 1;
+          const uint32_t bits = uint32_t(((e & 4) ? hi : lo) >> (16 * (e & 3))) & 0xFFFFu;
+          if (KD_DCHECK(pos < uint32_t(C::CAP), ws.err, 0x7101)) ws.buf[pos] = cand_make(bits, col0 + e);
+          ++pos;
+        } while (take);
+      }
     }
     st.cnt += tot;
     __syncwarp();
@@ -1166,19 +1257,19 @@ __global__ void __launch_bounds__(C::WARPS * 32, 1)
       // reached by at least K elements: an exact start near the row's K-th value.
       const uint32_t T = warp_kth_largest_bf16(tile_max + row * ld_tile_max, uint32_t(ntiles), Ku, ws.hist);
       if (T != 0) sel_set(st, T, true);
-    } else if (ngr > C::RING) {
-      // The ring holds this row's first RING groups (none of them the row's last).
-      for (int r = 0; r < C::RING && ok; ++r) {
+    } else if (ngr > TW_QS) {
+      // The ring holds this row's first TW_QS groups (none of them the row's last).
+      for (int r = 0; r < TW_QS && ok; ++r) {
         const uint32_t u = gidx + uint32_t(r);
-        ok = mbar_wait(&ws.full[u & (C::RING - 1)], (u / C::RING) & 1u, &ws.abort, err, 0x72u);
+        ok = mbar_wait(&ws.full[u % C::RING], (u / C::RING) & 1u, &ws.abort, err, 0x72u);
       }
       if (!ok) break;
-      uint32_t kp[C::RING * TW_GROUP];  // the lane's vector maxima keys + 1
+      uint32_t kp[TW_QS * TW_GROUP];  // the lane's vector maxima keys + 1
 #pragma unroll
-      for (int r = 0; r < C::RING; ++r) {
+      for (int r = 0; r < TW_QS; ++r) {
 #pragma unroll
         for (int k = 0; k < TW_GROUP; ++k) {
-          const uint4 v = ws.ring[(gidx + r) & (C::RING - 1)][k][lane];
+          const uint4 v = ws.ring[(gidx + r) % C::RING][k][lane];
           const float mx = vec_max(v);
           uint32_t key;
           if (mx == mx) {
@@ -1194,7 +1285,7 @@ __global__ void __launch_bounds__(C::WARPS * 32, 1)
       }
       const uint32_t rank[2] = {Ku, Ku / 4 > 0 ? Ku / 4 : 1u};
       uint32_t T[2], cge[2];
-      warp_rank_keys<C::RING * TW_GROUP, 2>(kp, rank, T, cge);
+      warp_rank_keys<TW_QS * TW_GROUP, 2>(kp, rank, T, cge);
       T0 = T[0];
       uint32_t start = T0;
       if (may_speculate) {
@@ -1213,7 +1304,7 @@ __global__ void __launch_bounds__(C::WARPS * 32, 1)
     }
 
     for (int g = 0; g < ngr; ++g, ++gidx) {
-      const uint32_t slot = gidx & (C::RING - 1);
+      const uint32_t slot = gidx % C::RING;
       if (!mbar_wait(&ws.full[slot], (gidx / C::RING) & 1u, &ws.abort, err, 0x70u)) {
         ok = false;
         break;
@@ -1263,7 +1354,7 @@ __global__ void __launch_bounds__(C::WARPS * 32, 1)
   }
   if (!ok) {  // a wait timed out: let this warp's copies still in flight land (bounded) before leaving
     for (uint32_t u = gidx; u < issued; ++u)
-      mbar_wait(&ws.full[u & (C::RING - 1)], (u / C::RING) & 1u, &ws.never, err, 0x71u, 10000000ull);
+      mbar_wait(&ws.full[u % C::RING], (u / C::RING) & 1u, &ws.never, err, 0x71u, 10000000ull);
   }
 }
 
