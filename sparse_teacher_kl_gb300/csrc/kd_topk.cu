@@ -977,24 +977,21 @@ __device__ __forceinline__ uint32_t queue_masks(const TwSmem<C>& ws, const Sel& 
 }
 
 // Warp: move every lane's queued vectors into the candidate buffer, keeping the elements that
-// pass the threshold exactly, then raise the threshold once the buffer holds K entries.
+// pass the threshold exactly, then (with `raise`: more of the row is still to come) raise the
+// threshold once the buffer holds K entries.  A row's last drain leaves the buffer as it is:
+// the hand-over finds the same K-th key itself.
 // Every lane tests all its vectors first (no warp operation between them), one prefix sum
 // over the lanes' counts places them, and each lane writes its own.  When they do not all
-// fit, the threshold is raised on the buffer first (the queued elements lie in later columns
-// than every buffered one; key >= T is kept, which is always safe) and they are tested again;
-// if they still do not fit, they go one queue slot at a time.
+// fit, they go one queue slot at a time, the threshold raised between slots.  (Raising it on
+// the buffer first would not help: every drain ends with the threshold at the buffer's K-th
+// key, and the buffer is unchanged until the next drain.)
 template <class C>
-__device__ __noinline__ Sel tw_drain(TwSmem<C>& ws, Sel st, uint32_t nq, uint32_t V32, uint32_t K) {
+__device__ __noinline__ Sel tw_drain(TwSmem<C>& ws, Sel st, uint32_t nq, uint32_t V32, uint32_t K, bool raise) {
   static_assert(8 * C::QL < 128, "a lane's passing count fits the seven-bit prefix sum");
   const uint32_t lane = lane_id();
   unsigned long long mw[2];
-  uint32_t n = queue_masks<C>(ws, st, nq, V32, mw);
-  uint32_t tot = __reduce_add_sync(0xffffffffu, n);
-  if (st.cnt + tot > uint32_t(C::CAP) && st.cnt >= K) {
-    st = tw_raise(ws, st, K, true, false);
-    n = queue_masks<C>(ws, st, nq, V32, mw);
-    tot = __reduce_add_sync(0xffffffffu, n);
-  }
+  const uint32_t n = queue_masks<C>(ws, st, nq, V32, mw);
+  const uint32_t tot = __reduce_add_sync(0xffffffffu, n);
   if (st.cnt + tot > uint32_t(C::CAP)) {
     st = tw_drain_slots(ws, st, nq, V32, K);
   } else {
@@ -1023,7 +1020,7 @@ __device__ __noinline__ Sel tw_drain(TwSmem<C>& ws, Sel st, uint32_t nq, uint32_
     st.cnt += tot;
     __syncwarp();
   }
-  if (st.cnt >= K) st = tw_raise(ws, st, K, st.cnt > uint32_t(C::CAP / 2), true);
+  if (raise && st.cnt >= K) st = tw_raise(ws, st, K, st.cnt > uint32_t(C::CAP / 2), true);
   return st;
 }
 
@@ -1119,7 +1116,7 @@ __device__ __forceinline__ void tw_group(TwSmem<C>& ws, Sel& st, uint32_t& nq, c
   }
   if (__any_sync(0xffffffffu, nq > uint32_t(C::QL - TW_GROUP))) {
     __syncwarp();
-    st = tw_drain(ws, st, nq, V32, K);
+    st = tw_drain(ws, st, nq, V32, K, true);
     nq = 0;
   }
 }
@@ -1180,7 +1177,7 @@ __device__ __noinline__ Sel tw_reselect(TwSmem<C>& ws, const uint16_t* xr, int64
 #pragma unroll
     for (int k = 0; k < TW_GROUP; ++k) a[k] = b[k];
   }
-  if (__any_sync(0xffffffffu, nq > 0)) st = tw_drain(ws, st, nq, V32, K);
+  if (__any_sync(0xffffffffu, nq > 0)) st = tw_drain(ws, st, nq, V32, K, false);
   return st;
 }
 
@@ -1330,7 +1327,7 @@ __global__ void __launch_bounds__(C::WARPS * 32, 1)
       tw_group<C, WITH_LSE>(ws, st, nq, v, s0, live, la, V32, Ku);
     }
     if (!ok) break;
-    if (__any_sync(0xffffffffu, nq > 0)) st = tw_drain(ws, st, nq, V32, Ku);
+    if (__any_sync(0xffffffffu, nq > 0)) st = tw_drain(ws, st, nq, V32, Ku, false);
     if (speculative && st.cnt < Ku) {
       // fewer than K elements reach the speculative start: select the row again from T0
       st = tw_reselect(ws, xr, V, nst, T0, V32, Ku);
