@@ -467,12 +467,14 @@ __global__ void __launch_bounds__(TK_THREADS, 2)
 //    raised by a speculative step (below) when that helps;
 //  * the pre-test: per step, each lane's 8 values reduced by three packed bf16 maxima
 //    and compared with the threshold by one packed unordered compare (a NaN passes);
-//  * a vector that passes is queued in the lane's own shared-memory queue by predicated
-//    stores (no warp vote per vector); when a lane's queue is nearly full the warp drains
-//    every queue: one slot at a time, each lane tests its vector's elements exactly and
-//    the warp appends the ones that pass to a candidate buffer; the threshold is then
-//    raised to the K-th largest key of the buffer, and the buffer is filtered to what
-//    reaches it when it runs short of room;
+//  * a vector that passes is queued in the lane's own shared-memory queue (no warp vote
+//    per vector); when a lane's queue is nearly full the warp drains every queue: each
+//    lane tests the elements of all its queued vectors exactly, one prefix sum over the
+//    lanes' counts places the ones that pass in a candidate buffer (one slot at a time,
+//    with raises between slots, when they would not fit); the threshold is then raised to
+//    the K-th largest key of the buffer, and the buffer is filtered to what reaches it
+//    when it runs short of room (not after the row's last drain: the hand-over below
+//    finds that key itself);
 //  * when the row ends: the K-th largest key T of the buffer, and the candidates that
 //    reach it (K of them, or a few more on ties) handed to a per-row slot of the
 //    workspace; the warp goes on with its next row.
