@@ -229,13 +229,31 @@ def bench_teacher_topk(kd, dev, stream, peaks, steps):
     flops = 2.0 * N * dt * V
     kernels = {k: {"launches": n, "avg_ms": t / n, "ms_per_call": t / steps}
                for k, (n, t) in prof.summary().items()}
+    # the same calls also returning each row's logsumexp and dropped teacher mass
+    lse = torch.empty((N,), dtype=torch.float32, device=dev)
+    dropped = torch.empty((N,), dtype=torch.float32, device=dev)
+
+    def run_lse():
+        st = kd._abi.kd_teacher_topk(Ht.data_ptr(), Wt.data_ptr(), N, dt, V, K, c, ids.data_ptr(), vals.data_ptr(),
+                                     lse.data_ptr(), dropped.data_ptr(), ws.data_ptr(), ws.numel(),
+                                     stream.cuda_stream)
+        assert st == 0
+    run_lse()
+    torch.cuda.synchronize(dev)
+    a.record(stream)
+    for _ in range(steps):
+        run_lse()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    ms_lse = a.elapsed_time(b) / steps
     out = {"workload": f"gpt-oss shape: N={N}, dt={dt}, V={V}, K={K}, chunk={c}",
            "ms": ms, "positions_per_s": N / (ms * 1e-3),
            "projection_tflops": flops / (ms * 1e-3) / 1e12,
            "frac_of_bf16_peak": flops / (ms * 1e-3) / 1e12 / peaks["bf16_sustained"],
+           "ms_with_lse_and_dropped": ms_lse,
            "peak_source": f"{peaks['source']} bf16 sustained", "kernels": kernels,
            "workspace_gb": ws.numel() / 1e9}
-    del Ht, Wt, ids, vals, ws
+    del Ht, Wt, ids, vals, ws, lse, dropped
     torch.cuda.empty_cache()
     return out
 
@@ -633,7 +651,8 @@ def main():
             "frac_of_hbm": topk["ids+vals"]["frac"], "ms_with_lse": topk["ids+vals+lse"]["ms"],
             "scale_spread_ms": {k: v["ms"] for k, v in topk.get("scale_spread", {}).items()},
             "prefix_high_ms": topk.get("prefix_high", {}).get("ms")}
-        teacher_brief = brief(teacher, ("ms", "positions_per_s", "projection_tflops", "frac_of_bf16_peak"))
+        teacher_brief = brief(teacher, ("ms", "positions_per_s", "projection_tflops", "frac_of_bf16_peak",
+                                        "ms_with_lse_and_dropped"))
         def config_brief(v):
             dt = v["dense_torch"]
             out = {"tokens_per_s": v["tokens_per_s"], "tflops": v["tflops_executed"],

@@ -119,7 +119,11 @@ KD_API int kd_topk_cache(const void* logits_bf16, int64_t N, int64_t V, int64_t 
  * row logsumexp and dropped mass).  dt % 8 == 0; chunk a multiple of 128.  The
  * workspace holds the [chunk, V] bf16 logits and, per row and 256-column tile, the
  * tile's largest logit, which the projection's epilogue emits: with at least K
- * tiles, their K-th largest is an exact start for the row's selection.
+ * tiles, their K-th largest is an exact start for the row's selection.  When the
+ * row logsumexp or the dropped mass is asked for (K <= 256), the epilogue also
+ * emits per row and tile the sum of exp(z - tile max) over the tile's stored
+ * (bf16) logits; the row logsumexp is combined from those, and the selection runs
+ * without computing it.
  */
 KD_API size_t kd_teacher_topk_workspace(int64_t N, int64_t dt, int64_t V, int K, int64_t chunk);
 KD_API int kd_teacher_topk(const void* Ht_bf16, const void* Wt_bf16, int64_t N, int64_t dt, int64_t V, int K,

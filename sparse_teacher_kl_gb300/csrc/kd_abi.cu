@@ -263,14 +263,16 @@ size_t kd_fused_kl_workspace(int64_t N, int64_t d, int64_t V, int K, int64_t chu
 }
 
 // Teacher workspace: control block | the chunk's bf16 logits [rows_pad, ldz] | per-tile row
-// maxima [rows_pad, ldt] | the top-K scratch of one chunk.
+// maxima [rows_pad, ldt] | per-tile row sums [rows_pad, ldt] (fp32) | the chunk's row
+// logsumexp [rows_pad] | the top-K scratch of one chunk.
 static size_t teacher_topk_ws(int64_t N, int64_t V, int K, int64_t chunk) {
   const int64_t c = chunk < N ? chunk : N;
   const int64_t rows_pad = (c + BM - 1) / BM * BM;
   const int64_t ldz = (V + 7) / 8 * 8;
   const int64_t ldt = ((V + BN - 1) / BN + 7) / 8 * 8;  // per-tile row maxima of the logits
   return sizeof(Ctrl) + align_up(size_t(rows_pad) * size_t(ldz) * 2, 256) +
-         align_up(size_t(rows_pad) * size_t(ldt) * 2, 256) + align_up(topk_scratch_bytes(c, K), 256);
+         align_up(size_t(rows_pad) * size_t(ldt) * 2, 256) + align_up(size_t(rows_pad) * size_t(ldt) * 4, 256) +
+         align_up(size_t(rows_pad) * 4, 256) + align_up(topk_scratch_bytes(c, K), 256);
 }
 
 size_t kd_teacher_topk_workspace(int64_t N, int64_t dt, int64_t V, int K, int64_t chunk) {
@@ -305,7 +307,12 @@ int kd_teacher_topk(const void* Ht_bf16, const void* Wt_bf16, int64_t N, int64_t
   const int64_t crows = chunk < N ? chunk : N;
   const size_t rows_pad = size_t((crows + BM - 1) / BM * BM);
   uint16_t* tmax = reinterpret_cast<uint16_t*>(w8 + sizeof(Ctrl) + align_up(rows_pad * size_t(ldz) * 2, 256));
-  void* tk_scratch = reinterpret_cast<uint8_t*>(tmax) + align_up(rows_pad * size_t(ldt) * 2, 256);
+  float* tsum = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(tmax) + align_up(rows_pad * size_t(ldt) * 2, 256));
+  float* lse_chunk = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(tsum) + align_up(rows_pad * size_t(ldt) * 4, 256));
+  void* tk_scratch = reinterpret_cast<uint8_t*>(lse_chunk) + align_up(rows_pad * 4, 256);
+  // the row logsumexp (asked for, or needed by the dropped mass) comes from the projection's
+  // epilogue in per-tile pieces, so that the selection below runs without it
+  const bool tile_lse = (lse_out != nullptr || dropped_out != nullptr) && topk_takes_known_lse(K);
   const uint16_t* Ht = static_cast<const uint16_t*>(Ht_bf16);
   const int grid_max = gemm_max_grid();
   // Wt boxes: BN rows for single CTAs, BN / 2 for a CTA pair's halves
@@ -336,15 +343,23 @@ int kd_teacher_topk(const void* Ht_bf16, const void* Wt_bf16, int64_t N, int64_t
     p.c_tma = 1;   // bf16 logits written as TMA boxes into the row-major chunk buffer
     p.tile_max = tmax;
     p.ld_tile_max = ldt;
+    p.tile_sum = tile_lse ? tsum : nullptr;
     p.m_fast = 1;  // Wt (larger than L2) read once per chunk, the chunk of Ht kept in L2
     alignas(64) CUtensorMap tz;
     if (!make_tmap_2d_bf16(&tz, zbuf, uint64_t(V), uint64_t(n), uint64_t(ldz) * 2, 64, 32)) return KD_ERR_CUDA;
     p.a_k3d = p.b_k3d = p.cta_pair && dt64;
     cudaError_t e = launch_gemm(p, p.a_k3d ? th2 : th, p.b_k3d ? tw2 : tw[p.cta_pair], tz, grid_max, s);
     if (e != cudaSuccess) return KD_ERR_CUDA;
-    // exact top-K (and row logsumexp, dropped mass) of those bf16 logits
-    e = launch_topk(zbuf, n, V, ldz, K, ids_out + c0 * K, vals_out + c0 * K, lse_out ? lse_out + c0 : nullptr,
-                    dropped_out ? dropped_out + c0 : nullptr, &ctrl->err, tk_scratch, s, tmax, ldt, ntiles);
+    float* lse_rows = nullptr;
+    if (tile_lse) {
+      lse_rows = lse_out ? lse_out + c0 : lse_chunk;
+      e = launch_tile_lse(tmax, tsum, ldt, ntiles, n, lse_rows, s);
+      if (e != cudaSuccess) return KD_ERR_CUDA;
+    }
+    // exact top-K (and dropped mass; row logsumexp when not known already) of those bf16 logits
+    e = launch_topk(zbuf, n, V, ldz, K, ids_out + c0 * K, vals_out + c0 * K,
+                    (lse_out && !tile_lse) ? lse_out + c0 : nullptr, dropped_out ? dropped_out + c0 : nullptr,
+                    &ctrl->err, tk_scratch, s, tmax, ldt, ntiles, lse_rows);
     if (e != cudaSuccess) return KD_ERR_CUDA;
   }
   return KD_OK;

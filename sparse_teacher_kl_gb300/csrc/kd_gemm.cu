@@ -364,6 +364,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         const uint32_t a = acc_it & 1u;
         const uint32_t aph = (acc_it >> 1) & 1u;
         float tmax = -INFINITY;  // EPI_STORE with tile_max: the row's largest value in this tile
+        float tsm = -INFINITY, tss = 0.f;  // with tile_sum: running maximum and sum, rounded values
         // the tensor-memory loads below are warp-collective: decide per warp
         const bool got = mbar_wait(&tail->tfull[a], aph, abort_flag, p.err, 0x500u);
         if (!__all_sync(0xffffffffu, got)) {
@@ -532,9 +533,38 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             if (p.tile_max) {
               // rounding to bf16 is monotonic: the largest of the fp32 values, rounded, is the
               // largest stored value (fmaxf skips NaNs)
+              float cm = -INFINITY;
 #pragma unroll
               for (int i = 0; i < 32; ++i)
-                if (col0 + i < p.N) tmax = fmaxf(tmax, x[i]);
+                if (col0 + i < p.N) cm = fmaxf(cm, x[i]);
+              tmax = fmaxf(tmax, cm);
+              if (p.tile_sum) {
+                // sum of 2^((z - m) log2 e) over the stored (rounded) values z, m the running
+                // maximum of those values: the tile's maximum once the tile is done
+                constexpr float kL2E = 1.4426950408889634f;
+                if (cm != -INFINITY) {
+                  const float cr = __uint_as_float(pack_bf16x2(cm, cm) << 16);
+                  if (cr > tsm) {
+                    tss *= ex2_approx((tsm - cr) * kL2E);  // 0 while nothing was summed
+                    tsm = cr;
+                  }
+                  const float off = -tsm * kL2E;
+                  float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+                  for (int i = 0; i < 32; i += 2) {
+                    const uint32_t w = pack_bf16x2(x[i], x[i + 1]);
+                    const float e0 = ex2_approx(fmaf(__uint_as_float(w << 16), kL2E, off));
+                    const float e1 = ex2_approx(fmaf(__uint_as_float(w & 0xFFFF0000u), kL2E, off));
+                    s0 += col0 + i < p.N ? e0 : 0.f;
+                    s1 += col0 + i + 1 < p.N ? e1 : 0.f;
+                  }
+                  tss += s0 + s1;
+                } else {
+#pragma unroll
+                  for (int i = 0; i < 32; ++i)  // no number here: a NaN still makes the sum NaN
+                    if (col0 + i < p.N && x[i] != x[i]) tss = x[i];
+                }
+              }
             }
             if (c & 1) {
               fence_proxy_async_smem();
@@ -581,8 +611,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         tc_fence_before();
         if (CG == 2 && crank != 0) mbar_arrive_remote(mapa_u32(&tail->tempty[a], 0));
         else mbar_arrive(&tail->tempty[a]);
-        if (EPI == EPI_STORE && p.tile_max && ok && row < p.M)
+        if (EPI == EPI_STORE && p.tile_max && ok && row < p.M) {
           p.tile_max[size_t(row) * p.ld_tile_max + nb] = uint16_t(pack_bf16x2(tmax, tmax) & 0xFFFFu);
+          if (p.tile_sum) p.tile_sum[size_t(row) * p.ld_tile_max + nb] = tss;
+        }
       }
       if ((EPI == EPI_LSE || EPI == EPI_LSE_Z) && ok && row < p.rows) {
         const int g = n_first / p.n_group;

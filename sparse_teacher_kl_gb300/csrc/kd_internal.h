@@ -104,6 +104,11 @@ struct GemmProblem {
   // of NaNs), at tile_max[row * ld_tile_max + tile] for rows < M.
   uint16_t* tile_max;
   int64_t ld_tile_max;
+  // tile_sum (with tile_max; NULL: none): per row and BN-column tile, the sum of
+  // 2^((z - m) log2 e) over the row's bf16-rounded values z in the tile (columns < N), m
+  // the tile's maximum above (NaN if one of them is NaN), at tile_sum[row * ld_tile_max +
+  // tile] for rows < M: with tile_max, the row's logsumexp in pieces.
+  float* tile_sum;
   // m_fast = 1 (EPI_STORE / EPI_ACCUM with k_splits = 1): units walk m fastest, so the CTAs
   // in flight share one B tile while the A operand stays in L2 (for a small A and a B
   // larger than L2, as in the teacher projection); 0: n fastest (they share one A slab).
@@ -167,11 +172,19 @@ int gemm_max_grid();
 // speculative start made select twice).  scratch: topk_scratch_bytes(N, K) bytes, 256-byte
 // aligned.  tile_max (NULL: none): per row, the maxima of ntiles disjoint column ranges of
 // the row (bf16 bits, [N, ld_tile_max]); with ntiles >= K their K-th largest is a lower
-// bound of the row's K-th largest value and starts the row.
+// bound of the row's K-th largest value and starts the row.  lse_known (NULL: none; only
+// where topk_takes_known_lse(K)): the rows' logsumexp, already computed, for the dropped
+// mass; the selection then computes none (lse must be NULL).
 size_t topk_scratch_bytes(int64_t N, int K);
+bool topk_takes_known_lse(int K);
 cudaError_t launch_topk(const uint16_t* X, int64_t N, int64_t V, int64_t ld, int K, int32_t* ids,
                         float* vals, float* lse, float* dropped, uint32_t* err, void* scratch, cudaStream_t s,
-                        const uint16_t* tile_max = nullptr, int64_t ld_tile_max = 0, int ntiles = 0);
+                        const uint16_t* tile_max = nullptr, int64_t ld_tile_max = 0, int ntiles = 0,
+                        const float* lse_known = nullptr);
+// Row logsumexp [rows] from the per-tile maxima and sums of a projection's epilogue
+// (GemmProblem::tile_max, tile_sum; ntiles of them per row, row stride ld).
+cudaError_t launch_tile_lse(const uint16_t* tile_max, const float* tile_sum, int64_t ld, int ntiles, int64_t rows,
+                            float* lse, cudaStream_t s);
 
 cudaError_t launch_count_valid(const uint8_t* mask, int64_t N, int32_t* n_valid, cudaStream_t s);
 cudaError_t launch_teacher_prologue(const int32_t* ids, const float* tlog, int rows, int K, int64_t V,

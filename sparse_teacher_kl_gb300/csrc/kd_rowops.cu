@@ -396,4 +396,42 @@ cudaError_t launch_wait_timeout(uint32_t* err, uint64_t limit_ns, cudaStream_t s
   return cudaGetLastError();
 }
 
+// ------------------------------------------------- row logsumexp of tiles ---
+// A row's logsumexp from the per-tile pieces the teacher projection's epilogue leaves: per
+// BN-column tile t its largest stored value m_t (bf16 bits) and s_t = the sum of
+// 2^((z - m_t) log2 e) over its stored values z.  lse = M + ln(sum_t s_t 2^((m_t - M) log2 e)),
+// M the row's largest m_t.  One warp per row; a NaN in any tile's sum makes the row's NaN.
+
+constexpr int TL_WARPS = 8;
+
+__global__ void __launch_bounds__(TL_WARPS * 32)
+    kd_tile_lse_kernel(const uint16_t* __restrict__ tile_max, const float* __restrict__ tile_sum, int64_t ld,
+                       int ntiles, int64_t rows, float* __restrict__ lse) {
+  const int64_t row = int64_t(blockIdx.x) * TL_WARPS + (threadIdx.x >> 5);
+  if (row >= rows) return;
+  const int lane = int(threadIdx.x & 31u);
+  const uint16_t* tm = tile_max + row * ld;
+  const float* ts = tile_sum + row * ld;
+  float M = -INFINITY;
+  for (int t = lane; t < ntiles; t += 32) M = fmaxf(M, __uint_as_float(uint32_t(tm[t]) << 16));
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  float S = 0.f;
+  for (int t = lane; t < ntiles; t += 32) {
+    const float m = __uint_as_float(uint32_t(tm[t]) << 16), q = ts[t];
+    S += m == -INFINITY ? (q != q ? q : 0.f) : q * ex2_approx((m - M) * 1.4426950408889634f);
+  }
+  for (int o = 16; o > 0; o >>= 1) S += __shfl_xor_sync(0xffffffffu, S, o);
+  if (lane == 0) lse[row] = M == -INFINITY ? (S != S ? S : -INFINITY) : M + log2f(S) * 0.69314718055994531f;
+}
+
+cudaError_t launch_tile_lse(const uint16_t* tile_max, const float* tile_sum, int64_t ld, int ntiles, int64_t rows,
+                            float* lse, cudaStream_t s) {
+  if (rows <= 0) return cudaSuccess;
+  prof_before("kd_tile_lse", s);
+  kd_tile_lse_kernel<<<unsigned((rows + TL_WARPS - 1) / TL_WARPS), TL_WARPS * 32, 0, s>>>(tile_max, tile_sum, ld,
+                                                                                          ntiles, rows, lse);
+  prof_after(s);
+  return cudaGetLastError();
+}
+
 }  // namespace kd

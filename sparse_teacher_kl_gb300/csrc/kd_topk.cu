@@ -1476,6 +1476,8 @@ static cudaError_t launch_topk_stream(const uint16_t* X, int64_t N, int64_t V, i
   return cudaGetLastError();
 }
 
+bool topk_takes_known_lse(int K) { return K <= TW_MAXK; }
+
 size_t topk_scratch_bytes(int64_t N, int K) {
   if (K > TW_MAXK) return 0;
   // per row: TW_HAND candidates, their count, the logsumexp (for the dropped mass)
@@ -1484,7 +1486,7 @@ size_t topk_scratch_bytes(int64_t N, int K) {
 
 cudaError_t launch_topk(const uint16_t* X, int64_t N, int64_t V, int64_t ld, int K, int32_t* ids, float* vals,
                         float* lse, float* dropped, uint32_t* err, void* scratch, cudaStream_t s,
-                        const uint16_t* tile_max, int64_t ld_tile_max, int ntiles) {
+                        const uint16_t* tile_max, int64_t ld_tile_max, int ntiles, const float* lse_known) {
   if (N <= 0) return cudaSuccess;
   prof_before("kd_topk_cache", s);
   if (K <= TW_MAXK) {
@@ -1492,7 +1494,9 @@ cudaError_t launch_topk(const uint16_t* X, int64_t N, int64_t V, int64_t ld, int
     unsigned long long* hand = reinterpret_cast<unsigned long long*>(w8);
     uint32_t* hand_cnt = reinterpret_cast<uint32_t*>(w8 + size_t(N) * TW_HAND * 8);
     float* lse_ws = reinterpret_cast<float*>(w8 + size_t(N) * TW_HAND * 8 + (size_t(N) * 4 + 255) / 256 * 256);
-    float* lse_rows = lse ? lse : (dropped ? lse_ws : nullptr);  // the dropped mass needs the logsumexp
+    // the dropped mass needs the logsumexp: given, else computed by the selection
+    float* lse_rows = lse_known ? nullptr : (lse ? lse : (dropped ? lse_ws : nullptr));
+    const float* lse_emit = lse_known ? lse_known : lse_rows;
     cudaError_t e = K <= TmSmallK::MAXK
                         ? launch_topk_stream<TmSmallK>(X, N, V, ld, K, hand, hand_cnt, lse_rows, err, s, tile_max,
                                                        ld_tile_max, ntiles)
@@ -1501,7 +1505,7 @@ cudaError_t launch_topk(const uint16_t* X, int64_t N, int64_t V, int64_t ld, int
     if (e != cudaSuccess) return e;
     int grid = 4 * gemm_max_grid();
     if (int64_t(grid) * EMIT_WARPS > N) grid = int((N + EMIT_WARPS - 1) / EMIT_WARPS);
-    kd_topk_emit_kernel<<<grid, EMIT_WARPS * 32, 0, s>>>(hand, hand_cnt, N, K, ids, vals, lse_rows, dropped, err);
+    kd_topk_emit_kernel<<<grid, EMIT_WARPS * 32, 0, s>>>(hand, hand_cnt, N, K, ids, vals, lse_emit, dropped, err);
   } else {
     static PerDevice<int> attr;
     const int smem = int(sizeof(TopkSmem));

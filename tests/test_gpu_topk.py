@@ -253,6 +253,8 @@ def test_topk_dropped_mass(kd, cuda_device):
     (600, 200, 256, 5000, 37),   # dt not a multiple of 64: a ragged last k-block
     (300, 192, 256, 12000, 37),  # 47 column tiles >= K: rows start from their tile maxima (ragged last tile)
     (520, 64, 256, 20000, 64),   # the same over 79 tiles, three chunks
+    (300, 64, 128, 5123, 37),    # a last tile of 3 columns: the tile sums skip the columns past V
+    (300, 64, 128, 5000, 300),   # K > 256: the block selection computes the row logsumexp itself
 ])
 def test_teacher_topk_exact_integer_logits(kd, cuda_device, N, dt, chunk, V, K):
     """Small-integer teacher hidden states and weights make every logit an integer that fp32 holds
