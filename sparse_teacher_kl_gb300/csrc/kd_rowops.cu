@@ -46,65 +46,97 @@ cudaError_t launch_count_valid(const uint8_t* mask, int64_t N, int32_t* n_valid,
 
 constexpr int PRO_WARPS = 4;
 
+// Warp: sort the 32 E entries a[] of the warp ascending, in registers: a bitonic network over
+// positions p = lane E + i; a partner within the lane is swapped in place, one in another
+// lane (distance >= E) comes by shuffle.
+template <int E>
+__device__ __forceinline__ void warp_sort_regs_asc(unsigned long long (&a)[E]) {
+  const uint32_t lane = threadIdx.x & 31u;
+#pragma unroll
+  for (int k = 2; k <= 32 * E; k <<= 1) {
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      if (j >= E) {
+#pragma unroll
+        for (int i = 0; i < E; ++i) {
+          const uint32_t p = lane * E + i;
+          const unsigned long long o = __shfl_xor_sync(0xffffffffu, a[i], uint32_t(j / E));
+          const bool asc = (p & uint32_t(k)) == 0;
+          const bool lower = (p & uint32_t(j)) == 0;
+          a[i] = (asc == lower) ? (a[i] < o ? a[i] : o) : (a[i] < o ? o : a[i]);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < E; ++i) {
+          if ((i & j) == 0) {
+            const uint32_t p = lane * E + i;
+            const bool asc = (p & uint32_t(k)) == 0;
+            const unsigned long long x = a[i], y = a[i + j];
+            const bool swap = asc ? (x > y) : (x < y);
+            a[i] = swap ? y : x;
+            a[i + j] = swap ? x : y;
+          }
+        }
+      }
+    }
+  }
+}
+
+// E = KP / 32 entries per lane, KP the power of two >= max(K, 32); entry k of the row is
+// held by lane k / E.
+template <int E>
 __global__ void __launch_bounds__(PRO_WARPS * 32)
     kd_teacher_prologue_kernel(const int32_t* __restrict__ ids, const float* __restrict__ tlog, int rows, int K,
-                               int KP, int64_t V, float inv_tau, int32_t* __restrict__ ids_sorted,
+                               int64_t V, float inv_tau, int32_t* __restrict__ ids_sorted,
                                float* __restrict__ p_sorted, float* __restrict__ negent,
                                uint32_t* __restrict__ err, int64_t row0) {
-  extern __shared__ unsigned long long pro_smem[];
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  unsigned long long* ent = pro_smem + size_t(warp) * KP;
-  const int row = blockIdx.x * PRO_WARPS + warp;
+  const uint32_t lane = threadIdx.x & 31u;
+  const int row = blockIdx.x * PRO_WARPS + int(threadIdx.x >> 5);
   if (row >= rows) return;
   const int32_t* idr = ids + size_t(row) * K;
   const float* tr = tlog + size_t(row) * K;
 
+  float t[E];
   float m = -INFINITY;
-  for (int k = lane; k < K; k += 32) m = fmaxf(m, tr[k] * inv_tau);
+#pragma unroll
+  for (int i = 0; i < E; ++i) {
+    const int k = int(lane) * E + i;
+    t[i] = k < K ? tr[k] * inv_tau : -INFINITY;
+    m = fmaxf(m, t[i]);
+  }
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
   float s = 0.f;
-  for (int k = lane; k < K; k += 32) s += expf(tr[k] * inv_tau - m);
+#pragma unroll
+  for (int i = 0; i < E; ++i)
+    if (int(lane) * E + i < K) s += expf(t[i] - m);
   for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
   const float log_s = logf(s);
   float h = 0.f;
   bool bad = false;
-  for (int k = lane; k < KP; k += 32) {
-    unsigned long long e = ~0ull;
+  unsigned long long a[E];
+#pragma unroll
+  for (int i = 0; i < E; ++i) {
+    const int k = int(lane) * E + i;
+    a[i] = ~0ull;  // padding sorts after every entry
     if (k < K) {
-      const float lp = tr[k] * inv_tau - m - log_s;
+      const float lp = t[i] - m - log_s;
       const float pk = expf(lp);
       if (pk > 0.f) h += pk * lp;
       const int32_t id = idr[k];
       bad |= (id < 0) || (int64_t(id) >= V);
-      e = (static_cast<unsigned long long>(uint32_t(id)) << 32) | __float_as_uint(pk);
+      a[i] = (static_cast<unsigned long long>(uint32_t(id)) << 32) | __float_as_uint(pk);
     }
-    ent[k] = e;
   }
   for (int o = 16; o > 0; o >>= 1) h += __shfl_xor_sync(0xffffffffu, h, o);
   if (__any_sync(0xffffffffu, bad) && lane == 0) raise_error(err, KD_DEVERR_BAD_ID, uint32_t(row0 + row));
-  __syncwarp();
-  // bitonic sort, ascending by id
-  for (int k = 2; k <= KP; k <<= 1) {
-    for (int j = k >> 1; j > 0; j >>= 1) {
-      for (int i = lane; i < KP; i += 32) {
-        const int ixj = i ^ j;
-        if (ixj > i) {
-          const unsigned long long a = ent[i], b = ent[ixj];
-          const bool asc = (i & k) == 0;
-          if (asc ? (a > b) : (a < b)) {
-            ent[i] = b;
-            ent[ixj] = a;
-          }
-        }
-      }
-      __syncwarp();
+  warp_sort_regs_asc<E>(a);  // ascending by id
+#pragma unroll
+  for (int i = 0; i < E; ++i) {
+    const int k = int(lane) * E + i;
+    if (k < K) {
+      ids_sorted[size_t(row) * K + k] = int32_t(uint32_t(a[i] >> 32));
+      p_sorted[size_t(row) * K + k] = __uint_as_float(uint32_t(a[i]));
     }
-  }
-  for (int k = lane; k < K; k += 32) {
-    const unsigned long long e = ent[k];
-    ids_sorted[size_t(row) * K + k] = int32_t(uint32_t(e >> 32));
-    p_sorted[size_t(row) * K + k] = __uint_as_float(uint32_t(e));
   }
   if (lane == 0) negent[row] = h;
 }
@@ -112,17 +144,18 @@ __global__ void __launch_bounds__(PRO_WARPS * 32)
 cudaError_t launch_teacher_prologue(const int32_t* ids, const float* tlog, int rows, int K, int64_t V,
                                     float inv_tau, int32_t* ids_sorted, float* p_sorted, float* negent,
                                     uint32_t* err, int64_t row0, cudaStream_t s) {
-  int KP = 32;
-  while (KP < K) KP <<= 1;
-  const size_t smem = size_t(PRO_WARPS) * KP * sizeof(unsigned long long);
-  static PerDevice<int> attr;
-  cudaError_t e = smem_attr_once(attr, reinterpret_cast<const void*>(kd_teacher_prologue_kernel),
-                                 int(PRO_WARPS * 1024 * sizeof(unsigned long long)));
-  if (e != cudaSuccess) return e;
   const int grid = (rows + PRO_WARPS - 1) / PRO_WARPS;
   prof_before("kd_teacher_prologue", s);
-  kd_teacher_prologue_kernel<<<grid, PRO_WARPS * 32, smem, s>>>(ids, tlog, rows, K, KP, V, inv_tau, ids_sorted,
-                                                                p_sorted, negent, err, row0);
+#define KD_PROLOGUE(E_)                                                                                          \
+  kd_teacher_prologue_kernel<E_><<<grid, PRO_WARPS * 32, 0, s>>>(ids, tlog, rows, K, V, inv_tau, ids_sorted, \
+                                                                 p_sorted, negent, err, row0)
+  if (K <= 32) KD_PROLOGUE(1);
+  else if (K <= 64) KD_PROLOGUE(2);
+  else if (K <= 128) KD_PROLOGUE(4);
+  else if (K <= 256) KD_PROLOGUE(8);
+  else if (K <= 512) KD_PROLOGUE(16);
+  else KD_PROLOGUE(32);
+#undef KD_PROLOGUE
   prof_after(s);
   return cudaGetLastError();
 }

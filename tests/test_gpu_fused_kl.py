@@ -96,6 +96,8 @@ def test_grad_H_bf16_output(kd, cuda_device):
     (640, 520, 2560, 64, 384),    # several tiles in every direction
     (512, 192, 3000, 20, 256),    # CTA pairs, d = 3 k-blocks: the last stage's depth-2 box half past d
     (600, 320, 2100, 10, 256),    # CTA pairs over 5 k-blocks, then a single-CTA 88-row chunk
+    (200, 64, 1500, 300, 128),    # K = 300: the prologue sorts 16 entries per lane
+    (130, 64, 1024, 1024, 128),   # K = V = 1024 (the largest K): 32 entries per lane
 ])
 def test_ragged_shapes(kd, cuda_device, N, d, V, K, chunk):
     w = Workload("ragged", 1, N, d, V, K, chunk, "normal3", 0.9, 4242 + N)
