@@ -31,9 +31,10 @@
 namespace kd {
 
 constexpr int MAX_STAGES = 6;
-// EPI_ACCUM with a reduction depth K up to this stages its output through shared memory
-// (whole-row reductions); deeper, each thread reduces its own row directly.
-constexpr int ACCUM_STAGED_MAX_K = 1024;
+// EPI_ACCUM with a reduction depth K up to this adds its output through shared memory and
+// TMA reduce-adds (tmap_c: fp32 C, 32 x 32 boxes, 128-byte swizzle); deeper, each thread adds
+// its own row with vector reductions.
+constexpr int ACCUM_STAGED_MAX_K = 2048;
 
 struct __align__(8) GemmSmemTail {
   uint64_t full[MAX_STAGES];
@@ -508,24 +509,21 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             // free for the operand loads.  Each element gets exactly one addition per launch.
             if (p.K <= ACCUM_STAGED_MAX_K) {
               // A shallow reduction leaves the launch bound by this read-modify-write: the
-              // warp's 32 x 32 block goes through shared memory (two alternating 4 KB boxes,
-              // 128-byte rows, 16-byte chunks swizzled by row), so that each reduction
-              // instruction covers four whole 128-byte rows instead of 16 bytes of 32 rows.
+              // warp's 32 x 32 block goes to shared memory (two alternating 4 KB boxes, 128-byte
+              // rows, 16-byte chunks swizzled by row, as tmap_c's 128-byte swizzle lays them
+              // out) and one TMA reduce-add per box adds it to C, clipped at the edges.
               uint8_t* box = my_staging + (uint32_t(c) & 1u) * 4096u;
+              if (lane == 0) bulk_wait_read<1>();  // this box's reduce from two chunks ago has read it
+              __syncwarp();
 #pragma unroll
               for (int g4 = 0; g4 < 8; ++g4)
                 *reinterpret_cast<float4*>(box + lane * 128u + ((uint32_t(g4) ^ (lane & 7u)) * 16u)) =
                     make_float4(x[g4 * 4 + 0], x[g4 * 4 + 1], x[g4 * 4 + 2], x[g4 * 4 + 3]);
-              __syncwarp();  // (the box was last read two chunks ago, before the previous barrier)
-              const uint32_t ch = lane & 7u;
-#pragma unroll
-              for (int it = 0; it < 8; ++it) {
-                const uint32_t r = uint32_t(it) * 4u + (lane >> 3);
-                const float4 v = *reinterpret_cast<const float4*>(box + r * 128u + ((ch ^ (r & 7u)) * 16u));
-                const int grow = m_blk * BM + int(quarter * 32u + r);
-                const int gcol = col0 + int(ch) * 4;
-                if (grow < p.M && gcol + 4 <= p.N)
-                  red_add_v4(reinterpret_cast<float*>(p.C) + size_t(grow) * p.ldc + gcol, v.x, v.y, v.z, v.w);
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                tma_reduce_add_2d(&tmap_c, box, col0, m_blk * BM + int(quarter) * 32);
+                bulk_commit();
               }
             } else if (row < p.M) {
               float* dst = reinterpret_cast<float*>(p.C) + size_t(row) * p.ldc + col0;
@@ -646,7 +644,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             make_float4(run_m * scale2, run_s, run_g * p.inv_tau, 0.f);
       }
     }
-    if ((EPI == EPI_DZ || EPI == EPI_LSE_Z || (EPI == EPI_STORE && p.c_tma)) && lane == 0)
+    if ((EPI == EPI_DZ || EPI == EPI_LSE_Z || (EPI == EPI_STORE && p.c_tma) || (EPI == EPI_ACCUM && p.K <= ACCUM_STAGED_MAX_K)) && lane == 0)
       bulk_wait_all();  // output boxes done before exit
   }
 

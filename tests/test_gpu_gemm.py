@@ -34,11 +34,17 @@ def test_gemm_matches_float64(kd, cuda_device, a_mn, b_mn, M, N, K):
     assert err <= 1e-5 * ref.abs().max().item() * max(1.0, K / 64)
 
 
-def test_gemm_accumulates(kd, cuda_device):
-    A, B, ref = _case(256, 512, 128, 1, 1, seed=3, dev=cuda_device)
-    C0 = torch.randn((256, 512), generator=torch.Generator().manual_seed(4))
+@pytest.mark.parametrize("M,N,K", [
+    (256, 512, 128),    # reductions up to 2048 deep: staged blocks added by TMA reduce-adds
+    (296, 520, 200),    # the same, ragged rows and columns (clipped by the tensor map)
+    (1000, 264, 1096),
+    (600, 264, 2112),   # deeper: each thread adds its own row with vector reductions
+])
+def test_gemm_accumulates(kd, cuda_device, M, N, K):
+    A, B, ref = _case(M, N, K, 1, 1, seed=3 + K, dev=cuda_device)
+    C0 = torch.randn((M, N), generator=torch.Generator().manual_seed(4))
     C = C0.clone().to(cuda_device)
-    kd.gemm_bf16(A, B, 256, 512, 128, 1, 1, C=C)
+    kd.gemm_bf16(A, B, M, N, K, 1, 1, C=C)
     torch.cuda.synchronize()
     err = (C.double().cpu() - (ref + C0.double())).abs().max().item()
-    assert err <= 1e-4
+    assert err <= 1e-5 * ref.abs().max().item() * max(1.0, K / 64) + 1e-5
