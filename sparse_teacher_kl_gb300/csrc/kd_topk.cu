@@ -712,9 +712,11 @@ __device__ __forceinline__ uint32_t cand_bits(unsigned long long c) { return uin
 // keys present: count(>= lo) >= r > count(>= hi) holds from the start, and each step halves
 // the bracket until it is one key wide (a handful of steps for keys that lie close, 16 for
 // keys spread over the whole 16-bit range); rank must not exceed the number of keys.
+// lo_hint: per rank a warp-uniform kp value that at least rank[r] keys reach, a higher start
+// for the bracket (0: none).
 template <int E, int R>
 __device__ __forceinline__ void warp_rank_keys(const uint32_t (&kp)[E], const uint32_t (&rank)[R], uint32_t (&T)[R],
-                                               uint32_t (&count_ge)[R]) {
+                                               uint32_t (&count_ge)[R], const uint32_t (&lo_hint)[R]) {
   uint32_t n = 0, kmin = 0xFFFFFFFFu, kmax = 0u;
 #pragma unroll
   for (int i = 0; i < E; ++i) {
@@ -735,6 +737,13 @@ __device__ __forceinline__ void warp_rank_keys(const uint32_t (&kp)[E], const ui
     lo[r] = kmin;        // keys + 1 >= lo: all n of them
     hi[r] = kmax + 1u;   // none
     clo[r] = n;
+    if (lo_hint[r] > kmin && lo_hint[r] <= kmax) {
+      uint32_t c = 0;
+#pragma unroll
+      for (int i = 0; i < E; ++i) c += kp[i] >= lo_hint[r] ? 1u : 0u;
+      lo[r] = lo_hint[r];
+      clo[r] = __reduce_add_sync(0xffffffffu, c);
+    }
   }
 #pragma unroll 1
   for (;;) {
@@ -787,7 +796,8 @@ __device__ __forceinline__ uint32_t buf_rank_key_e(const unsigned long long* buf
   }
   const uint32_t rank[1] = {K};
   uint32_t T[1], cge[1];
-  warp_rank_keys<E, 1>(kp, rank, T, cge);
+  const uint32_t none[1] = {0u};
+  warp_rank_keys<E, 1>(kp, rank, T, cge, none);
   count_ge = cge[0];
   return T[0];
 }
@@ -1263,6 +1273,7 @@ __global__ void __launch_bounds__(C::WARPS * 32, 1)
         ok = mbar_wait(&ws.full[u % C::RING], (u / C::RING) & 1u, &ws.abort, err, 0x72u);
       }
       if (!ok) break;
+      static_assert(TW_QS * TW_GROUP == 16, "the bracket bounds below take 16 keys per lane");
       uint32_t kp[TW_QS * TW_GROUP];  // the lane's vector maxima keys + 1
 #pragma unroll
       for (int r = 0; r < TW_QS; ++r) {
@@ -1283,8 +1294,34 @@ __global__ void __launch_bounds__(C::WARPS * 32, 1)
         }
       }
       const uint32_t rank[2] = {Ku, Ku / 4 > 0 ? Ku / 4 : 1u};
+      // Lower bounds for the bracket: when every lane has g keys that reach b (the smallest
+      // of its g group maxima, groups of 16 / g consecutive keys), 32 g keys reach the smallest
+      // b of the warp; g is the least power of two with 32 g >= rank.
+      // lb[l]: the lane's smallest maximum over groups of 16 >> l keys (lb[0] its largest key)
+      uint32_t p2[8], p4[4], lb[5];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) p2[i] = max(kp[2 * i], kp[2 * i + 1]);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) p4[i] = max(p2[2 * i], p2[2 * i + 1]);
+      const uint32_t p8a = max(p4[0], p4[1]), p8b = max(p4[2], p4[3]);
+      lb[0] = max(p8a, p8b);
+      lb[1] = min(p8a, p8b);
+      lb[2] = min(min(p4[0], p4[1]), min(p4[2], p4[3]));
+      lb[3] = p2[0];
+#pragma unroll
+      for (int i = 1; i < 8; ++i) lb[3] = min(lb[3], p2[i]);
+      lb[4] = kp[0];
+#pragma unroll
+      for (int i = 1; i < 16; ++i) lb[4] = min(lb[4], kp[i]);
+      uint32_t hint[2];
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const uint32_t g = (rank[r] + 31u) / 32u;
+        const uint32_t b = g <= 1u ? lb[0] : g <= 2u ? lb[1] : g <= 4u ? lb[2] : g <= 8u ? lb[3] : lb[4];
+        hint[r] = __reduce_min_sync(0xffffffffu, b);
+      }
       uint32_t T[2], cge[2];
-      warp_rank_keys<TW_QS * TW_GROUP, 2>(kp, rank, T, cge);
+      warp_rank_keys<TW_QS * TW_GROUP, 2>(kp, rank, T, cge, hint);
       T0 = T[0];
       uint32_t start = T0;
       if (may_speculate) {
