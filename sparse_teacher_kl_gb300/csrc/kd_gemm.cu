@@ -504,9 +504,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
               sbuf ^= 1u;
             }
           } else if (EPI == EPI_ACCUM) {
-            // C[row, col0 .. col0+31] += acc with fire-and-forget vector reductions: the
-            // read-modify-write happens in L2, nothing waits on it, and the TMA unit stays
-            // free for the operand loads.  Each element gets exactly one addition per launch.
+            // C[row, col0 .. col0+31] += acc, each element exactly one addition per launch, as
+            // a read-modify-write in L2 that nothing waits on.
             if (p.K <= ACCUM_STAGED_MAX_K) {
               // A shallow reduction leaves the launch bound by this read-modify-write: the
               // warp's 32 x 32 block goes to shared memory (two alternating 4 KB boxes, 128-byte
@@ -526,6 +525,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 bulk_commit();
               }
             } else if (row < p.M) {
+              // deeper: fire-and-forget vector reductions of the thread's own row, which leave
+              // the TMA unit to the operand loads
               float* dst = reinterpret_cast<float*>(p.C) + size_t(row) * p.ldc + col0;
 #pragma unroll
               for (int g4 = 0; g4 < 8; ++g4) {
